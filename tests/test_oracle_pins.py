@@ -1,0 +1,398 @@
+"""Pins for the CPU oracle: each check rests on something other than the
+oracle's own code -- hand-worked examples of the pages' rules, library
+routines (torch rounding / float8 casts, numpy binary16), exhaustive
+neighbour enumeration, closed forms, error bounds, invariants and a
+brute-force dense attention written here from the definition.
+
+CPU only (no GPU marker)."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import kvq_inputs as inp
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16(values):
+    return inp.to_bf16_bits(np.asarray(values, np.float32))
+
+
+# ---------------------------------------------------------------- INT8 ----
+def _golden_int8():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "int8_rows.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        xs, cs, sc = line.split("|")
+        rows.append(([float(t) for t in xs.split()], [int(t) for t in cs.split()], float(sc)))
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_int8())
+def test_int8_hand_examples(row):
+    xs, codes, scale = row
+    x = bf16(xs)
+    assert np.array_equal(inp.bf16_bits_to_float(x), np.float32(xs)), "fixture must be bf16-exact"
+    c, s = oracle.quant_int8_row(x)
+    assert c.tolist() == codes
+    assert s == np.float32(scale)
+
+
+def test_int8_matches_torch_restatement_of_worked_function():
+    """The worked INT8 function of the page, evaluated with torch CPU (IEEE
+    fp32 division, torch.round = half-to-even) per (token, head) row."""
+    r = np.random.default_rng(11)
+    for trial in range(300):
+        n = [64, 128][trial % 2]
+        x = (r.standard_normal(n) * r.choice([1e-3, 1.0, 30.0])).astype(np.float32)
+        if trial % 7 == 0:
+            x[r.integers(n)] *= 50
+        xb = bf16(x)
+        t = torch.from_numpy(inp.bf16_bits_to_float(xb))
+        abs_max = t.abs().max()
+        scale = abs_max / 127.0
+        ref = torch.round(t / scale).clamp(-127, 127).to(torch.int8).numpy()
+        c, s = oracle.quant_int8_row(xb)
+        assert np.float32(s) == scale.item()
+        assert np.array_equal(c, ref)
+
+
+def test_int8_round_trip_bound_and_extremes():
+    r = np.random.default_rng(12)
+    for _ in range(200):
+        x = bf16(r.standard_normal(128).astype(np.float32) * 3)
+        xf = inp.bf16_bits_to_float(x).astype(np.float64)
+        c, s = oracle.quant_int8_row(x)
+        err = np.abs(xf - c.astype(np.float64) * s)
+        # |x/s| <= 127 is rounded once in fp32 (at most 128 * 2^-24 code
+        # units) before the half-unit rounding to an integer code
+        assert err.max() <= s * (0.5 + 128 * 2.0 ** -24)
+        assert np.abs(c).max() == 127          # the absmax element lands on qmax
+        assert c.min() >= -127                 # -128 never occurs
+
+
+# ---------------------------------------------------------------- E4M3 ----
+def _golden_e4m3():
+    dec, enc = [], []
+    for line in open(os.path.join(GOLDEN, "e4m3_codes.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = line.split()
+        if parts[0] == "encode":
+            enc.append((float(parts[1]), int(parts[2], 16)))
+        else:
+            dec.append((float(parts[0]), int(parts[1], 16)))
+    return dec, enc
+
+
+def test_e4m3_hand_values():
+    dec, enc = _golden_e4m3()
+    for v, c in dec:
+        assert oracle.e4m3_value(c) == v
+        assert oracle.e4m3_encode(v) == c
+    for v, c in enc:
+        assert oracle.e4m3_encode(v) == c
+    assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+
+
+def test_e4m3_all_codes_round_trip_and_midpoints():
+    vals = [oracle.e4m3_value(c) for c in range(0x7F)]
+    assert all(vals[i] < vals[i + 1] for i in range(len(vals) - 1))  # monotone magnitudes
+    for c in range(0x7F):
+        assert oracle.e4m3_encode(vals[c]) == c
+        assert oracle.e4m3_encode(-vals[c]) == (0x80 | c)
+        if c < 0x7E:
+            mid = (vals[c] + vals[c + 1]) / 2          # exact in fp32
+            want = c if c % 2 == 0 else c + 1           # tie -> even significand
+            assert oracle.e4m3_encode(mid) == want
+            lo = np.nextafter(np.float32(mid), np.float32(-1))
+            hi = np.nextafter(np.float32(mid), np.float32(1000))
+            assert oracle.e4m3_encode(float(lo)) == c
+            assert oracle.e4m3_encode(float(hi)) == c + 1
+
+
+def test_e4m3_encode_matches_torch_float8():
+    """torch's fp32 -> float8_e4m3fn cast (round-to-nearest-even; it does not
+    saturate, so the input is clamped to +-448 first)."""
+    r = np.random.default_rng(13)
+    y = np.concatenate([
+        r.standard_normal(4000).astype(np.float32) * 100,
+        r.standard_normal(2000).astype(np.float32) * 0.01,
+        (r.random(2000).astype(np.float32) - 0.5) * 1000,
+    ]).astype(np.float32)
+    ref = torch.from_numpy(np.clip(y, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(v)) for v in y], np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_fp8_row_bound():
+    r = np.random.default_rng(14)
+    for _ in range(100):
+        x = bf16(r.standard_normal(128).astype(np.float32) * 2)
+        xf = inp.bf16_bits_to_float(x).astype(np.float64)
+        c, s = oracle.quant_fp8_row(x)
+        assert s == np.float32(np.abs(inp.bf16_bits_to_float(x)).max() / np.float32(448))
+        dq = np.array([oracle.e4m3_value(int(v)) for v in c]) * s
+        # E4M3 keeps 3 fraction bits: half-spacing is 2^-4 relative (normal
+        # range) and 2^-10 absolute (subnormal range), in units of the scale.
+        bound = s * np.maximum(np.abs(xf / s) * 2.0 ** -4, 2.0 ** -10)
+        assert np.all(np.abs(xf - dq) <= bound * (1 + 1e-6))
+        assert np.max(np.abs(dq)) == pytest.approx(448 * s, rel=1e-6)
+
+
+# ---------------------------------------------------------- binary16 ----
+def _all_fp16():
+    bits = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    f = bits.view(np.float16).astype(np.float64)
+    ok = np.isfinite(f)
+    return np.unique(f[ok])  # sorted, -0 and +0 merged
+
+
+def test_fp16_directed_rounding_brute_force():
+    """Round-down / round-up against the sorted list of every finite binary16
+    value (numpy): RD(x) is the largest value <= x, RU(x) the smallest >= x."""
+    grid = _all_fp16()
+    r = np.random.default_rng(15)
+    xs = np.concatenate([
+        grid.astype(np.float32),
+        np.nextafter(grid.astype(np.float32), np.float32(np.inf)),
+        np.nextafter(grid.astype(np.float32), np.float32(-np.inf)),
+        (r.standard_normal(3000) * 10.0 ** r.integers(-9, 5, 3000)).astype(np.float32),
+    ])
+    xs = xs[np.abs(xs) <= 65504]
+    for x in xs[::7]:
+        x = float(np.float32(x))
+        i_dn = np.searchsorted(grid, x, side="right") - 1
+        i_up = np.searchsorted(grid, x, side="left")
+        rd = oracle.fp16_value(oracle.fp16_round_down(x))
+        ru = oracle.fp16_value(oracle.fp16_round_up(x))
+        assert rd == grid[i_dn], x
+        assert ru == grid[i_up], x
+        rn = float(np.float16(x))
+        assert rn in (rd, ru)
+
+
+def test_fp16_directed_overflow_and_zero_sign():
+    assert oracle.fp16_value(oracle.fp16_round_down(70000.0)) == 65504.0
+    assert math.isinf(oracle.fp16_value(oracle.fp16_round_up(70000.0)))
+    assert math.isinf(oracle.fp16_value(oracle.fp16_round_down(-70000.0)))
+    assert oracle.fp16_round_up(-1e-30) == 0x8000      # -0: IEEE sign of an inexact zero
+    assert oracle.fp16_round_down(1e-30) == 0x0000
+    assert oracle.fp16_round_down(-1e-30) == 0x8001     # away from zero: -2^-24
+
+
+# ---------------------------------------------------------------- INT4 ----
+def _golden_int4():
+    out = []
+    for line in open(os.path.join(GOLDEN, "int4_groups.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, xs, packed, sc, zp = [p.strip() for p in line.split("|")]
+        out.append((name, [float(t) for t in xs.split()], [int(t, 16) for t in packed.split()],
+                    float(sc), float(zp)))
+    return out
+
+
+@pytest.mark.parametrize("case", _golden_int4(), ids=lambda c: c[0])
+def test_int4_hand_examples(case):
+    name, xs, packed, sc, zp = case
+    p, s, z = oracle.quant_int4_row(bf16(xs), 32)
+    assert p.tolist() == packed
+    assert oracle.fp16_value(int(s[0])) == sc
+    assert oracle.fp16_value(int(z[0])) == zp
+
+
+def test_int4_bounds_and_range():
+    r = np.random.default_rng(16)
+    for _ in range(200):
+        x = bf16((r.standard_normal(128) * r.choice([0.01, 1, 40]) + r.choice([0, 5, -3])).astype(np.float32))
+        xf = inp.bf16_bits_to_float(x).astype(np.float64)
+        p, s, z = oracle.quant_int4_row(x, 32)
+        codes = np.stack([p & 15, p >> 4], axis=1).reshape(-1).astype(np.int64)
+        for gi in range(4):
+            sv, zv = oracle.fp16_value(int(s[gi])), oracle.fp16_value(int(z[gi]))
+            g = slice(32 * gi, 32 * gi + 32)
+            assert zv <= xf[g].min()                                 # zero-point below the minimum
+            assert zv + 15 * sv >= xf[g].max() - 1e-6 * abs(xf[g].max())  # top code reaches the maximum
+            dq = codes[g] * sv + zv
+            assert np.all(np.abs(xf[g] - dq) <= sv / 2 * (1 + 1e-3) + 1e-7)
+
+
+# ------------------------------------------------------------ attention ----
+def dense_dequant(cache: oracle.OracleCache, kv: int, rows: np.ndarray) -> np.ndarray:
+    """Dequantize pool rows with this test's own reading of the layout and
+    torch / numpy number formats (independent of the oracle's decoder)."""
+    D = cache.head_dim
+    codes = (cache.k_codes if kv == 0 else cache.v_codes)
+    scales = (cache.k_scales if kv == 0 else cache.v_scales)
+    if cache.scheme == "int8":
+        c = codes.reshape(-1, D)[rows].view(np.int8).astype(np.float64)
+        return c * scales[rows][:, None].astype(np.float64)
+    if cache.scheme == "fp8":
+        c = codes.reshape(-1, D)[rows]
+        v = torch.from_numpy(np.ascontiguousarray(c)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        return v * scales[rows][:, None].astype(np.float64)
+    zeros = cache.k_zeros if kv == 0 else cache.v_zeros
+    ng = D // cache.group
+    pk = codes.reshape(-1, D // 2)[rows]
+    c = np.stack([pk & 15, pk >> 4], axis=-1).reshape(len(rows), D).astype(np.float64)
+    s = scales.reshape(-1, ng)[rows].view(np.float16).astype(np.float64)
+    z = zeros.reshape(-1, ng)[rows].view(np.float16).astype(np.float64)
+    return c * np.repeat(s, cache.group, axis=1) + np.repeat(z, cache.group, axis=1)
+
+
+def brute_attention(cache, q_bits, bt, lens, Hq):
+    """softmax(q K^T / sqrt(d)) V in fp64 over densely gathered rows."""
+    H, D, P = cache.num_kv_heads, cache.head_dim, cache.page_size
+    G = Hq // H
+    q = inp.bf16_bits_to_float(q_bits).astype(np.float64).reshape(len(lens), Hq, D)
+    out = np.zeros((len(lens), Hq, D))
+    for b, L in enumerate(lens):
+        if L == 0:
+            continue
+        t = np.arange(L)
+        for hq in range(Hq):
+            h = hq // G
+            rows = (bt[b, t // P].astype(np.int64) * H + h) * P + t % P
+            K = dense_dequant(cache, 0, rows)
+            V = dense_dequant(cache, 1, rows)
+            s = K @ q[b, hq] / math.sqrt(D)
+            p = np.exp(s - s.max())
+            out[b, hq] = p @ V / p.sum()
+    return out
+
+
+def _build(scheme, lens, Hq, H, D, P, seed, spare=3):
+    w = inp.Workload(0, "t", scheme, 1, len(lens), Hq, H, D, P, ("fixed", 0), seed=seed,
+                     outlier_pairs=2, outlier_gain=6.0)
+    bt, npg = inp.page_table(np.asarray(lens), P, seed, spare=spare)
+    cache = oracle.OracleCache(scheme, npg, P, H, D)
+    for b, L in enumerate(lens):
+        k, v = inp.kv_rows(w, 0, b, 0, L)
+        assert cache.append(inp.slots(bt, b, np.arange(L), P), k, v) == 0
+    q = inp.queries(w, 0)
+    return w, cache, bt, q
+
+
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4"])
+def test_decode_matches_brute_force(scheme):
+    lens = np.array([1, 17, 40, 0, 33], np.int32)
+    w, cache, bt, q = _build(scheme, lens, Hq=8, H=2, D=64, P=16, seed=21)
+    got = cache.decode_attn(q, bt, lens, 8)
+    ref = brute_attention(cache, q, bt, lens, 8)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    assert np.all(got[3] == 0)
+
+
+def test_decode_page_permutation_invariance():
+    lens = np.array([50, 64, 7], np.int32)
+    w, cache, bt, q = _build("int8", lens, Hq=4, H=2, D=64, P=16, seed=22)
+    ref = cache.decode_attn(q, bt, lens, 4)
+    # move every page to a new physical id
+    perm = np.random.default_rng(5).permutation(cache.num_pages).astype(np.int32)
+    c2 = oracle.OracleCache("int8", cache.num_pages, 16, 2, 64)
+    rows_per_page = 2 * 16
+    for old in range(cache.num_pages):
+        new = perm[old]
+        for name in ("k_codes", "v_codes"):
+            src = getattr(cache, name).reshape(cache.num_pages, -1)
+            getattr(c2, name).reshape(cache.num_pages, -1)[new] = src[old]
+        for name in ("k_scales", "v_scales"):
+            src = getattr(cache, name).reshape(cache.num_pages, rows_per_page)
+            getattr(c2, name).reshape(cache.num_pages, rows_per_page)[new] = src[old]
+    bt2 = np.where(bt >= 0, perm[np.maximum(bt, 0)], -1).astype(np.int32)
+    got = c2.decode_attn(q, bt2, lens, 4)
+    assert np.array_equal(got, ref)
+
+
+def test_decode_closed_forms():
+    # one cached token: the output is that token's dequantized value row
+    lens = np.array([1], np.int32)
+    w, cache, bt, q = _build("fp8", lens, Hq=4, H=1, D=64, P=16, seed=23)
+    got = cache.decode_attn(q, bt, lens, 4)
+    v0 = dense_dequant(cache, 1, np.array([bt[0, 0] * 16]))[0]
+    for hq in range(4):
+        assert np.array_equal(got[0, hq], v0)
+    # identical keys: uniform weights, the output is the mean of the values
+    L, H, D, P = 37, 1, 64, 16
+    bt, npg = inp.page_table(np.array([L]), P, 3)
+    cache = oracle.OracleCache("int8", npg, P, H, D)
+    r = np.random.default_rng(9)
+    krow = inp.to_bf16_bits(r.standard_normal(D).astype(np.float32))
+    k = np.tile(krow, (L, 1)).reshape(L, H, D)
+    v = inp.to_bf16_bits(r.standard_normal((L, H, D)).astype(np.float32))
+    cache.append(inp.slots(bt, 0, np.arange(L), P), k, v)
+    qb = inp.to_bf16_bits(r.standard_normal((1, 2, D)).astype(np.float32))
+    got = cache.decode_attn(qb, bt, np.array([L], np.int32), 2)
+    rows = bt[0, np.arange(L) // P].astype(np.int64) * P + np.arange(L) % P
+    mean_v = dense_dequant(cache, 1, rows).mean(axis=0)
+    np.testing.assert_allclose(got[0, 0], mean_v, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(got[0, 1], mean_v, rtol=0, atol=1e-13)
+
+
+def test_append_skips_negative_slots_and_rejects_out_of_pool():
+    cache = oracle.OracleCache("int8", 2, 16, 1, 64)
+    k = bf16(np.ones((2, 1, 64)))
+    assert cache.append(np.array([-1, 3], np.int64), k, k) == 0
+    assert np.all(cache.k_codes.reshape(-1, 64)[3] == 127)
+    assert np.all(cache.k_codes.reshape(-1, 64)[0] == 0)
+    assert cache.append(np.array([32, 0], np.int64), k, k) == -1
+
+
+# ------------------------------------------------------------ byte counts ----
+def test_bytes_per_token_printed_figures():
+    for line in open(os.path.join(GOLDEN, "bytes_per_token.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = line.split()
+        if parts[0] == "context":
+            ctx, bits, gb, tol = int(parts[1]), int(parts[2]), float(parts[3]), float(parts[4])
+            total = oracle.kv_bytes_per_token(80, 8, 128, bits) * ctx
+            assert abs(total / 1e9 - gb) <= tol * gb
+            # the page's 64 (query) heads would give 8x that, far from the figure
+            assert oracle.kv_bytes_per_token(80, 64, 128, bits) * ctx / 1e9 > 5 * gb
+        else:
+            bits, kb = int(parts[0]), float(parts[1])
+            assert oracle.kv_bytes_per_token(80, 8, 128, bits) == kb * 1000
+    # 2x at INT8 and 4x at INT4 versus 16-bit ("KV Cache Optimization: Strategies
+    # for Faster LLM Inference", section "KV Cache Quantization: When and How to
+    # Compress"), codes only
+    b16 = oracle.kv_bytes_per_token(80, 8, 128, 16)
+    assert b16 / oracle.kv_bytes_per_token(80, 8, 128, 8) == 2
+    assert b16 / oracle.kv_bytes_per_token(80, 8, 128, 4) == 4
+    # per-layer overhead stated separately: fp32 scale per token-head; INT4
+    # fp16 scale + zero per 32-channel group
+    assert oracle.scale_bytes_per_token(1, 8, 128, "int8") == 64
+    assert oracle.scale_bytes_per_token(1, 8, 128, "int4") == 256
+
+
+# ------------------------------------------------------------ allocator ----
+def test_splitmix64_published_vector():
+    # SplitMix64 seeded with 1234567: the test vector published with the
+    # generator's reference implementation.
+    assert oracle.splitmix64_stream(1234567, 5) == [
+        6457827717110365317, 3203168211198807973, 9817491932198370423,
+        4593380528125082431, 16408922859458223821]
+
+
+def test_free_list_is_uniform_permutation():
+    for n in (1, 2, 17, 1000):
+        fl = oracle.free_list(n, 99)
+        assert sorted(fl.tolist()) == list(range(n))
+    # every permutation of 3 pages is reachable with near-equal frequency
+    # (Sattolo's off-by-one would never give the identity)
+    counts = {}
+    for seed in range(6000):
+        key = tuple(oracle.free_list(3, seed).tolist())
+        counts[key] = counts.get(key, 0) + 1
+    assert len(counts) == 6
+    assert min(counts.values()) > 800
