@@ -1,0 +1,239 @@
+"""Dynamic KV-cache quantization with fused-dequantization paged decode
+attention for NVIDIA GB300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/kvq.h`` (``libkvq.so``, built
+in-tree by ``build.py``).  This module only marshals arguments: torch tensors
+are passed as raw device pointers with the current CUDA stream; every step of
+the computation runs in the library's CUDA kernels.  There is no CPU
+fallback: if the library is missing, importing this package raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+INT8, FP8, INT4 = 1, 2, 3
+SCHEMES = {"int8": INT8, "fp8": FP8, "int4": INT4}
+
+OK = 0
+STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_SCHEME_MISMATCH",
+                3: "KVQ_ERR_OUT_OF_PAGES", 4: "KVQ_ERR_BAD_TABLE", 5: "KVQ_ERR_CUDA",
+                6: "KVQ_ERR_DEVICE_TIMEOUT", 7: "KVQ_ERR_UNSUPPORTED", 8: "KVQ_ERR_WORKSPACE"}
+
+# Every function the header declares (checked against include/kvq.h by the tests).
+EXPORTS = ["kvq_status_string", "kvq_cache_bytes", "kvq_append", "kvq_decode_workspace_bytes",
+           "kvq_decode_attn", "kvq_decode_partial", "kvq_decode_merge", "kvq_validate_tables",
+           "kvq_last_device_error", "kvq_allocator_create", "kvq_allocator_destroy",
+           "kvq_alloc_pages", "kvq_free_pages", "kvq_allocator_free_count"]
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+class CacheStruct(ctypes.Structure):
+    _fields_ = [("scheme", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+                ("k_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
+                ("k_zeros", ctypes.c_void_p), ("v_zeros", ctypes.c_void_p)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built: run `python dynamically_quantized_paged_gb300/build.py` "
+                          "(or __graft_entry__.build()); there is no fallback path")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64p = ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p
+    cachep = ctypes.POINTER(CacheStruct)
+    sz = ctypes.POINTER(ctypes.c_size_t)
+    L.kvq_status_string.argtypes, L.kvq_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+    L.kvq_cache_bytes.argtypes = [i32, i32, i32, i32, i32, sz, sz, sz]
+    L.kvq_append.argtypes = [cachep, P, i32, i32, i64p, P, P, i32, i32, P]
+    L.kvq_decode_workspace_bytes.argtypes = [cachep, i32, i32, i32, sz]
+    dec = [cachep, P, P, P, P, i32, i32, i32, ctypes.c_float, P, ctypes.c_size_t, P]
+    L.kvq_decode_attn.argtypes = dec
+    L.kvq_decode_partial.argtypes = dec
+    L.kvq_decode_merge.argtypes = dec
+    L.kvq_validate_tables.argtypes = [cachep, P, P, i32, i32, P]
+    L.kvq_last_device_error.argtypes = [P]
+    L.kvq_allocator_create.argtypes, L.kvq_allocator_create.restype = [i32, ctypes.c_uint64], P
+    L.kvq_allocator_destroy.argtypes, L.kvq_allocator_destroy.restype = [P], None
+    L.kvq_alloc_pages.argtypes = [P, i32, P]
+    L.kvq_free_pages.argtypes = [P, i32, P]
+    L.kvq_allocator_free_count.argtypes, L.kvq_allocator_free_count.restype = [P], i32
+    for name in EXPORTS:
+        getattr(L, name)  # every declared entry point must be exported
+    return L
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.kvq_status_string(status).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise KvqError(status, what)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        if not torch.cuda.is_available():
+            return None
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream) if hasattr(stream, "cuda_stream") else stream
+
+
+def cache_bytes(scheme: str | int, num_pages: int, page_size: int, num_kv_heads: int,
+                head_dim: int) -> tuple[int, int, int]:
+    """(code_bytes, scale_bytes, zero_bytes) of one K (or V) pool."""
+    sid = SCHEMES.get(scheme, scheme)
+    c, s, z = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib.kvq_cache_bytes(sid, num_pages, page_size, num_kv_heads, head_dim,
+                               ctypes.byref(c), ctypes.byref(s), ctypes.byref(z)), "kvq_cache_bytes")
+    return c.value, s.value, z.value
+
+
+class PagedKVCache:
+    """One layer's paged quantized cache: six caller-owned device pools (torch
+    uint8 tensors) laid out as include/kvq.h describes."""
+
+    def __init__(self, scheme: str, num_pages: int, page_size: int, num_kv_heads: int,
+                 head_dim: int, device="cuda", zero_init: bool = True):
+        self.scheme = scheme
+        self.sid = SCHEMES[scheme]
+        self.num_pages, self.page_size = num_pages, page_size
+        self.num_kv_heads, self.head_dim = num_kv_heads, head_dim
+        self.group = 32 if scheme == "int4" else 0
+        cb, sb, zb = cache_bytes(scheme, num_pages, page_size, num_kv_heads, head_dim)
+        alloc = torch.zeros if zero_init else torch.empty
+        self.k_codes = alloc(cb, dtype=torch.uint8, device=device)
+        self.v_codes = alloc(cb, dtype=torch.uint8, device=device)
+        self.k_scales = alloc(sb, dtype=torch.uint8, device=device)
+        self.v_scales = alloc(sb, dtype=torch.uint8, device=device)
+        self.k_zeros = alloc(zb, dtype=torch.uint8, device=device) if zb else None
+        self.v_zeros = alloc(zb, dtype=torch.uint8, device=device) if zb else None
+        self.struct = CacheStruct(self.sid, num_pages, page_size, num_kv_heads, head_dim, self.group,
+                                  self.k_codes.data_ptr(), self.v_codes.data_ptr(),
+                                  self.k_scales.data_ptr(), self.v_scales.data_ptr(),
+                                  self.k_zeros.data_ptr() if zb else None,
+                                  self.v_zeros.data_ptr() if zb else None)
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() for t in (self.k_codes, self.v_codes, self.k_scales, self.v_scales,
+                                       self.k_zeros, self.v_zeros) if t is not None)
+
+
+def append(cache: PagedKVCache, slot_mapping: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+           block_table: torch.Tensor | None = None, stream=None) -> None:
+    """kvq_append: quantize bf16 k, v [T, Hkv, d] into the slots slot_mapping
+    (int64 [T]) of the cache."""
+    T = slot_mapping.numel()
+    B, maxp = (block_table.shape[0], block_table.shape[1]) if block_table is not None else (0, 1)
+    _check(lib.kvq_append(ctypes.byref(cache.struct), _ptr(block_table), B, maxp, _ptr(slot_mapping),
+                          _ptr(k), _ptr(v), T, cache.sid, _stream(stream)), "kvq_append")
+
+
+def decode_workspace_bytes(cache: PagedKVCache, num_seqs: int, num_q_heads: int,
+                           max_pages_per_seq: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib.kvq_decode_workspace_bytes(ctypes.byref(cache.struct), num_seqs, num_q_heads,
+                                          max_pages_per_seq, ctypes.byref(n)),
+           "kvq_decode_workspace_bytes")
+    return n.value
+
+
+def alloc_workspace(cache: PagedKVCache, num_seqs: int, num_q_heads: int, max_pages_per_seq: int,
+                    device="cuda") -> torch.Tensor:
+    n = decode_workspace_bytes(cache, num_seqs, num_q_heads, max_pages_per_seq)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _decode_call(fn, name, cache, q, block_table, seq_lens, out, workspace, softmax_scale, stream):
+    B, Hq, _ = q.shape
+    _check(fn(ctypes.byref(cache.struct), _ptr(q), _ptr(block_table), _ptr(seq_lens), _ptr(out), B, Hq,
+              block_table.shape[1], float(softmax_scale), _ptr(workspace), workspace.numel(),
+              _stream(stream)), name)
+
+
+def decode_attn(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                seq_lens: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+    """kvq_decode_attn: out[B, Hq, d] (fp32) = paged GQA decode attention of
+    q[B, Hq, d] (bf16) over the quantized cache."""
+    _decode_call(lib.kvq_decode_attn, "kvq_decode_attn", cache, q, block_table, seq_lens, out,
+                 workspace, softmax_scale, stream)
+    return out
+
+
+def decode_partial(cache, q, block_table, seq_lens, out, workspace, softmax_scale=0.0, stream=None):
+    _decode_call(lib.kvq_decode_partial, "kvq_decode_partial", cache, q, block_table, seq_lens, out,
+                 workspace, softmax_scale, stream)
+
+
+def decode_merge(cache, q, block_table, seq_lens, out, workspace, softmax_scale=0.0, stream=None):
+    _decode_call(lib.kvq_decode_merge, "kvq_decode_merge", cache, q, block_table, seq_lens, out,
+                 workspace, softmax_scale, stream)
+
+
+def validate_tables(cache: PagedKVCache, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                    stream=None) -> None:
+    _check(lib.kvq_validate_tables(ctypes.byref(cache.struct), _ptr(block_table), _ptr(seq_lens),
+                                   block_table.shape[0], block_table.shape[1], _stream(stream)),
+           "kvq_validate_tables")
+
+
+def last_device_error(stream=None) -> int:
+    """Synchronizes the stream; returns (and clears) the device error status."""
+    return lib.kvq_last_device_error(_stream(stream))
+
+
+class PageAllocator:
+    """Host page allocator (kvq_allocator_*): scattered page ids handed out on
+    demand from a seeded shuffled free list."""
+
+    def __init__(self, num_pages: int, seed: int = 0):
+        self._h = lib.kvq_allocator_create(num_pages, seed)
+        if not self._h:
+            raise KvqError(1, "kvq_allocator_create")
+        self.num_pages = num_pages
+
+    def alloc(self, n: int) -> list[int]:
+        out = (ctypes.c_int32 * max(n, 1))()
+        _check(lib.kvq_alloc_pages(self._h, n, out), "kvq_alloc_pages")
+        return list(out[:n])
+
+    def free(self, pages) -> None:
+        arr = (ctypes.c_int32 * max(len(pages), 1))(*pages)
+        _check(lib.kvq_free_pages(self._h, len(pages), arr), "kvq_free_pages")
+
+    @property
+    def free_count(self) -> int:
+        return lib.kvq_allocator_free_count(self._h)
+
+    def close(self) -> None:
+        if self._h:
+            lib.kvq_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,397 @@
+// kvq_api.cu -- the C ABI declared in include/kvq.h: argument checks on the
+// host, dispatch to the kernels, the per-device error word, and the host page
+// allocator.  Nothing here allocates device memory.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+// Per-device error word written by the kernels (atomicOr of kvq::ERR_* bits).
+__device__ unsigned g_error_word;
+
+std::mutex g_mu;
+unsigned* g_err_ptr[MAX_DEVICES];
+int g_sm_count[MAX_DEVICES];
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return -1;
+    return dev;
+}
+
+kvq_status check_cache(const kvq_cache* c) {
+    if (!c) return KVQ_ERR_INVALID_ARG;
+    if (c->scheme < KVQ_INT8_SYM_TOKEN || c->scheme > KVQ_INT4_ASYM_G32) return KVQ_ERR_INVALID_ARG;
+    if (c->num_pages < 1 || c->page_size < 1 || c->num_kv_heads < 1 || c->head_dim < 1)
+        return KVQ_ERR_INVALID_ARG;
+    if (c->page_size % kvq::UNIT != 0) return KVQ_ERR_UNSUPPORTED;
+    if (c->head_dim != 64 && c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+    if (c->scheme == KVQ_INT4_ASYM_G32 && c->group != 32) return KVQ_ERR_UNSUPPORTED;
+    const void* need[4] = {c->k_codes, c->v_codes, c->k_scales, c->v_scales};
+    for (const void* p : need)
+        if (!p || !aligned(p, 16)) return KVQ_ERR_INVALID_ARG;
+    if (c->scheme == KVQ_INT4_ASYM_G32) {
+        if (!c->k_zeros || !c->v_zeros || !aligned(c->k_zeros, 16) || !aligned(c->v_zeros, 16))
+            return KVQ_ERR_INVALID_ARG;
+    }
+    // the pool must be addressable with 64-bit row arithmetic and int32 page ids
+    const int64_t rows = (int64_t)c->num_pages * c->num_kv_heads * c->page_size;
+    if (rows <= 0 || rows > ((int64_t)1 << 40)) return KVQ_ERR_INVALID_ARG;
+    return KVQ_OK;
+}
+
+kvq::CacheView view_of(const kvq_cache* c) {
+    kvq::CacheView v;
+    v.scheme = c->scheme;
+    v.num_pages = c->num_pages;
+    v.page_size = c->page_size;
+    v.num_kv_heads = c->num_kv_heads;
+    v.head_dim = c->head_dim;
+    v.group = c->group;
+    v.k_codes = static_cast<const uint8_t*>(c->k_codes);
+    v.v_codes = static_cast<const uint8_t*>(c->v_codes);
+    v.k_scales = c->k_scales;
+    v.v_scales = c->v_scales;
+    v.k_zeros = c->k_zeros;
+    v.v_zeros = c->v_zeros;
+    return v;
+}
+
+int gqa_ratio(const kvq_cache* c, int32_t Hq) {
+    if (Hq < 1 || Hq % c->num_kv_heads != 0) return -1;
+    const int G = Hq / c->num_kv_heads;
+    return (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
+}
+
+int n_ctas_for_device() { return kvq::device_sm_count() * kvq::DECODE_CTAS_PER_SM; }
+
+// Shared argument checks of the three decode entry points; fills p.
+kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                          const int32_t* seq_lens, float* out, int32_t B, int32_t Hq,
+                          int32_t max_pages, float softmax_scale, void* workspace,
+                          size_t workspace_bytes, kvq::DecodeParams& p, int& G) {
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    if (B < 0 || B > kvq::MAX_SEQS || max_pages < 1) return KVQ_ERR_INVALID_ARG;
+    G = gqa_ratio(cache, Hq);
+    if (G < 0) return KVQ_ERR_INVALID_ARG;
+    if (G == 0) return KVQ_ERR_UNSUPPORTED;
+    if (B == 0) return KVQ_OK;
+    if (!q || !block_table || !seq_lens || !out || !workspace) return KVQ_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return KVQ_ERR_INVALID_ARG;
+    // all per-head unit counts must fit int32 (the plan's prefix sums)
+    const int64_t units_per_seq = ((int64_t)max_pages * cache->page_size + kvq::UNIT - 1) / kvq::UNIT;
+    if (units_per_seq * B * cache->num_kv_heads >= ((int64_t)1 << 31)) return KVQ_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0) return KVQ_ERR_CUDA;
+    const int n_ctas = n_ctas_for_device();
+    if (n_ctas <= 0) return KVQ_ERR_CUDA;
+    const size_t need = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, B);
+    if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+    unsigned* err = kvq::device_error_word();
+    if (!err) return KVQ_ERR_CUDA;
+    const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)cache->head_dim);
+    p.c = view_of(cache);
+    p.q = static_cast<const uint16_t*>(q);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_m = p.ws_o + (size_t)2 * n_ctas * G * cache->head_dim;
+    p.ws_l = p.ws_m + (size_t)2 * n_ctas * G;
+    p.B = B;
+    p.Hq = Hq;
+    p.max_pages = max_pages;
+    p.n_ctas = n_ctas;
+    p.q_scale = scale * 1.4426950408889634f;  // log2(e): the kernel works in base 2
+    p.err = err;
+    return KVQ_OK;
+}
+
+}  // namespace
+
+namespace kvq {
+
+unsigned* device_error_word() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+    }
+    return g_err_ptr[dev];
+}
+
+int device_sm_count() {
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+}  // namespace kvq
+
+struct kvq_allocator {
+    int32_t num_pages;
+    std::vector<int32_t> stack;   // free pages; allocation pops from the back
+    std::vector<uint8_t> is_free;
+};
+
+extern "C" {
+
+const char* kvq_status_string(kvq_status s) {
+    switch (s) {
+        case KVQ_OK: return "ok";
+        case KVQ_ERR_INVALID_ARG: return "invalid argument";
+        case KVQ_ERR_SCHEME_MISMATCH: return "scheme does not match the cache";
+        case KVQ_ERR_OUT_OF_PAGES: return "out of pages";
+        case KVQ_ERR_BAD_TABLE: return "page, slot or sequence length outside the pool";
+        case KVQ_ERR_CUDA: return "CUDA error";
+        case KVQ_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case KVQ_ERR_UNSUPPORTED: return "unsupported shape";
+        case KVQ_ERR_WORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+kvq_status kvq_cache_bytes(int32_t scheme, int32_t num_pages, int32_t page_size,
+                           int32_t num_kv_heads, int32_t head_dim, size_t* code_bytes,
+                           size_t* scale_bytes, size_t* zero_bytes) {
+    if (scheme < KVQ_INT8_SYM_TOKEN || scheme > KVQ_INT4_ASYM_G32) return KVQ_ERR_INVALID_ARG;
+    if (num_pages < 1 || page_size < 1 || num_kv_heads < 1 || head_dim < 1) return KVQ_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+    const size_t rows = (size_t)num_pages * num_kv_heads * page_size;
+    const bool int4 = scheme == KVQ_INT4_ASYM_G32;
+    if (code_bytes) *code_bytes = rows * (int4 ? head_dim / 2 : head_dim);
+    if (scale_bytes) *scale_bytes = rows * (int4 ? (head_dim / 32) * 2 : 4);
+    if (zero_bytes) *zero_bytes = int4 ? rows * (head_dim / 32) * 2 : 0;
+    return KVQ_OK;
+}
+
+kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_t num_seqs,
+                      int32_t max_pages_per_seq, const int64_t* slot_mapping, const void* k,
+                      const void* v, int32_t num_tokens, int32_t scheme, kvq_stream_t stream) {
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    if (scheme != cache->scheme) return KVQ_ERR_SCHEME_MISMATCH;
+    if (num_tokens < 0) return KVQ_ERR_INVALID_ARG;
+    if (block_table && (num_seqs < 0 || max_pages_per_seq < 1 || !aligned(block_table, 4)))
+        return KVQ_ERR_INVALID_ARG;
+    if (num_tokens > 0) {
+        if (!slot_mapping || !k || !v || !aligned(slot_mapping, 8) || !aligned(k, 16) ||
+            !aligned(v, 16))
+            return KVQ_ERR_INVALID_ARG;
+    }
+    if (num_tokens == 0 && !(block_table && num_seqs > 0)) return KVQ_OK;
+    unsigned* err = kvq::device_error_word();
+    if (!err) return KVQ_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (block_table && num_seqs > 0) {
+        if (kvq::launch_validate(view_of(cache), block_table, nullptr, num_seqs, max_pages_per_seq,
+                                 err, s) != cudaSuccess)
+            return KVQ_ERR_CUDA;
+    }
+    if (num_tokens == 0) return KVQ_OK;
+    kvq::AppendParams p;
+    p.k_codes = static_cast<uint8_t*>(cache->k_codes);
+    p.v_codes = static_cast<uint8_t*>(cache->v_codes);
+    p.k_scales = cache->k_scales;
+    p.v_scales = cache->v_scales;
+    p.k_zeros = cache->k_zeros;
+    p.v_zeros = cache->v_zeros;
+    p.slot_mapping = slot_mapping;
+    p.k = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.num_slots = (int64_t)cache->num_pages * cache->page_size;
+    p.num_tokens = num_tokens;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.page_size = cache->page_size;
+    p.err = err;
+    if (kvq::launch_append(p, cache->scheme, cache->head_dim, s) != cudaSuccess) return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t max_pages_per_seq,
+                                      size_t* bytes) {
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    if (!bytes || num_seqs < 0 || num_seqs > kvq::MAX_SEQS || max_pages_per_seq < 1)
+        return KVQ_ERR_INVALID_ARG;
+    const int G = gqa_ratio(cache, num_q_heads);
+    if (G < 0) return KVQ_ERR_INVALID_ARG;
+    if (G == 0) return KVQ_ERR_UNSUPPORTED;
+    const int n_ctas = n_ctas_for_device();
+    if (n_ctas <= 0) return KVQ_ERR_CUDA;
+    *bytes = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, num_seqs);
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_partial(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                              const int32_t* seq_lens, float* out, int32_t num_seqs,
+                              int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
+                              void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+    kvq::DecodeParams p;
+    int G = 0;
+    kvq_status st = prepare_decode(cache, q, block_table, seq_lens, out, num_seqs, num_q_heads,
+                                   max_pages_per_seq, softmax_scale, workspace, workspace_bytes, p, G);
+    if (st != KVQ_OK || num_seqs == 0) return st;
+    if (kvq::launch_decode_partial(p, G, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_merge(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                            const int32_t* seq_lens, float* out, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
+                            void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+    kvq::DecodeParams p;
+    int G = 0;
+    kvq_status st = prepare_decode(cache, q, block_table, seq_lens, out, num_seqs, num_q_heads,
+                                   max_pages_per_seq, softmax_scale, workspace, workspace_bytes, p, G);
+    if (st != KVQ_OK || num_seqs == 0) return st;
+    if (kvq::launch_decode_merge(p, G, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                           const int32_t* seq_lens, float* out, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
+                           void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+    kvq::DecodeParams p;
+    int G = 0;
+    kvq_status st = prepare_decode(cache, q, block_table, seq_lens, out, num_seqs, num_q_heads,
+                                   max_pages_per_seq, softmax_scale, workspace, workspace_bytes, p, G);
+    if (st != KVQ_OK || num_seqs == 0) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (kvq::launch_decode_partial(p, G, s) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (kvq::launch_decode_merge(p, G, s) != cudaSuccess) return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+kvq_status kvq_validate_tables(const kvq_cache* cache, const int32_t* block_table,
+                               const int32_t* seq_lens, int32_t num_seqs,
+                               int32_t max_pages_per_seq, kvq_stream_t stream) {
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    if (num_seqs < 0 || max_pages_per_seq < 1) return KVQ_ERR_INVALID_ARG;
+    if (num_seqs == 0) return KVQ_OK;
+    if (!block_table || !seq_lens || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return KVQ_ERR_INVALID_ARG;
+    unsigned* err = kvq::device_error_word();
+    if (!err) return KVQ_ERR_CUDA;
+    if (kvq::launch_validate(view_of(cache), block_table, seq_lens, num_seqs, max_pages_per_seq, err,
+                             reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+kvq_status kvq_last_device_error(kvq_stream_t stream) {
+    if (current_device() < 0) return KVQ_ERR_CUDA;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof v) != cudaSuccess) return KVQ_ERR_CUDA;
+    const unsigned zero = 0;
+    if (v && cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (v & kvq::ERR_TIMEOUT) return KVQ_ERR_DEVICE_TIMEOUT;
+    if (v & kvq::ERR_BAD_TABLE) return KVQ_ERR_BAD_TABLE;
+    return KVQ_OK;
+}
+
+// ---- host page allocator -------------------------------------------------------
+
+static uint64_t splitmix64(uint64_t* state) {
+    // SplitMix64 (Steele, Lea and Flood, OOPSLA 2014): golden-ratio increment,
+    // then two xor-shift-multiply mixing rounds and a final xor-shift.
+    uint64_t z = (*state += 0x9e3779b97f4a7c15ULL);
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+    return z ^ (z >> 31);
+}
+
+kvq_allocator* kvq_allocator_create(int32_t num_pages, uint64_t seed) {
+    if (num_pages < 1) return nullptr;
+    kvq_allocator* a = new (std::nothrow) kvq_allocator;
+    if (!a) return nullptr;
+    try {
+        a->num_pages = num_pages;
+        a->stack.resize(num_pages);
+        a->is_free.assign(num_pages, 1);
+    } catch (...) {
+        delete a;
+        return nullptr;
+    }
+    for (int32_t i = 0; i < num_pages; ++i) a->stack[i] = i;
+    uint64_t st = seed;
+    for (int32_t i = num_pages - 1; i >= 1; --i) {  // Fisher-Yates, Durstenfeld's order
+        const uint64_t j = splitmix64(&st) % (uint64_t)(i + 1);
+        const int32_t t = a->stack[i];
+        a->stack[i] = a->stack[j];
+        a->stack[j] = t;
+    }
+    return a;
+}
+
+void kvq_allocator_destroy(kvq_allocator* a) { delete a; }
+
+kvq_status kvq_alloc_pages(kvq_allocator* a, int32_t n, int32_t* out) {
+    if (!a || n < 0 || (n > 0 && !out)) return KVQ_ERR_INVALID_ARG;
+    if ((size_t)n > a->stack.size()) return KVQ_ERR_OUT_OF_PAGES;
+    for (int32_t i = 0; i < n; ++i) {
+        out[i] = a->stack.back();
+        a->stack.pop_back();
+        a->is_free[out[i]] = 0;
+    }
+    return KVQ_OK;
+}
+
+kvq_status kvq_free_pages(kvq_allocator* a, int32_t n, const int32_t* pages) {
+    if (!a || n < 0 || (n > 0 && !pages)) return KVQ_ERR_INVALID_ARG;
+    std::vector<uint8_t> seen;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t p = pages[i];
+        if (p < 0 || p >= a->num_pages || a->is_free[p]) return KVQ_ERR_INVALID_ARG;
+    }
+    try {
+        seen.assign(a->num_pages, 0);
+    } catch (...) {
+        return KVQ_ERR_INVALID_ARG;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        if (seen[pages[i]]) return KVQ_ERR_INVALID_ARG;
+        seen[pages[i]] = 1;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        a->stack.push_back(pages[i]);
+        a->is_free[pages[i]] = 1;
+    }
+    return KVQ_OK;
+}
+
+int32_t kvq_allocator_free_count(const kvq_allocator* a) {
+    return a ? (int32_t)a->stack.size() : 0;
+}
+
+}  // extern "C"

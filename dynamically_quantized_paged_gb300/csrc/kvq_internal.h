@@ -1,0 +1,87 @@
+// kvq_internal.h -- launch parameters and launcher entry points shared by the
+// host API (kvq_api.cu) and the kernel translation units.  Not public.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+// Bits of the per-device error word (see kvq_last_device_error).
+constexpr unsigned ERR_BAD_TABLE = 1u;
+constexpr unsigned ERR_TIMEOUT = 2u;
+
+// Tokens per pipeline stage ("unit").  Pages are a multiple of it, so a unit
+// never straddles two pages and split boundaries fall on unit boundaries.
+constexpr int UNIT = 16;
+// Decode CTA: one producer warp (bulk copies) + CONSUMER_WARPS compute warps.
+constexpr int CONSUMER_WARPS = 4;
+constexpr int DECODE_THREADS = 32 * (CONSUMER_WARPS + 1);
+constexpr int DECODE_CTAS_PER_SM = 2;
+constexpr int STAGES = 4;          // ring depth per consumer warp
+constexpr int MAX_SEQS = 4096;     // per decode call (the plan lives in shared memory)
+constexpr int MIN_SLICE_UNITS = 8; // smallest per-CTA share of the work, in units
+
+struct CacheView {
+    int scheme, num_pages, page_size, num_kv_heads, head_dim, group;
+    const uint8_t* k_codes;
+    const uint8_t* v_codes;
+    const void* k_scales;
+    const void* v_scales;
+    const void* k_zeros;
+    const void* v_zeros;
+};
+
+struct AppendParams {
+    uint8_t* k_codes;
+    uint8_t* v_codes;
+    void* k_scales;
+    void* v_scales;
+    void* k_zeros;
+    void* v_zeros;
+    const int64_t* slot_mapping;
+    const uint16_t* k;  // bf16 bits
+    const uint16_t* v;
+    int64_t num_slots;  // num_pages * page_size
+    int num_tokens, num_kv_heads, page_size;
+    unsigned* err;
+};
+
+struct DecodeParams {
+    CacheView c;
+    const uint16_t* q;  // bf16 bits [B][Hq][D]
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    float* out;
+    float* ws_o;  // [2 * n_ctas][G][D]
+    float* ws_m;  // [2 * n_ctas][G]
+    float* ws_l;  // [2 * n_ctas][G]
+    int B, Hq, max_pages;
+    int n_ctas;
+    float q_scale;  // softmax scale * log2(e), folded into q
+    unsigned* err;
+};
+
+// Workspace layout for n_ctas persistent CTAs (two partial slots each):
+// o [2 n_ctas][G][D], m [2 n_ctas][G], l [2 n_ctas][G] (fp32), then the
+// published plan: int64 U, int64 S, int32 prefix[B + 1].
+inline size_t decode_workspace_bytes(int n_ctas, int G, int D, int B) {
+    const size_t slots = 2 * (size_t)n_ctas;
+    return slots * G * D * sizeof(float) + 2 * slots * G * sizeof(float) + 16 +
+           ((size_t)B + 1) * sizeof(int32_t);
+}
+
+cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaStream_t s);
+cudaError_t launch_decode_partial(const DecodeParams& p, int G, cudaStream_t s);
+cudaError_t launch_decode_merge(const DecodeParams& p, int G, cudaStream_t s);
+cudaError_t launch_validate(const CacheView& c, const int32_t* block_table,
+                            const int32_t* seq_lens, int B, int max_pages, unsigned* err,
+                            cudaStream_t s);
+
+// Per-device error word (device address) and SM count.
+unsigned* device_error_word();
+int device_sm_count();
+
+}  // namespace kvq

@@ -1,0 +1,32 @@
+// kvq_merge.cu -- the split merge (K3) instantiations and the scheme dispatch
+// of the decode launch.
+#include "kvq_decode.cuh"
+
+namespace kvq {
+
+cudaError_t launch_decode_partial(const DecodeParams& p, int G, cudaStream_t s) {
+    switch (p.c.scheme) {
+        case KVQ_INT8_SYM_TOKEN: return launch_decode_partial_int8(p, G, s);
+        case KVQ_FP8E4M3_TOKEN: return launch_decode_partial_fp8(p, G, s);
+        default: return launch_decode_partial_int4(p, G, s);
+    }
+}
+
+cudaError_t launch_decode_merge(const DecodeParams& p, int G, cudaStream_t s) {
+    if (p.c.head_dim == 128) {
+        switch (G) {
+            case 1: return launch_decode_merge_t<128, 1>(p, s);
+            case 2: return launch_decode_merge_t<128, 2>(p, s);
+            case 4: return launch_decode_merge_t<128, 4>(p, s);
+            default: return launch_decode_merge_t<128, 8>(p, s);
+        }
+    }
+    switch (G) {
+        case 1: return launch_decode_merge_t<64, 1>(p, s);
+        case 2: return launch_decode_merge_t<64, 2>(p, s);
+        case 4: return launch_decode_merge_t<64, 4>(p, s);
+        default: return launch_decode_merge_t<64, 8>(p, s);
+    }
+}
+
+}  // namespace kvq

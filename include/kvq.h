@@ -1,0 +1,216 @@
+/*
+ * kvq.h -- dynamic KV-cache quantization with fused-dequantization paged
+ * decode attention, for NVIDIA GB300 (sm_103a).  Plain C ABI.
+ *
+ * The operations follow three web pages on the subject:
+ *  [P1] "Dynamic KV Cache Quantization for Fast LLM Inference"
+ *  [P2] "What is KV Cache Optimization? Definition, Quantization & Memory
+ *       Management in Enterprise AI?"
+ *  [P3] "KV Cache Optimization: Strategies for Faster LLM Inference"
+ * Their pipeline ([P2] section "Technical Architecture"): capture each
+ * token's key/value projections, quantize them with a dynamically computed
+ * scale, store the codes in fixed-size non-contiguous pages, and dequantize
+ * inside the attention kernel while decoding.
+ *
+ * Conventions shared by every call:
+ *  - Every pointer argument named as device memory must be device memory of
+ *    the current CUDA device, allocated and owned by the caller.  The library
+ *    allocates no device memory and keeps no pointer after a call returns.
+ *  - Device buffers must start on a 16-byte boundary (kvq_append,
+ *    kvq_decode_*: the page pools, q, k, v, out, workspace).
+ *  - Calls that launch work are asynchronous on `stream` (a cudaStream_t;
+ *    NULL is the legacy default stream) and never synchronize, except
+ *    kvq_last_device_error.
+ *  - Every call returns a kvq_status; nothing throws across the ABI.  Argument
+ *    errors are detected on the host before any launch, and then nothing is
+ *    launched.  Errors that only the device can see (a page id outside the
+ *    pool, a slot outside the pool, a sequence longer than its table row, a
+ *    wait that timed out) are recorded in a per-device flag word, the
+ *    offending access is skipped, and kvq_last_device_error reports them.
+ *  - The kernels never trap and never wait without a time limit.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kvq_stream_t; /* same type as cudaStream_t */
+
+typedef enum kvq_status {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = 1,     /* null / misaligned pointer, bad size or shape */
+    KVQ_ERR_SCHEME_MISMATCH = 2, /* scheme argument differs from cache->scheme */
+    KVQ_ERR_OUT_OF_PAGES = 3,    /* allocator exhausted ([P1]'s out-of-memory case) */
+    KVQ_ERR_BAD_TABLE = 4,       /* device saw a page / slot / length outside the pool */
+    KVQ_ERR_CUDA = 5,            /* a CUDA runtime call failed (no device, launch error) */
+    KVQ_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait ran out */
+    KVQ_ERR_UNSUPPORTED = 7,     /* valid but not implemented: head_dim, GQA ratio, page size */
+    KVQ_ERR_WORKSPACE = 8        /* workspace smaller than kvq_decode_workspace_bytes */
+} kvq_status;
+
+/* Quantization schemes ([P1] section "Understanding Dynamic Quantization
+ * Techniques for KV Caches (e.g., INT8, INT4)"; FP8 from [P2] "Technical
+ * Architecture").  All scales are computed on the fly from the data. */
+typedef enum kvq_scheme {
+    /* per (token, KV head): scale = max|x| / 127 (fp32), code = round-half-
+     * even(x / scale) in [-127, 127]; an all-zero row stores scale 1.0. */
+    KVQ_INT8_SYM_TOKEN = 1,
+    /* per (token, KV head): scale = max|x| / 448 (fp32), code = E4M3
+     * round-to-nearest-even of x / scale with saturation to +-448. */
+    KVQ_FP8E4M3_TOKEN = 2,
+    /* per (token, KV head, 32-channel group): zero = fp16 round-down of the
+     * group minimum, scale = fp16 round-up of (max - zero) / 15 (1.0 if that
+     * is 0), code = round-half-even((x - zero) / scale) in [0, 15], two codes
+     * per byte, even channel in the low nibble. */
+    KVQ_INT4_ASYM_G32 = 3
+} kvq_scheme;
+
+/* One layer of the paged quantized cache ([P1] section "Integrating Dynamic
+ * Quantization with PagedAttention ...": fixed-size blocks at scattered
+ * physical locations; [P3] section "How vLLM Implements KV Cache
+ * Optimization": 16 tokens per block by default).  All six pools are
+ * caller-owned device memory, sized by kvq_cache_bytes.  Layout:
+ *   codes   [num_pages][num_kv_heads][page_size][head_dim]    int8 / e4m3
+ *           [num_pages][num_kv_heads][page_size][head_dim/2]  INT4 (packed)
+ *   scales  [num_pages][num_kv_heads][page_size]              fp32
+ *           [num_pages][num_kv_heads][page_size][head_dim/32] fp16 (INT4)
+ *   zeros   INT4 only, same shape as its scales; NULL otherwise.
+ * The token stored at physical slot s lives in page s / page_size at
+ * offset s % page_size.  Supported: head_dim 64 or 128, page_size a positive
+ * multiple of 16, num_kv_heads >= 1.  Several layers share one block table
+ * by using one descriptor per layer. */
+typedef struct kvq_cache {
+    int32_t scheme;       /* kvq_scheme */
+    int32_t num_pages;
+    int32_t page_size;    /* tokens per page */
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t group;        /* channels per INT4 group: must be 32; ignored otherwise */
+    void* k_codes;
+    void* v_codes;
+    void* k_scales;
+    void* v_scales;
+    void* k_zeros;        /* INT4 only */
+    void* v_zeros;        /* INT4 only */
+} kvq_cache;
+
+/* Human-readable name of a status.  Never NULL; static storage. */
+const char* kvq_status_string(kvq_status status);
+
+/* Bytes of ONE of the K / V pools of each kind for the given geometry (the
+ * V pools have the same sizes).  zero_bytes is 0 for the 8-bit schemes.
+ * Per token and KV head this is head_dim code bytes (head_dim/2 for INT4)
+ * plus 4 scale bytes (INT4: 2 + 2 bytes per 32-channel group): the
+ * bytes-per-token rule of [P2] "Technical Architecture" (2 x layers x KV
+ * heads x head_dim x bytes per element) with the scale overhead separate.
+ * Host only; any output pointer may be NULL. */
+kvq_status kvq_cache_bytes(int32_t scheme, int32_t num_pages, int32_t page_size,
+                           int32_t num_kv_heads, int32_t head_dim, size_t* code_bytes,
+                           size_t* scale_bytes, size_t* zero_bytes);
+
+/* Quantize-append ([P2] "Key-Value Tensor Capture" and "Dynamic FP8/INT8
+ * Quantization"; [P1] "Understanding Dynamic Quantization Techniques").
+ *   k, v          device, bf16 [num_tokens][num_kv_heads][head_dim], the new
+ *                 tokens' key / value projections.
+ *   slot_mapping  device, int64 [num_tokens]: physical slot of each token
+ *                 (page id * page_size + offset); a negative slot skips the
+ *                 token.  A slot >= num_pages * page_size is skipped and
+ *                 flagged KVQ_ERR_BAD_TABLE.
+ *   block_table   device, int32 [num_seqs][max_pages_per_seq], or NULL.  When
+ *                 given, its entries are checked (each must be -1 or a page id
+ *                 of the pool) and violations flagged KVQ_ERR_BAD_TABLE; the
+ *                 codes are written through slot_mapping either way.
+ *   scheme        must equal cache->scheme (else KVQ_ERR_SCHEME_MISMATCH).
+ * Writes, for every token and KV head, the codes and scale (and INT4 zero)
+ * at the slot.  num_tokens == 0 launches nothing. */
+kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_t num_seqs,
+                      int32_t max_pages_per_seq, const int64_t* slot_mapping, const void* k,
+                      const void* v, int32_t num_tokens, int32_t scheme, kvq_stream_t stream);
+
+/* Device scratch needed by kvq_decode_attn / kvq_decode_partial /
+ * kvq_decode_merge for this cache geometry and query-head count on the
+ * current device (split-K partials: at most two per persistent CTA).  The
+ * size does not depend on the sequence lengths. */
+kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t max_pages_per_seq,
+                                      size_t* bytes);
+
+/* Fused-dequantization paged GQA decode attention ([P2] "Fused
+ * Dequantization Attention Kernel"; [P1] "Recap of KV Caching": the new
+ * token attends to every cached token, itself included).
+ *   q             device, bf16 [num_seqs][num_q_heads][head_dim].
+ *   block_table   device, int32 [num_seqs][max_pages_per_seq]: logical page
+ *                 i of sequence b is physical page block_table[b][i].
+ *   seq_lens      device, int32 [num_seqs]: cached tokens per sequence (0 is
+ *                 allowed and gives a zero output row).
+ *   out           device, fp32 [num_seqs][num_q_heads][head_dim].
+ *   softmax_scale <= 0 selects 1/sqrt(head_dim).
+ *   workspace     device, >= kvq_decode_workspace_bytes bytes; contents need
+ *                 no initialization and are clobbered.
+ * Query head g reads KV head g / (num_q_heads / num_kv_heads); the ratio must
+ * be 1, 2, 4 or 8.  num_seqs <= 4096.  The work is split over a persistent
+ * grid along logical token positions only, so the output does not depend on
+ * which physical pages hold the tokens.  Two launches: kvq_decode_partial then
+ * kvq_decode_merge. */
+kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                           const int32_t* seq_lens, float* out, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
+                           void* workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/* The first of kvq_decode_attn's two launches: every (sequence, KV head)
+ * whose tokens one CTA covers entirely gets its final output row; the rest
+ * leave split partials (max, sum, unnormalized output) in the workspace.
+ * Same arguments and rules as kvq_decode_attn. */
+kvq_status kvq_decode_partial(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                              const int32_t* seq_lens, float* out, int32_t num_seqs,
+                              int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
+                              void* workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/* The second launch: log-sum-exp merge of the split partials into out, and
+ * zero rows for empty sequences.  Must follow kvq_decode_partial on the same
+ * stream with the same arguments. */
+kvq_status kvq_decode_merge(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                            const int32_t* seq_lens, float* out, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
+                            void* workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/* Table check: flags KVQ_ERR_BAD_TABLE if a sequence is longer than
+ * max_pages_per_seq * page_size, or a page it uses is outside the pool. */
+kvq_status kvq_validate_tables(const kvq_cache* cache, const int32_t* block_table,
+                               const int32_t* seq_lens, int32_t num_seqs,
+                               int32_t max_pages_per_seq, kvq_stream_t stream);
+
+/* Synchronizes `stream`, then returns and clears the current device's error
+ * flags: KVQ_OK, KVQ_ERR_BAD_TABLE or KVQ_ERR_DEVICE_TIMEOUT (the latter wins
+ * when both are set), or KVQ_ERR_CUDA if the synchronization failed. */
+kvq_status kvq_last_device_error(kvq_stream_t stream);
+
+/* ---- host page allocator ([P3] "How vLLM Implements KV Cache
+ * Optimization": pages are handed out on demand, only used pages cost
+ * memory).  The free list starts as the page ids 0..num_pages-1 shuffled by
+ * Fisher-Yates driven by SplitMix64(seed), so that physical pages are
+ * scattered; allocation pops pages from the end of the list, freeing pushes
+ * them back (last freed, first reused).  Host only, not thread-safe. */
+typedef struct kvq_allocator kvq_allocator;
+
+/* NULL if num_pages < 1 or the host allocation fails. */
+kvq_allocator* kvq_allocator_create(int32_t num_pages, uint64_t seed);
+void kvq_allocator_destroy(kvq_allocator* alloc);
+/* Pops n page ids into out[0..n).  KVQ_ERR_OUT_OF_PAGES (nothing taken) if
+ * fewer than n are free. */
+kvq_status kvq_alloc_pages(kvq_allocator* alloc, int32_t n, int32_t* out);
+/* Pushes n page ids back.  KVQ_ERR_INVALID_ARG (nothing freed) if an id is
+ * outside the pool, already free, or repeated. */
+kvq_status kvq_free_pages(kvq_allocator* alloc, int32_t n, const int32_t* pages);
+int32_t kvq_allocator_free_count(const kvq_allocator* alloc);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

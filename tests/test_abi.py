@@ -1,0 +1,152 @@
+"""The C ABI on the host (no GPU needed): the library loads, exports every
+entry point include/kvq.h declares, sizes pools by the pages' bytes-per-token
+rule, checks arguments before touching the device, and its page allocator
+reproduces the oracle's seeded free list."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import dynamically_quantized_paged_gb300 as kvq
+import oracle
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kvq.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported():
+    names = declared_functions()
+    assert len(names) >= 14
+    assert sorted(kvq.EXPORTS) == names
+    lib = ctypes.CDLL(kvq.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    seen = set()
+    for s in range(9):
+        txt = kvq.status_string(s)
+        assert txt and txt not in seen
+        seen.add(txt)
+    assert kvq.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("scheme,bits", [("int8", 8), ("fp8", 8), ("int4", 4)])
+def test_cache_bytes_match_printed_bytes_per_token(scheme, bits):
+    # 80 layers, 8 KV heads, head_dim 128: K+V codes per token
+    code, scale, zero = kvq.cache_bytes(scheme, 3, 16, 8, 128)
+    per_token_layer_codes = 2 * code // (3 * 16)
+    assert per_token_layer_codes * 80 == oracle.kv_bytes_per_token(80, 8, 128, bits)
+    per_token_layer_meta = 2 * (scale + zero) // (3 * 16)
+    assert per_token_layer_meta == oracle.scale_bytes_per_token(1, 8, 128, scheme)
+
+
+def test_cache_bytes_rejects_bad_geometry():
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.cache_bytes("int8", 0, 16, 8, 128)
+    assert e.value.status == 1
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.cache_bytes("int8", 4, 16, 8, 96)
+    assert e.value.status == 7
+
+
+def test_allocator_matches_oracle_free_list_and_semantics():
+    for n, seed in ((1, 0), (10, 7), (1000, 123456789)):
+        a = kvq.PageAllocator(n, seed)
+        got = a.alloc(n)
+        assert got == oracle.free_list(n, seed)[::-1].tolist()
+        assert a.free_count == 0
+        with pytest.raises(kvq.KvqError) as e:
+            a.alloc(1)
+        assert e.value.status == 3  # out of pages: the pages' out-of-memory case
+        if n >= 3:
+            a.free(got[:3])
+            assert a.free_count == 3
+            assert a.alloc(2) == [got[2], got[1]]  # last freed, first reused
+        a.close()
+
+
+def test_allocator_rejects_bad_frees():
+    a = kvq.PageAllocator(8, 1)
+    pages = a.alloc(4)
+    for bad in ([99], [-1], [pages[0], pages[0]]):
+        with pytest.raises(kvq.KvqError):
+            a.free(bad)
+    assert a.free_count == 4  # nothing was freed by the failed calls
+    a.free(pages[:1])
+    with pytest.raises(kvq.KvqError):
+        a.free(pages[:1])  # double free
+    a.close()
+
+
+def fake_cache(scheme=1, head_dim=128, page_size=16, heads=8, align=256, group=32):
+    base = 1 << 20  # never dereferenced: argument checks run before any device access
+    p = lambda i: base + i * (1 << 16) + (0 if align >= 16 else align)
+    return kvq.CacheStruct(scheme, 4, page_size, heads, head_dim, group if scheme == 3 else 0,
+                           p(0), p(1), p(2), p(3), p(4) if scheme == 3 else None,
+                           p(5) if scheme == 3 else None)
+
+
+def call_append(c, scheme=None, T=1, k=1 << 24, v=1 << 25, slots=1 << 26):
+    return kvq.lib.kvq_append(ctypes.byref(c), None, 0, 1, slots, k, v, T,
+                              c.scheme if scheme is None else scheme, None)
+
+
+def test_append_argument_errors_before_any_launch():
+    assert kvq.lib.kvq_append(None, None, 0, 1, None, None, None, 0, 1, None) == 1
+    assert call_append(fake_cache(), scheme=2) == 2            # scheme mismatch
+    assert call_append(fake_cache(head_dim=96)) == 7           # unsupported head_dim
+    assert call_append(fake_cache(page_size=8)) == 7           # page not a multiple of 16
+    assert call_append(fake_cache(align=8)) == 1               # misaligned pool
+    assert call_append(fake_cache(scheme=3, group=64)) == 7    # INT4 group must be 32
+    assert call_append(fake_cache(), T=-1) == 1
+    assert call_append(fake_cache(), k=(1 << 24) + 2) == 1     # misaligned k
+    assert call_append(fake_cache(), T=0) == 0                 # nothing to do
+    c = fake_cache(scheme=3)
+    c.k_zeros = None
+    assert call_append(c) == 1                                 # INT4 needs zero pools
+
+
+def call_decode(c, B=2, Hq=32, maxp=4, ws_bytes=1 << 30, q=1 << 24):
+    return kvq.lib.kvq_decode_attn(ctypes.byref(c), q, 1 << 25, 1 << 26, 1 << 27, B, Hq, maxp, 0.0,
+                                   1 << 28, ws_bytes, None)
+
+
+def test_decode_argument_errors_before_any_launch():
+    c = fake_cache()
+    assert call_decode(c, Hq=30) == 1          # not a multiple of the KV heads
+    assert call_decode(c, Hq=24) == 7          # GQA ratio 3
+    assert call_decode(c, Hq=128) == 7         # GQA ratio 16
+    assert call_decode(c, B=5000) == 1         # more sequences than one call plans for
+    assert call_decode(c, maxp=0) == 1
+    assert call_decode(c, B=0) == 0            # empty batch: nothing to do
+    assert call_decode(c, q=(1 << 24) + 4) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_device_calls_report_cuda_error_without_a_gpu():
+    c = fake_cache()
+    n = ctypes.c_size_t()
+    assert kvq.lib.kvq_decode_workspace_bytes(ctypes.byref(c), 2, 32, 4, ctypes.byref(n)) == 5
+    assert call_decode(c) == 5
+    assert call_append(fake_cache()) == 5
+    assert kvq.lib.kvq_last_device_error(None) == 5
+
+
+def test_no_oracle_in_product_path():
+    """The product package never imports or links the oracle."""
+    pkg = os.path.dirname(kvq.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(root, f)).read()
+                assert "import oracle" not in text and "liboracle" not in text and "kvq_oracle" not in text, f

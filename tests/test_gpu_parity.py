@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Codes, scales and zero-points must be bit-exact; attention must be within
+max-abs 1e-2 and mean-rel 2e-3 of the oracle's fp64 attention over the same
+dequantized cache.  Covers the five workloads at full size (sampled where the
+oracle would take minutes), ragged and degenerate shapes, tie-breaking
+inputs, page-permutation invariance and the device-side error flags."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU-only machines, never run there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import dynamically_quantized_paged_gb300 as kvq  # noqa: E402
+import kvq_inputs as inp  # noqa: E402
+import oracle  # noqa: E402
+from gpu_harness import Case, DEV, assert_attn_close, dev, dev_bits  # noqa: E402
+
+
+def small(scheme, Hq, Hkv, D, P, seed=7, outliers=2):
+    return inp.Workload(0, "edge", scheme, 1, 1, Hq, Hkv, D, P, ("fixed", 0), seed=seed,
+                        outlier_pairs=outliers, outlier_gain=8.0)
+
+
+# ------------------------------------------------------------- full workloads
+@pytest.mark.parametrize("cid", [1, 2, 5])
+def test_workload_full_parity(cid):
+    w = inp.WORKLOADS[cid]
+    case = Case(w, inp.seq_lens(w))
+    case.compare_cache(full=True)
+    got = case.decode()
+    ref = case.oracle_decode()
+    assert_attn_close(got, ref, f"workload {cid}")
+
+
+def test_workload3_fp8_70b_layer():
+    w = inp.WORKLOADS[3]
+    lens = inp.seq_lens(w)
+    r = np.random.default_rng(33)
+    sample = sorted(set(r.choice(len(lens), 6, replace=False).tolist()) | {int(np.argmax(lens)), int(np.argmin(lens))})
+    case = Case(w, lens, oracle_seqs=sample)
+    case.compare_cache(full=False)
+    got = case.decode()
+    ref = case.oracle_decode()
+    assert_attn_close(got[sample], ref, "workload 3 (sampled sequences)")
+
+
+def test_workload4_int4_eight_layers():
+    w = inp.WORKLOADS[4]
+    lens = inp.seq_lens(w)
+    for layer in range(w.layers):
+        sample = [layer % w.batch, (layer * 5 + 3) % w.batch]
+        case = Case(w, lens, layer=layer, oracle_seqs=sample)
+        case.compare_cache(full=False)
+        got = case.decode()
+        assert_attn_close(got[sample], case.oracle_decode(), f"workload 4 layer {layer}")
+        del case
+        torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------- edge cases
+SHAPES = [  # scheme, Hq, Hkv, D, P
+    ("int8", 8, 8, 64, 16), ("int8", 8, 4, 64, 16), ("int8", 16, 4, 128, 32), ("int8", 32, 4, 128, 16),
+    ("fp8", 4, 4, 128, 16), ("fp8", 16, 8, 64, 32), ("fp8", 32, 8, 128, 16), ("fp8", 8, 2, 128, 48),
+    ("int4", 8, 8, 128, 32), ("int4", 16, 8, 64, 16), ("int4", 16, 4, 128, 16), ("int4", 64, 8, 128, 32),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_ragged_and_degenerate_lengths(shape):
+    scheme, Hq, Hkv, D, P = shape
+    w = small(scheme, Hq, Hkv, D, P)
+    lens = np.array([1, 0, 17, 15, 16, 300, 2049, 33, 0, 5000, 129], np.int32)
+    case = Case(w, lens, spare=5)
+    case.compare_cache(full=True)
+    got = case.decode()
+    ref = case.oracle_decode()
+    assert_attn_close(got, ref, str(shape))
+    assert np.all(got[1] == 0) and np.all(got[8] == 0)  # empty sequences give zero rows
+
+
+def test_single_sequence_many_splits_and_custom_scale():
+    w = small("int8", 16, 2, 128, 16)
+    case = Case(w, np.array([40000], np.int32))
+    case.compare_cache(full=True)
+    for scale in (0.0, 0.05):
+        got = case.decode(softmax_scale=scale)
+        assert_attn_close(got, case.oracle_decode(softmax_scale=scale), f"scale {scale}")
+
+
+def test_page_permutation_is_bitwise_invariant():
+    w = small("fp8", 16, 4, 128, 16)
+    lens = np.array([700, 3000, 45, 1600], np.int32)
+    a = Case(w, lens, table_seed=1, oracle_seqs=[])
+    b = Case(w, lens, table_seed=2, oracle_seqs=[], spare=40)
+    assert not np.array_equal(a.bt, b.bt)
+    assert np.array_equal(a.decode(), b.decode())
+
+
+def test_two_launch_form_matches_one_call():
+    w = small("int4", 32, 4, 128, 32)
+    case = Case(w, np.array([5000, 70, 2300], np.int32), oracle_seqs=[])
+    assert np.array_equal(case.decode(), case.decode(split_calls=True))
+
+
+# ------------------------------------------------------------- crafted inputs
+def _tie_rows(scheme, D):
+    """Rows whose quotients land exactly on rounding ties."""
+    f = np.zeros((4, D), np.float32)
+    if scheme == "int8":       # absmax 127 -> scale 1: x.5 ties
+        f[:, 0] = 127.0
+        f[:, 1:] = (np.arange(1, D) % 40 - 20) + 0.5
+        f[3] = 0.0             # all-zero row: scale 1.0, zero codes
+    elif scheme == "fp8":      # absmax 448 -> scale 1: E4M3 midpoints
+        vals = np.array([oracle.e4m3_value(c) for c in range(0x7F)])
+        mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+        f[:, 0] = 448.0
+        f[:, 1:] = np.resize(np.concatenate([mids, -mids]), D - 1)
+        f[3] = 0.0
+    else:                      # INT4: constant groups, tiny minima, exact ties
+        f[0] = 0.5
+        f[1] = np.tile(np.concatenate([[-1.5, 6.0, 0.0, 0.25, 0.75, 1.25], np.full(26, 2.0)]), D // 32)
+        f[2] = np.float32(2.0 ** -30) * (np.arange(D) % 7)
+        f[3] = 0.0
+    return inp.to_bf16_bits(f)
+
+
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4"])
+def test_tie_breaking_and_zero_rows_bit_exact(scheme):
+    D, H = 128, 2
+    w = small(scheme, 4, H, D, 16)
+    rows = _tie_rows(scheme, D)
+
+    def kv(b, s0, s1):
+        n = s1 - s0
+        k = np.stack([rows[(s0 + i) % 4] for i in range(n)])[:, None, :].repeat(H, axis=1)
+        v = np.stack([rows[(s0 + i + 1) % 4] for i in range(n)])[:, None, :].repeat(H, axis=1)
+        return np.ascontiguousarray(k), np.ascontiguousarray(v)
+
+    case = Case(w, np.array([64, 23], np.int32), kv_override=kv)
+    case.compare_cache(full=True)
+    assert_attn_close(case.decode(), case.oracle_decode(), scheme)
+
+
+# ------------------------------------------------------------- device-side errors
+def test_bad_page_id_is_flagged_not_faulted():
+    w = small("int8", 8, 4, 64, 16)
+    case = Case(w, np.array([100, 50], np.int32), oracle_seqs=[])
+    bt = case.bt.copy()
+    bt[0, 2] = case.num_pages + 1000  # outside the pool
+    out = torch.zeros((2, 8, 64), dtype=torch.float32, device=DEV)
+    ws = kvq.alloc_workspace(case.g, 2, 8, bt.shape[1], device=DEV)
+    kvq.decode_attn(case.g, dev_bits(case.q), dev(bt), dev(case.lens), out, ws)
+    assert kvq.last_device_error() == 4
+    assert kvq.last_device_error() == 0  # reading clears the flag
+    assert torch.isfinite(out).all()
+    kvq.validate_tables(case.g, dev(bt), dev(case.lens))
+    assert kvq.last_device_error() == 4
+
+
+def test_sequence_longer_than_its_table_is_flagged():
+    w = small("int8", 8, 4, 64, 16)
+    case = Case(w, np.array([64], np.int32), oracle_seqs=[])
+    lens = np.array([64 + 10 * 16 * case.bt.shape[1]], np.int32)
+    out = torch.zeros((1, 8, 64), dtype=torch.float32, device=DEV)
+    ws = kvq.alloc_workspace(case.g, 1, 8, case.bt.shape[1], device=DEV)
+    kvq.decode_attn(case.g, dev_bits(case.q), dev(case.bt), dev(lens), out, ws)
+    assert kvq.last_device_error() == 4
+
+
+def test_append_slot_outside_pool_is_flagged_and_negative_slots_skipped():
+    w = small("fp8", 8, 4, 64, 16)
+    g = kvq.PagedKVCache("fp8", 2, 16, 4, 64, device=DEV)
+    k, v = inp.kv_rows(w, 0, 0, 0, 3)
+    kvq.append(g, dev(np.array([-1, 5, 32], np.int64)), dev_bits(k), dev_bits(v))
+    assert kvq.last_device_error() == 4
+    codes = g.k_codes.cpu().numpy().reshape(2, 4, 16, 64)
+    assert codes[0, :, 5].any() and not codes[0, :, 0].any() and not codes[1].any()
+    # a block table given to append is checked too
+    bt = np.array([[0, 1, 7]], np.int32)
+    kvq.append(g, dev(np.array([1], np.int64)), dev_bits(k[:1]), dev_bits(v[:1]), block_table=dev(bt))
+    assert kvq.last_device_error() == 4
