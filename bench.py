@@ -107,6 +107,24 @@ def traffic_record(cid: int):
     return None if entry is None else entry.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (timing: the slowest rank sets
+    the job's time).  Uses whatever process group is initialized."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank moves its own batch (weak scaling) in the
+    time of the slowest rank."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -131,6 +149,12 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def wait_first(self, timeout_s: float = 10.0) -> None:
+        """Returns once the sampler has produced a line (its start-up is done)."""
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout_s:
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -258,9 +282,10 @@ class Bench:
         torch.cuda.synchronize(self.dev)
         barrier()
         wall = time.perf_counter() - t0
+        status = self.kvq.last_device_error()
         step_ms = [a.elapsed_time(b) for a, b in step_ev]
         k2_ms = [a.elapsed_time(b) for row in k2_ev for a, b in row]
-        return step_ms, k2_ms, wall
+        return step_ms, k2_ms, wall, status
 
     def run_e2e(self, steps: int, warmup: int):
         """The same step through the public API with HOST buffers: pinned host
@@ -390,6 +415,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=2.0,
                     help="wall seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi during the timed region")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -416,27 +442,21 @@ def main(argv=None):
     bench = Bench(w, dev, rank)
     nb = algorithmic_bytes(w, bench.lens, bench.n_new)
     clocks = ClockSampler(local_rank)
-    clocks.start()
-    step_ms, k2_ms, wall = bench.run(args.steps, args.warmup, barrier)
+    if not args.no_clocks:
+        clocks.start()
+        clocks.wait_first()
+    step_ms, k2_ms, wall, status = bench.run(args.steps, args.warmup, barrier)
     clock_info = clocks.stop()
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
     e2e_ms, h2d, d2h = bench.run_e2e(max(3, args.steps // 2), 3)
-    e2e_per_step = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_per_step = float(t.item())
+    e2e_per_step = max_over_ranks(statistics.mean(e2e_ms), world, dev)
 
     if rank == 0:
         peak, peak_kind = measured_hbm_peak()
         k2_mean_ms = statistics.mean(k2_ms)
         achieved = nb["decode_partial"] / w.layers / (k2_mean_ms * 1e-3) / 1e9
-        value = world * nb["step"] / (ms_per_step * 1e-3) / 1e9
+        value = job_throughput(nb["step"], world, ms_per_step)
         decode_gbs = nb["decode"] / (ms_per_step * 1e-3) / 1e9
         line = {
             "metric": METRIC,
@@ -467,11 +487,14 @@ def main(argv=None):
                          "traffic": traffic_record(w.cid),
                          "mean_launch_us": round(k2_mean_ms * 1e3, 3),
                          "algorithmic_bytes_per_launch": nb["decode_partial"] // w.layers},
-            "e2e": {"value": round(world * nb["step"] / (e2e_per_step * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "e2e": {"value": round(job_throughput(nb["step"], world, e2e_per_step), 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_per_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": bench.launches_per_step * args.steps,
             "clocks": clock_info,
             "wall_s_timed_region": round(wall, 4),
+            "step_ms_min_median_max": [round(min(step_ms), 5), round(statistics.median(step_ms), 5),
+                                       round(max(step_ms), 5)],
+            "device_status": bench.kvq.status_string(status),
         }
         if not args.no_cpu_baseline and world >= 1:
             gbs, cores, desc, _ = oracle_sample_run(w, rank, args.cpu_budget)

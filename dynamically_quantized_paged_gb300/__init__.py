@@ -145,6 +145,9 @@ def append(cache: PagedKVCache, slot_mapping: torch.Tensor, k: torch.Tensor, v: 
     """kvq_append: quantize bf16 k, v [T, Hkv, d] into the slots slot_mapping
     (int64 [T]) of the cache."""
     T = slot_mapping.numel()
+    if slot_mapping.element_size() != 8 or k.shape != v.shape or k.numel() != T * cache.num_kv_heads * cache.head_dim \
+            or k.element_size() != 2:
+        raise ValueError("kvq_append: slot_mapping must be int64 [T]; k, v bf16 [T, Hkv, d]")
     B, maxp = (block_table.shape[0], block_table.shape[1]) if block_table is not None else (0, 1)
     _check(lib.kvq_append(ctypes.byref(cache.struct), _ptr(block_table), B, maxp, _ptr(slot_mapping),
                           _ptr(k), _ptr(v), T, cache.sid, _stream(stream)), "kvq_append")
@@ -166,7 +169,15 @@ def alloc_workspace(cache: PagedKVCache, num_seqs: int, num_q_heads: int, max_pa
 
 
 def _decode_call(fn, name, cache, q, block_table, seq_lens, out, workspace, softmax_scale, stream):
-    B, Hq, _ = q.shape
+    B = seq_lens.numel()
+    if q.dim() != 3 or q.shape[0] != B or q.shape[2] != cache.head_dim or tuple(out.shape) != tuple(q.shape) \
+            or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError(f"{name}: shapes q{tuple(q.shape)} out{tuple(out.shape)} "
+                         f"block_table{tuple(block_table.shape)} seq_lens[{B}] do not agree")
+    if q.element_size() != 2 or out.dtype != torch.float32 or seq_lens.element_size() != 4 \
+            or block_table.element_size() != 4:
+        raise ValueError(f"{name}: q must be bf16 bits, out fp32, tables int32")
+    Hq = q.shape[1]
     _check(fn(ctypes.byref(cache.struct), _ptr(q), _ptr(block_table), _ptr(seq_lens), _ptr(out), B, Hq,
               block_table.shape[1], float(softmax_scale), _ptr(workspace), workspace.numel(),
               _stream(stream)), name)

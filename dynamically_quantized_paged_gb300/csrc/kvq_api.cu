@@ -75,7 +75,11 @@ int gqa_ratio(const kvq_cache* c, int32_t Hq) {
     return (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
 }
 
-int n_ctas_for_device() { return kvq::device_sm_count() * kvq::DECODE_CTAS_PER_SM; }
+// The persistent decode grid: resident CTAs per SM (occupancy of this kernel
+// configuration at this batch size) times the SM count.
+int n_ctas_for(const kvq_cache* c, int G, int B) {
+    return kvq::device_sm_count() * kvq::decode_ctas_per_sm(c->scheme, c->head_dim, G, B);
+}
 
 // Shared argument checks of the three decode entry points; fills p.
 kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* block_table,
@@ -98,7 +102,7 @@ kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* 
     if (units_per_seq * B * cache->num_kv_heads >= ((int64_t)1 << 31)) return KVQ_ERR_INVALID_ARG;
     const int dev = current_device();
     if (dev < 0) return KVQ_ERR_CUDA;
-    const int n_ctas = n_ctas_for_device();
+    const int n_ctas = n_ctas_for(cache, G, B);
     if (n_ctas <= 0) return KVQ_ERR_CUDA;
     const size_t need = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, B);
     if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
@@ -242,7 +246,7 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_seqs,
     const int G = gqa_ratio(cache, num_q_heads);
     if (G < 0) return KVQ_ERR_INVALID_ARG;
     if (G == 0) return KVQ_ERR_UNSUPPORTED;
-    const int n_ctas = n_ctas_for_device();
+    const int n_ctas = n_ctas_for(cache, G, num_seqs);
     if (n_ctas <= 0) return KVQ_ERR_CUDA;
     *bytes = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, num_seqs);
     return KVQ_OK;

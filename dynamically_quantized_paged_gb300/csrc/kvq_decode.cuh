@@ -24,10 +24,18 @@
 // codes, V codes and scales (and INT4 zero-points) of those 16 tokens into a
 // stage of a per-consumer-warp ring, completing on an mbarrier; the query
 // rows of each piece are bulk-copied too.  Warps 0-3 consume units round
-// robin: dequantize in registers, scores for the G query heads that share the
-// KV head (warp-shuffle transpose-reduction), online softmax in base 2, V
-// accumulation, and release the stage.  At the end of a piece the four warps'
-// states are combined through shared memory.
+// robin:
+//  * scores: each lane holds 16 channels of the G query rows as fp16 and
+//    turns 16 codes into fp16 with byte permutes (INT8, INT4: exact integer
+//    plus a constant bias removed once per score) or the E4M3 converter;
+//    mixed-precision FMAs (fp16 x fp16 -> fp32) form partial dots, a
+//    transpose-reduction across the lanes sharing a token leaves one score
+//    per lane, and the per-token scale is applied once;
+//  * online softmax in base 2 directly on those lanes (max over the unit by
+//    two shuffles), weights p*scale to shared memory;
+//  * values: each lane owns 8 channels x G heads of fp32 accumulators,
+//    updated with packed fp32x2 FMAs on exactly converted codes.
+// At the end of a piece the four warps' states are combined in shared memory.
 #pragma once
 
 #include "kvq_device.cuh"
@@ -38,6 +46,7 @@ namespace kvq {
 template <int SCHEME, int D, int G>
 struct DecodeCfg {
     static constexpr bool INT4 = SCHEME == KVQ_INT4_ASYM_G32;
+    static constexpr bool INT8 = SCHEME == KVQ_INT8_SYM_TOKEN;
     static constexpr int CB = INT4 ? D / 2 : D;        // code bytes per token row
     static constexpr int NGR = D / 32;                 // INT4 groups per row
     static constexpr int MB = INT4 ? NGR * 2 : 4;      // bytes per token in one scale/zero array
@@ -50,16 +59,23 @@ struct DecodeCfg {
     static constexpr int VZ = KZ + (INT4 ? UNIT * MB : 0);
     static constexpr int STAGE = VZ + (INT4 ? UNIT * MB : 0);
     static constexpr uint32_t STAGE_TX = STAGE;  // bytes one stage receives
-    // K phase: KL lanes per token, CPL channels per lane, TPP tokens per pass
-    static constexpr int CPL = (G >= 8) ? 8 : 16;
+    static constexpr int STAGES = STAGE >= 4096 ? 3 : 4;  // ring depth per consumer warp
+    // occupancy target: CTAs per SM the register budget is compiled for
+    static constexpr int MIN_CTAS = (G >= 8) ? 2 : 3;
+    // scores: KL lanes per token, CPL channels per lane, TPP tokens per pass
+    static constexpr int CPL = (D == 64 && G == 8) ? 8 : 16;
     static constexpr int KL = D / CPL;
     static constexpr int TPP = 32 / KL;
-    // V phase: 8 channels per lane, VT token groups
-    static constexpr int VL = D / 8;
+    static constexpr int PASSES = UNIT / TPP;
+    static constexpr int DUP = KL / G;  // lanes that end holding the same (token, head) score
+    static constexpr int QW = CPL / 2;  // fp16 pairs of query per head per lane
+    static constexpr bool TWO_ACC = G <= 2;  // a second accumulator set for more ILP when registers allow
+    // values: VCH channels per lane, VL lanes per token, VT token groups
+    static constexpr int VCH = (G >= 8 && D == 128) ? 4 : 8;
+    static constexpr int VP = VCH / 2;  // fp32 pairs per head per lane
+    static constexpr int VL = D / VCH;
     static constexpr int VT = 32 / VL;
-    // softmax: SLH lanes per head, STPL tokens per lane
-    static constexpr int SLH = (32 / G) < UNIT ? (32 / G) : UNIT;
-    static constexpr int STPL = UNIT / SLH;
+    static constexpr int V_UNROLL = (G >= 8) ? 2 : UNIT / VT;  // token loop unrolling (register pressure)
     // shared memory layout (bytes)
     static constexpr int OFF_STAGES = 0;
     static constexpr int OFF_Q = OFF_STAGES + CONSUMER_WARPS * STAGES * STAGE;
@@ -67,9 +83,10 @@ struct DecodeCfg {
     static constexpr int OFF_CO = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_CM = OFF_CO + CONSUMER_WARPS * G * D * 4;
     static constexpr int OFF_CL = OFF_CM + CONSUMER_WARPS * G * 4;
-    static constexpr int OFF_W = OFF_CL + CONSUMER_WARPS * G * 4;
-    static constexpr int W_FLOATS = UNIT * G + G;  // per warp: Wt[UNIT][G] + alpha[G]
-    static constexpr int OFF_BAR = (OFF_W + CONSUMER_WARPS * W_FLOATS * 4 + 15) / 16 * 16;
+    static constexpr int OFF_W = (OFF_CL + CONSUMER_WARPS * G * 4 + 15) / 16 * 16;
+    // per warp: weight pairs Wt[UNIT][G] (w, w) as 8 bytes, then alpha[G]
+    static constexpr int W_BYTES = (UNIT * G * 8 + G * 4 + 15) / 16 * 16;
+    static constexpr int OFF_BAR = OFF_W + CONSUMER_WARPS * W_BYTES;
     static constexpr int NBAR = 2 * CONSUMER_WARPS * STAGES + 4;
     static constexpr int OFF_BAD = OFF_BAR + NBAR * 8;  // per stage "page id was invalid" marks
     static constexpr int OFF_MISC = OFF_BAD + CONSUMER_WARPS * STAGES * 4;
@@ -87,25 +104,9 @@ struct DecodeCfg {
 struct Plan {
     int B, Hkv;
     int64_t U, S;
-    const int32_t* prefix;  // shared memory, B + 1 entries
-    __device__ int units(int b) const { return prefix[b + 1] - prefix[b]; }
-    __device__ int64_t seg_start(int b, int h) const {
-        return (int64_t)Hkv * prefix[b] + (int64_t)h * units(b);
-    }
-    // segment containing global unit x (0 <= x < U): smallest b with Hkv*prefix[b+1] > x
-    __device__ void locate(int64_t x, int& b, int& h) const {
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if ((int64_t)Hkv * prefix[mid + 1] > x) hi = mid;
-            else lo = mid + 1;
-        }
-        b = lo;
-        h = (int)((x - (int64_t)Hkv * prefix[b]) / units(b));
-    }
 };
 
-// All threads of the block build the plan in shared memory.
+// All threads of the block build the plan (prefix sums in shared memory).
 __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefix, int64_t* misc) {
     const int B = p.B;
     const int nthr = blockDim.x;
@@ -124,7 +125,7 @@ __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefi
         prefix[b] = u;  // the count, replaced by the exclusive prefix below
         local += u;
     }
-    // exclusive scan of the per-thread sums: warp 0 scans the (<= 32 * ceil(nthr/32)) values
+    // exclusive scan of the per-thread sums by warp 0
     __shared__ int tsum[DECODE_THREADS];
     tsum[tid] = local;
     __syncthreads();
@@ -166,9 +167,8 @@ __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefi
     Plan pl;
     pl.B = B;
     pl.Hkv = p.c.num_kv_heads;
-    pl.prefix = prefix;
     pl.U = (int64_t)pl.Hkv * misc[0];
-    int64_t S = (pl.U + p.n_ctas - 1) / p.n_ctas;
+    const int64_t S = (pl.U + p.n_ctas - 1) / p.n_ctas;
     pl.S = S < MIN_SLICE_UNITS ? MIN_SLICE_UNITS : S;
     return pl;
 }
@@ -182,28 +182,45 @@ struct Piece {
     int slot;         // partial slot otherwise
 };
 
+// Walks the segment pieces of one CTA's slice.  Holds only scalars and the
+// shared-memory prefix pointer (nothing that forces a stack frame).
 struct PieceWalk {
-    const Plan* pl;
+    const int32_t* prefix;
+    int B, Hkv;
     int64_t x, end;
-    int b, h;
-    int idx;  // piece index within the slice
-    int cta;
-    __device__ void begin(const Plan& plan, int c) {
-        pl = &plan;
+    int b, h, idx, cta;
+    __device__ int units(int bb) const { return prefix[bb + 1] - prefix[bb]; }
+    __device__ int64_t seg_start(int bb, int hh) const {
+        return (int64_t)Hkv * prefix[bb] + (int64_t)hh * units(bb);
+    }
+    __device__ void begin(const Plan& pl, const int32_t* pre, int c) {
+        prefix = pre;
+        B = pl.B;
+        Hkv = pl.Hkv;
         cta = c;
-        x = (int64_t)c * plan.S;
-        end = x + plan.S;
-        if (end > plan.U) end = plan.U;
+        x = (int64_t)c * pl.S;
+        end = x + pl.S;
+        if (end > pl.U) end = pl.U;
         idx = 0;
-        if (x < end) plan.locate(x, b, h);
+        b = h = 0;
+        if (x < end) {  // segment containing x: smallest b with Hkv*prefix[b+1] > x
+            int lo = 0, hi = B - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if ((int64_t)Hkv * prefix[mid + 1] > x) hi = mid;
+                else lo = mid + 1;
+            }
+            b = lo;
+            h = (int)((x - (int64_t)Hkv * prefix[b]) / units(b));
+        }
     }
     __device__ bool done() const { return x >= end; }
     __device__ Piece get(const DecodeParams& p) const {
         Piece pc;
         pc.b = b;
         pc.h = h;
-        const int64_t a = pl->seg_start(b, h);
-        const int n = pl->units(b);
+        const int64_t a = seg_start(b, h);
+        const int n = units(b);
         const int64_t e = a + n;
         pc.u_lo = (int)(x - a);
         pc.u_hi = (int)((end < e ? end : e) - a);
@@ -216,13 +233,13 @@ struct PieceWalk {
         return pc;
     }
     __device__ void next() {
-        const int64_t e = pl->seg_start(b, h) + pl->units(b);
+        const int64_t e = seg_start(b, h) + units(b);
         x = e < end ? e : end;
         ++idx;
         if (x >= end) return;
-        if (++h == pl->Hkv) {
+        if (++h == Hkv) {
             h = 0;
-            do { ++b; } while (pl->units(b) == 0);
+            do { ++b; } while (units(b) == 0);
         }
     }
 };
@@ -250,16 +267,17 @@ __device__ __forceinline__ void transpose_reduce(float* v, int lane) {
 }
 
 template <int SCHEME, int D, int G>
-__global__ void __launch_bounds__(DECODE_THREADS, DECODE_CTAS_PER_SM)
+__global__ void __launch_bounds__(DECODE_THREADS, (DecodeCfg<SCHEME, D, G>::MIN_CTAS))
 decode_partial_kernel(const DecodeParams p) {
     using C = DecodeCfg<SCHEME, D, G>;
+    constexpr int STAGES_ = C::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* full = bars;                                   // [CW][STAGES]
-    uint64_t* empty = bars + CONSUMER_WARPS * STAGES;        // [CW][STAGES]
-    uint64_t* qfull = bars + 2 * CONSUMER_WARPS * STAGES;    // [2]
+    uint64_t* empty = bars + CONSUMER_WARPS * STAGES_;       // [CW][STAGES]
+    uint64_t* qfull = bars + 2 * CONSUMER_WARPS * STAGES_;   // [2]
     uint64_t* qempty = qfull + 2;                            // [2]
     int32_t* bad = reinterpret_cast<int32_t*>(smem + C::OFF_BAD);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -267,7 +285,7 @@ decode_partial_kernel(const DecodeParams p) {
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + C::OFF_PLAN);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < CONSUMER_WARPS * STAGES; ++i) {
+        for (int i = 0; i < CONSUMER_WARPS * STAGES_; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
@@ -297,7 +315,7 @@ decode_partial_kernel(const DecodeParams p) {
         const uint64_t pol = l2_evict_first_policy();
         int cnt0 = 0, cnt1 = 0, cnt2 = 0, cnt3 = 0;
         PieceWalk walk;
-        walk.begin(plan, blockIdx.x);
+        walk.begin(plan, prefix, blockIdx.x);
         int pi = 0;
         for (; !walk.done(); walk.next(), ++pi) {
             const Piece pc = walk.get(p);
@@ -330,9 +348,9 @@ decode_partial_kernel(const DecodeParams p) {
                     const int page = __shfl_sync(0xffffffffu, pid, lp - batch0);
                     int& cnt = (w == 0) ? cnt0 : (w == 1) ? cnt1 : (w == 2) ? cnt2 : cnt3;
                     if (lane == 0 && !*abort_flag) {
-                        const int st = cnt % STAGES;
-                        const int k = cnt / STAGES;
-                        const int bi = w * STAGES + st;
+                        const int st = cnt % STAGES_;
+                        const int k = cnt / STAGES_;
+                        const int bi = w * STAGES_ + st;
                         if (!mbar_wait(&empty[bi], (k & 1) ^ 1)) {
                             flag_error(p.err, ERR_TIMEOUT);
                             *abort_flag = 1;
@@ -369,41 +387,40 @@ decode_partial_kernel(const DecodeParams p) {
         if (lane == 0 && *abort_flag) {
             const int cnts[4] = {cnt0, cnt1, cnt2, cnt3};
             for (int w = 0; w < CONSUMER_WARPS; ++w)
-                for (int k = (cnts[w] > STAGES ? cnts[w] - STAGES : 0); k < cnts[w]; ++k)
-                    mbar_wait(&full[w * STAGES + k % STAGES], (k / STAGES) & 1);
+                for (int k = (cnts[w] > STAGES_ ? cnts[w] - STAGES_ : 0); k < cnts[w]; ++k)
+                    mbar_wait(&full[w * STAGES_ + k % STAGES_], (k / STAGES_) & 1);
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
     const int tid = threadIdx.x;  // 0 .. 127
-    float* Wt = reinterpret_cast<float*>(smem + C::OFF_W) + warp * C::W_FLOATS;  // [UNIT][G]
-    float* AL = Wt + UNIT * G;                                                    // [G]
+    uint8_t* wbase = smem + C::OFF_W + warp * C::W_BYTES;
+    uint64_t* Wt = reinterpret_cast<uint64_t*>(wbase);             // [UNIT][G] (w, w)
+    float* AL = reinterpret_cast<float*>(wbase + UNIT * G * 8);    // [G]
     float* CO = reinterpret_cast<float*>(smem + C::OFF_CO);
     float* CM = reinterpret_cast<float*>(smem + C::OFF_CM);
     float* CL = reinterpret_cast<float*>(smem + C::OFF_CL);
-    // K-phase lane coordinates
+    // score-lane coordinates
     const int k_tok = lane / C::KL;
     const int k_c0 = (lane % C::KL) * C::CPL;
-    const int k_head = (lane % C::KL) / (C::KL / G);
-    const bool k_writer = (lane % (C::KL / G)) == 0;
-    // softmax lane coordinates
-    const int s_head = lane / C::SLH;
-    const bool s_act = s_head < G;
-    const int s_t0 = lane % C::SLH;
-    // V-phase lane coordinates
-    const int v_c0 = (lane % C::VL) * 8;
+    const int k_head = (lane % C::KL) / C::DUP;
+    const bool k_writer = (lane % C::DUP) == 0;
+    // value-lane coordinates
+    const int v_c0 = (lane % C::VL) * C::VCH;
     const int v_tok = lane / C::VL;
+    const float qk_scale = p.q_scale;  // softmax scale * log2(e)
 
     int cnt = 0;
     PieceWalk walk;
-    walk.begin(plan, blockIdx.x);
+    walk.begin(plan, prefix, blockIdx.x);
     int pi = 0;
     for (; !walk.done(); walk.next(), ++pi) {
         const Piece pc = walk.get(p);
-        // ---- query rows for this piece -> registers (prescaled)
-        float qf[G][C::CPL];
-        float qsum[G];
+        // ---- query rows of this piece -> fp16 pairs in registers
+        uint32_t qh[G][C::QW];
+        float qsum[G];         // INT4: sum of the query over this lane's channels, per head
+        float my_qsum = 0.0f;  // INT8: sum of the query over all channels, this lane's head
         {
             const int qs = pi & 1;
             if (!*abort_flag && !mbar_wait(&qfull[qs], (pi >> 1) & 1)) {
@@ -413,37 +430,63 @@ decode_partial_kernel(const DecodeParams p) {
             const uint16_t* qb = reinterpret_cast<const uint16_t*>(smem + C::OFF_Q + qs * C::Q_BYTES);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                qsum[g] = 0.0f;
+                float qf[C::CPL];
 #pragma unroll
                 for (int j = 0; j < C::CPL; j += 8) {
                     const uint4 raw = *reinterpret_cast<const uint4*>(qb + g * D + k_c0 + j);
                     const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        qf[g][j + 2 * i] = bf16_bits_to_float(w4[i] & 0xFFFFu) * p.q_scale;
-                        qf[g][j + 2 * i + 1] = bf16_bits_to_float(w4[i] >> 16) * p.q_scale;
-                        qsum[g] += qf[g][j + 2 * i] + qf[g][j + 2 * i + 1];
+                        qf[j + 2 * i] = __half2float(__float2half_rn(bf16_bits_to_float(w4[i] & 0xFFFFu)));
+                        qf[j + 2 * i + 1] = __half2float(__float2half_rn(bf16_bits_to_float(w4[i] >> 16)));
                     }
                 }
+                float s = 0.0f;
+#pragma unroll
+                for (int j = 0; j < C::CPL; ++j) s += qf[j];
+                qsum[g] = s;
+#pragma unroll
+                for (int i = 0; i < C::QW; ++i) {
+                    int a, b2;
+                    if constexpr (C::INT4) {  // pair (s, s+4) inside each 8-channel word
+                        a = (i / 4) * 8 + (i % 4);
+                        b2 = a + 4;
+                    } else {                  // consecutive channels
+                        a = 2 * i;
+                        b2 = 2 * i + 1;
+                    }
+                    const __half2 h = __floats2half2_rn(qf[a], qf[b2]);
+                    qh[g][i] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+            }
+            if constexpr (C::INT8) {  // full-row sums for the bias correction
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int off = C::KL / 2; off >= 1; off >>= 1) qsum[g] += __shfl_xor_sync(0xffffffffu, qsum[g], off);
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    if (g == k_head) my_qsum = qsum[g];
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&qempty[qs]);
         }
+
         float m_run = -INFINITY, l_run = 0.0f;
-        float o[G][8];
+        uint64_t o[G][C::VP];
         float zacc[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             zacc[g] = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) o[g][j] = 0.0f;
+            for (int j = 0; j < C::VP; ++j) o[g][j] = 0ull;
         }
 
         for (int j = warp; j < pc.u_hi - pc.u_lo; j += CONSUMER_WARPS, ++cnt) {
-            const int st = cnt % STAGES;
-            const int bi = warp * STAGES + st;
+            const int st = cnt % STAGES_;
+            const int bi = warp * STAGES_ + st;
             bool ok = !*abort_flag;
-            if (ok && !mbar_wait(&full[bi], (cnt / STAGES) & 1)) {
+            if (ok && !mbar_wait(&full[bi], (cnt / STAGES_) & 1)) {
                 flag_error(p.err, ERR_TIMEOUT);
                 *abort_flag = 1;
                 ok = false;
@@ -455,12 +498,22 @@ decode_partial_kernel(const DecodeParams p) {
             const uint8_t* stg = smem + C::OFF_STAGES + bi * C::STAGE;
 
             if (n_valid > 0) {
-                // ---- K phase: scores for G heads x UNIT tokens
+                // ---- scores for G heads x UNIT tokens
+                float sc[C::PASSES];
 #pragma unroll
-                for (int pass = 0; pass < UNIT / C::TPP; ++pass) {
+                for (int pass = 0; pass < C::PASSES; ++pass) {
                     const int t = pass * C::TPP + k_tok;
-                    float acc[G];
-                    float c[C::CPL];
+                    constexpr int NA1 = C::TWO_ACC ? G : 1;
+                    float acc[G], acc1[NA1];
+#pragma unroll
+                    for (int g = 0; g < G; ++g) acc[g] = 0.0f;
+#pragma unroll
+                    for (int g = 0; g < NA1; ++g) acc1[g] = 0.0f;
+                    // acc[g] (+ acc1[g]) += q_g . c over this lane's channels
+                    auto dot2 = [&](int g, uint32_t q2, uint32_t c2) {
+                        if constexpr (C::TWO_ACC) mfma_h2(q2, c2, acc[g], acc1[g % NA1]);
+                        else mfma_h2_1(q2, c2, acc[g]);
+                    };
                     if constexpr (!C::INT4) {
                         const uint8_t* src = stg + C::KC + t * D + k_c0;
                         uint32_t wv[C::CPL / 4];
@@ -473,15 +526,24 @@ decode_partial_kernel(const DecodeParams p) {
                         }
 #pragma unroll
                         for (int i = 0; i < C::CPL / 4; ++i) {
-                            if constexpr (SCHEME == KVQ_INT8_SYM_TOKEN) s8x4_to_float(wv[i], c + 4 * i);
-                            else e4m3x4_to_float(wv[i], c + 4 * i);
+                            uint32_t c01, c23;
+                            if constexpr (C::INT8) {
+                                const uint32_t u = wv[i] ^ 0x80808080u;
+                                c01 = s8x2_to_h2_biased(u, 0);
+                                c23 = s8x2_to_h2_biased(u, 1);
+                            } else {
+                                c01 = e4m3x2_to_h2(wv[i]);
+                                c23 = e4m3x2_to_h2(wv[i] >> 16);
+                            }
+#pragma unroll
+                            for (int g = 0; g < G; ++g) {
+                                dot2(g, qh[g][2 * i], c01);
+                                dot2(g, qh[g][2 * i + 1], c23);
+                            }
                         }
+                        if constexpr (C::TWO_ACC) {
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            float a = qf[g][0] * c[0];
-#pragma unroll
-                            for (int i = 1; i < C::CPL; ++i) a = fmaf(qf[g][i], c[i], a);
-                            acc[g] = a;
+                            for (int g = 0; g < G; ++g) acc[g] += acc1[g % NA1];
                         }
                     } else {
                         const uint8_t* src = stg + C::KC + t * (D / 2) + k_c0 / 2;
@@ -493,111 +555,140 @@ decode_partial_kernel(const DecodeParams p) {
                             wv[0] = *reinterpret_cast<const uint32_t*>(src);
                         }
 #pragma unroll
-                        for (int i = 0; i < C::CPL / 8; ++i) u4x8_to_float(wv[i], c + 8 * i);
+                        for (int i = 0; i < C::CPL / 8; ++i) {
+#pragma unroll
+                            for (int s = 0; s < 4; ++s) {
+                                const uint32_t c2 = u4pair_to_h2_biased(wv[i], s);
+#pragma unroll
+                                for (int g = 0; g < G; ++g) dot2(g, qh[g][4 * i + s], c2);
+                            }
+                        }
                         const int gi = t * C::NGR + k_c0 / 32;
                         const float ks = __half2float(reinterpret_cast<const __half*>(stg + C::KS)[gi]);
                         const float kz = __half2float(reinterpret_cast<const __half*>(stg + C::KZ)[gi]);
+                        const float zc = fmaf(-U4_H2_BIAS, ks, kz);  // zero - 1024 * scale
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            float a = qf[g][0] * c[0];
-#pragma unroll
-                            for (int i = 1; i < C::CPL; ++i) a = fmaf(qf[g][i], c[i], a);
-                            acc[g] = fmaf(ks, a, kz * qsum[g]);
-                        }
+                        for (int g = 0; g < G; ++g)
+                            acc[g] = fmaf(ks, C::TWO_ACC ? acc[g] + acc1[g % NA1] : acc[g], zc * qsum[g]);
                     }
                     transpose_reduce<G, C::KL / 2>(acc, lane);
+                    float s;
+                    if constexpr (C::INT8) {
+                        s = fmaf(-S8_H2_BIAS, my_qsum, acc[0]) * (reinterpret_cast<const float*>(stg + C::KS)[t] * qk_scale);
+                    } else if constexpr (C::INT4) {
+                        s = acc[0] * qk_scale;
+                    } else {
+                        s = acc[0] * (reinterpret_cast<const float*>(stg + C::KS)[t] * qk_scale);
+                    }
+                    sc[pass] = (t < n_valid) ? s : -INFINITY;
+                }
+                // ---- online softmax (base 2) on the score lanes
+                float mx = sc[0];
+#pragma unroll
+                for (int pass = 1; pass < C::PASSES; ++pass) mx = fmaxf(mx, sc[pass]);
+#pragma unroll
+                for (int off = C::KL; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float m_new = fmaxf(m_run, mx);
+                const float alpha = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - m_new);
+                float psum = 0.0f;
+#pragma unroll
+                for (int pass = 0; pass < C::PASSES; ++pass) {
+                    const int t = pass * C::TPP + k_tok;
+                    const float pr = (sc[pass] == -INFINITY) ? 0.0f : fast_exp2(sc[pass] - m_new);
+                    psum += pr;
                     if (k_writer) {
-                        float sc = acc[0];
-                        if constexpr (!C::INT4) sc *= reinterpret_cast<const float*>(stg + C::KS)[t];
-                        Wt[t * G + k_head] = (t < n_valid) ? sc : -INFINITY;
+                        float wv = pr;
+                        if constexpr (!C::INT4) wv = (t < n_valid) ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
+                        Wt[t * G + k_head] = f2pack(wv, wv);
                     }
                 }
+                l_run = l_run * alpha + psum;
+                m_run = m_new;
+                if (k_writer && k_tok == 0) AL[k_head] = alpha;
+                const bool rescale = __any_sync(0xffffffffu, alpha != 1.0f);
                 __syncwarp();
-                // ---- online softmax (base 2; q carries log2(e) / sqrt(d))
-                bool rescale;
-                {
-                    float s[C::STPL];
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int k = 0; k < C::STPL; ++k) {
-                        const int t = s_t0 + k * C::SLH;
-                        s[k] = s_act ? Wt[t * G + s_head] : -INFINITY;
-                        mx = fmaxf(mx, s[k]);
-                    }
-#pragma unroll
-                    for (int off = C::SLH / 2; off >= 1; off >>= 1)
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                    const float m_new = fmaxf(m_run, mx);
-                    const float alpha = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - m_new);
-                    float psum = 0.0f;
-#pragma unroll
-                    for (int k = 0; k < C::STPL; ++k) {
-                        const int t = s_t0 + k * C::SLH;
-                        const float pr = (s[k] == -INFINITY) ? 0.0f : fast_exp2(s[k] - m_new);
-                        psum += pr;
-                        if (s_act) {
-                            float wv = pr;
-                            if constexpr (!C::INT4) wv = (t < n_valid) ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
-                            Wt[t * G + s_head] = wv;
-                        }
-                    }
-                    l_run = l_run * alpha + psum;
-                    m_run = m_new;
-                    if (s_act && s_t0 == 0) AL[s_head] = alpha;
-                    rescale = __any_sync(0xffffffffu, s_act && alpha != 1.0f);
-                }
-                __syncwarp();
-                // ---- V phase
+                // ---- values
                 if (rescale) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         const float a = AL[g];
+                        const uint64_t a2 = f2pack(a, a);
                         zacc[g] *= a;
 #pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) o[g][jj] *= a;
+                        for (int jj = 0; jj < C::VP; ++jj) o[g][jj] = fmul2(o[g][jj], a2);
                     }
                 }
-#pragma unroll
+#pragma unroll(C::V_UNROLL)
                 for (int k = 0; k < UNIT / C::VT; ++k) {
                     const int t = v_tok + k * C::VT;
                     if (t < n_valid) {
-                        float c[8];
-                        float wg[G];
-#pragma unroll
-                        for (int g = 0; g < G; g += 4) {
-                            if constexpr (G >= 4) {
-                                const float4 w4 = *reinterpret_cast<const float4*>(Wt + t * G + g);
-                                wg[g] = w4.x; wg[g + 1] = w4.y; wg[g + 2] = w4.z; wg[g + 3] = w4.w;
+                        uint64_t c2[C::VP];
+                        if constexpr (C::INT8) {
+                            const uint64_t bias = f2pack(-8388736.0f, -8388736.0f);
+                            uint32_t words[C::VCH / 4];
+                            if constexpr (C::VCH == 8) {
+                                const uint2 r = *reinterpret_cast<const uint2*>(stg + C::VC + t * D + v_c0);
+                                words[0] = r.x;
+                                words[1] = r.y;
                             } else {
+                                words[0] = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * D + v_c0);
+                            }
 #pragma unroll
-                                for (int gg = 0; gg < G; ++gg) wg[gg] = Wt[t * G + gg];
+                            for (int i = 0; i < C::VCH / 4; ++i) {
+                                const uint32_t u = words[i] ^ 0x80808080u;
+                                c2[2 * i] = fadd2(f2pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                                         __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))), bias);
+                                c2[2 * i + 1] = fadd2(f2pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                                             __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))), bias);
+                            }
+                        } else if constexpr (!C::INT4) {
+                            uint32_t words[C::VCH / 4];
+                            if constexpr (C::VCH == 8) {
+                                const uint2 r = *reinterpret_cast<const uint2*>(stg + C::VC + t * D + v_c0);
+                                words[0] = r.x;
+                                words[1] = r.y;
+                            } else {
+                                words[0] = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * D + v_c0);
+                            }
+#pragma unroll
+                            for (int i = 0; i < C::VP; ++i) {
+                                const uint32_t hw = e4m3x2_to_h2(words[i / 2] >> (16 * (i % 2)));
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw));
+                                c2[i] = f2pack(f.x, f.y);
+                            }
+                        } else {
+                            uint32_t r;
+                            if constexpr (C::VCH == 8) r = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * (D / 2) + v_c0 / 2);
+                            else r = *reinterpret_cast<const uint16_t*>(stg + C::VC + t * (D / 2) + v_c0 / 2);
+                            const uint64_t bias = f2pack(-8388608.0f, -8388608.0f);
+#pragma unroll
+                            for (int i = 0; i < C::VP; ++i) {
+                                const float lo = __uint_as_float(((r >> (8 * i)) & 0xFu) | 0x4B000000u);
+                                const float hi = __uint_as_float(((r >> (8 * i + 4)) & 0xFu) | 0x4B000000u);
+                                c2[i] = fadd2(f2pack(lo, hi), bias);
                             }
                         }
                         if constexpr (!C::INT4) {
-                            const uint2 r = *reinterpret_cast<const uint2*>(stg + C::VC + t * D + v_c0);
-                            if constexpr (SCHEME == KVQ_INT8_SYM_TOKEN) {
-                                s8x4_to_float(r.x, c);
-                                s8x4_to_float(r.y, c + 4);
-                            } else {
-                                e4m3x4_to_float(r.x, c);
-                                e4m3x4_to_float(r.y, c + 4);
+#pragma unroll
+                            for (int g = 0; g < G; ++g) {
+                                const uint64_t w2 = Wt[t * G + g];
+#pragma unroll
+                                for (int jj = 0; jj < C::VP; ++jj) o[g][jj] = ffma2(c2[jj], w2, o[g][jj]);
                             }
-#pragma unroll
-                            for (int g = 0; g < G; ++g)
-#pragma unroll
-                                for (int jj = 0; jj < 8; ++jj) o[g][jj] = fmaf(wg[g], c[jj], o[g][jj]);
                         } else {
-                            const uint32_t r = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * (D / 2) + v_c0 / 2);
-                            u4x8_to_float(r, c);
                             const int gi = t * C::NGR + v_c0 / 32;
                             const float vs = __half2float(reinterpret_cast<const __half*>(stg + C::VS)[gi]);
                             const float vz = __half2float(reinterpret_cast<const __half*>(stg + C::VZ)[gi]);
+                            const uint64_t s2 = f2pack(vs, vs);
 #pragma unroll
                             for (int g = 0; g < G; ++g) {
-                                const float a = wg[g] * vs;
-                                zacc[g] = fmaf(wg[g], vz, zacc[g]);
+                                const uint64_t w2 = Wt[t * G + g];
+                                float wl, wh;
+                                f2unpack(w2, wl, wh);
+                                zacc[g] = fmaf(wl, vz, zacc[g]);
+                                const uint64_t a2 = fmul2(w2, s2);
 #pragma unroll
-                                for (int jj = 0; jj < 8; ++jj) o[g][jj] = fmaf(a, c[jj], o[g][jj]);
+                                for (int jj = 0; jj < C::VP; ++jj) o[g][jj] = ffma2(c2[jj], a2, o[g][jj]);
                             }
                         }
                     }
@@ -609,28 +700,38 @@ decode_partial_kernel(const DecodeParams p) {
 
         // ---- per-warp state -> shared memory
 #pragma unroll
-        for (int off = C::SLH / 2; off >= 1; off >>= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
+        for (int off = C::KL; off < 32; off <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                float v = o[g][jj] + zacc[g];
+            for (int jj = 0; jj < C::VP; ++jj) {
+                float lo, hi;
+                f2unpack(o[g][jj], lo, hi);
+                lo += zacc[g];
+                hi += zacc[g];
 #pragma unroll
-                for (int off = C::VL; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                o[g][jj] = v;
+                for (int off = C::VL; off < 32; off <<= 1) {
+                    lo += __shfl_xor_sync(0xffffffffu, lo, off);
+                    hi += __shfl_xor_sync(0xffffffffu, hi, off);
+                }
+                o[g][jj] = f2pack(lo, hi);
             }
         }
         if (v_tok == 0) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
+                float f[C::VCH];
+#pragma unroll
+                for (int jj = 0; jj < C::VP; ++jj) f2unpack(o[g][jj], f[2 * jj], f[2 * jj + 1]);
                 float* dst = CO + (warp * G + g) * D + v_c0;
-                *reinterpret_cast<float4*>(dst) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
-                *reinterpret_cast<float4*>(dst + 4) = make_float4(o[g][4], o[g][5], o[g][6], o[g][7]);
+#pragma unroll
+                for (int jj = 0; jj < C::VCH; jj += 4)
+                    *reinterpret_cast<float4*>(dst + jj) = make_float4(f[jj], f[jj + 1], f[jj + 2], f[jj + 3]);
             }
         }
-        if (s_act && s_t0 == 0) {
-            CM[warp * G + s_head] = m_run;
-            CL[warp * G + s_head] = l_run;
+        if (k_writer && k_tok == 0) {
+            CM[warp * G + k_head] = m_run;
+            CL[warp * G + k_head] = l_run;
         }
         named_barrier_sync(1, 32 * CONSUMER_WARPS);
         // ---- combine the warps; final row or split partial
@@ -704,21 +805,42 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
     }
 }
 
+// Shared memory attribute per device, set once (host-only state).
+template <int SCHEME, int D, int G>
+cudaError_t configure_decode_t() {
+    using C = DecodeCfg<SCHEME, D, G>;
+    static int configured[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(decode_partial_kernel<SCHEME, D, G>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(MAX_SEQS));
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    return cudaSuccess;
+}
+
+// Resident CTAs per SM for this instantiation and batch size (the persistent
+// grid is this times the SM count).
+template <int SCHEME, int D, int G>
+int decode_ctas_per_sm_t(int B) {
+    using C = DecodeCfg<SCHEME, D, G>;
+    if (configure_decode_t<SCHEME, D, G>() != cudaSuccess) return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partial_kernel<SCHEME, D, G>, DECODE_THREADS,
+                                                      C::smem_bytes(B)) != cudaSuccess)
+        return 0;
+    return n;
+}
+
 template <int SCHEME, int D, int G>
 cudaError_t launch_decode_partial_t(const DecodeParams& p, cudaStream_t s) {
     using C = DecodeCfg<SCHEME, D, G>;
-    const size_t smem = C::smem_bytes(p.B);
-    static int configured_device = -1;  // attribute set per device (few devices, host-only)
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<SCHEME, D, G>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::smem_bytes(MAX_SEQS));
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
-    decode_partial_kernel<SCHEME, D, G><<<p.n_ctas, DECODE_THREADS, smem, s>>>(p);
+    cudaError_t e = configure_decode_t<SCHEME, D, G>();
+    if (e != cudaSuccess) return e;
+    decode_partial_kernel<SCHEME, D, G><<<p.n_ctas, DECODE_THREADS, C::smem_bytes(p.B), s>>>(p);
     return cudaGetLastError();
 }
 
@@ -729,26 +851,41 @@ cudaError_t launch_decode_merge_t(const DecodeParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+#define KVQ_DISPATCH_DG(D_, G_, CALL)              \
+    do {                                           \
+        if ((D_) == 128) {                         \
+            switch (G_) {                          \
+                case 1: { constexpr int D = 128, G = 1; CALL; } \
+                case 2: { constexpr int D = 128, G = 2; CALL; } \
+                case 4: { constexpr int D = 128, G = 4; CALL; } \
+                default: { constexpr int D = 128, G = 8; CALL; } \
+            }                                      \
+        }                                          \
+        switch (G_) {                              \
+            case 1: { constexpr int D = 64, G = 1; CALL; } \
+            case 2: { constexpr int D = 64, G = 2; CALL; } \
+            case 4: { constexpr int D = 64, G = 4; CALL; } \
+            default: { constexpr int D = 64, G = 8; CALL; } \
+        }                                          \
+    } while (0)
+
 template <int SCHEME>
-cudaError_t launch_decode_partial_scheme(const DecodeParams& p, int G, cudaStream_t s) {
-    if (p.c.head_dim == 128) {
-        switch (G) {
-            case 1: return launch_decode_partial_t<SCHEME, 128, 1>(p, s);
-            case 2: return launch_decode_partial_t<SCHEME, 128, 2>(p, s);
-            case 4: return launch_decode_partial_t<SCHEME, 128, 4>(p, s);
-            default: return launch_decode_partial_t<SCHEME, 128, 8>(p, s);
-        }
-    }
-    switch (G) {
-        case 1: return launch_decode_partial_t<SCHEME, 64, 1>(p, s);
-        case 2: return launch_decode_partial_t<SCHEME, 64, 2>(p, s);
-        case 4: return launch_decode_partial_t<SCHEME, 64, 4>(p, s);
-        default: return launch_decode_partial_t<SCHEME, 64, 8>(p, s);
-    }
+cudaError_t launch_decode_partial_scheme(const DecodeParams& p, int G_, cudaStream_t s) {
+    KVQ_DISPATCH_DG(p.c.head_dim, G_, return (launch_decode_partial_t<SCHEME, D, G>(p, s)));
+    return cudaErrorInvalidValue;
+}
+
+template <int SCHEME>
+int decode_ctas_per_sm_scheme(int head_dim, int G_, int B) {
+    KVQ_DISPATCH_DG(head_dim, G_, return (decode_ctas_per_sm_t<SCHEME, D, G>(B)));
+    return 0;
 }
 
 cudaError_t launch_decode_partial_int8(const DecodeParams& p, int G, cudaStream_t s);
 cudaError_t launch_decode_partial_fp8(const DecodeParams& p, int G, cudaStream_t s);
 cudaError_t launch_decode_partial_int4(const DecodeParams& p, int G, cudaStream_t s);
+int decode_ctas_per_sm_int8(int head_dim, int G, int B);
+int decode_ctas_per_sm_fp8(int head_dim, int G, int B);
+int decode_ctas_per_sm_int4(int head_dim, int G, int B);
 
 }  // namespace kvq

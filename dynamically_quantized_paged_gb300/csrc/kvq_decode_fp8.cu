@@ -8,4 +8,8 @@ cudaError_t launch_decode_partial_fp8(const DecodeParams& p, int G, cudaStream_t
     return launch_decode_partial_scheme<KVQ_FP8E4M3_TOKEN>(p, G, s);
 }
 
+int decode_ctas_per_sm_fp8(int head_dim, int G, int B) {
+    return decode_ctas_per_sm_scheme<KVQ_FP8E4M3_TOKEN>(head_dim, G, B);
+}
+
 }  // namespace kvq

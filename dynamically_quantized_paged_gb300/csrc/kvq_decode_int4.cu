@@ -8,4 +8,8 @@ cudaError_t launch_decode_partial_int4(const DecodeParams& p, int G, cudaStream_
     return launch_decode_partial_scheme<KVQ_INT4_ASYM_G32>(p, G, s);
 }
 
+int decode_ctas_per_sm_int4(int head_dim, int G, int B) {
+    return decode_ctas_per_sm_scheme<KVQ_INT4_ASYM_G32>(head_dim, G, B);
+}
+
 }  // namespace kvq

@@ -140,6 +140,74 @@ __device__ __forceinline__ void u4x8_to_float(uint32_t w, float f[8]) {
     }
 }
 
+// ---- packed fp32 pairs (sm_100+ .f32x2 arithmetic) ------------------------
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Two mixed-precision FMAs: acc0 += lo(q2) * lo(c2), acc1 += hi(q2) * hi(c2),
+// fp16 operands, fp32 accumulation (the product is exact in fp32).
+__device__ __forceinline__ void mfma_h2(uint32_t q2, uint32_t c2, float& acc0, float& acc1) {
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %2;\n\t"
+        "mov.b32 {b0, b1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+        "fma.rn.f32.f16 %1, a1, b1, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(q2), "r"(c2));
+}
+
+// The same two products accumulated into one fp32 value.
+__device__ __forceinline__ void mfma_h2_1(uint32_t q2, uint32_t c2, float& acc) {
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "mov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+        "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(q2), "r"(c2));
+}
+
+// Two int8 codes (bytes 2k, 2k+1 of w) -> fp16 pair holding 1152 + code,
+// exactly: flip the sign bit (code + 128) and place the byte in the low
+// mantissa byte of 1024 (fp16 exponent 10, spacing 1).
+__device__ __forceinline__ uint32_t s8x2_to_h2_biased(uint32_t flipped, int k) {
+    return __byte_perm(flipped, 0x64646464u, k == 0 ? 0x4140 : 0x4342);
+}
+constexpr float S8_H2_BIAS = 1152.0f;
+
+// Two E4M3 codes (low 16 bits) -> exact fp16 pair.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t w16) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w16 & 0xFFFFu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Nibbles s and s+4 of an 8-code word -> fp16 pair holding 1024 + code.
+__device__ __forceinline__ uint32_t u4pair_to_h2_biased(uint32_t w, int s) {
+    return ((w >> (4 * s)) & 0x000F000Fu) | 0x64006400u;
+}
+constexpr float U4_H2_BIAS = 1024.0f;
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);
 }

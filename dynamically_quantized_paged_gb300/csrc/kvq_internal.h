@@ -19,8 +19,6 @@ constexpr int UNIT = 16;
 // Decode CTA: one producer warp (bulk copies) + CONSUMER_WARPS compute warps.
 constexpr int CONSUMER_WARPS = 4;
 constexpr int DECODE_THREADS = 32 * (CONSUMER_WARPS + 1);
-constexpr int DECODE_CTAS_PER_SM = 2;
-constexpr int STAGES = 4;          // ring depth per consumer warp
 constexpr int MAX_SEQS = 4096;     // per decode call (the plan lives in shared memory)
 constexpr int MIN_SLICE_UNITS = 8; // smallest per-CTA share of the work, in units
 
@@ -76,6 +74,8 @@ inline size_t decode_workspace_bytes(int n_ctas, int G, int D, int B) {
 cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaStream_t s);
 cudaError_t launch_decode_partial(const DecodeParams& p, int G, cudaStream_t s);
 cudaError_t launch_decode_merge(const DecodeParams& p, int G, cudaStream_t s);
+// Resident decode CTAs per SM for this configuration (0 if the query fails).
+int decode_ctas_per_sm(int scheme, int head_dim, int G, int B);
 cudaError_t launch_validate(const CacheView& c, const int32_t* block_table,
                             const int32_t* seq_lens, int B, int max_pages, unsigned* err,
                             cudaStream_t s);

@@ -12,6 +12,14 @@ cudaError_t launch_decode_partial(const DecodeParams& p, int G, cudaStream_t s) 
     }
 }
 
+int decode_ctas_per_sm(int scheme, int head_dim, int G, int B) {
+    switch (scheme) {
+        case KVQ_INT8_SYM_TOKEN: return decode_ctas_per_sm_int8(head_dim, G, B);
+        case KVQ_FP8E4M3_TOKEN: return decode_ctas_per_sm_fp8(head_dim, G, B);
+        default: return decode_ctas_per_sm_int4(head_dim, G, B);
+    }
+}
+
 cudaError_t launch_decode_merge(const DecodeParams& p, int G, cudaStream_t s) {
     if (p.c.head_dim == 128) {
         switch (G) {

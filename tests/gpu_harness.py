@@ -51,7 +51,8 @@ class Case:
                 kvq.append(self.g, dev(slots), dev_bits(k), dev_bits(v))
                 if b in self.oracle_seqs:
                     assert self.o.append(slots, k, v) == 0
-        self.q = inp.queries(w, layer)
+        import dataclasses
+        self.q = inp.queries(dataclasses.replace(w, batch=len(self.lens)), layer)
         torch.cuda.synchronize()
 
     def decode(self, q: np.ndarray | None = None, softmax_scale: float = 0.0, split_calls=False):
