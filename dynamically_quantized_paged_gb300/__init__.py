@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_SCHEME_MISMAT
 EXPORTS = ["kvq_status_string", "kvq_cache_bytes", "kvq_append", "kvq_decode_workspace_bytes",
            "kvq_decode_attn", "kvq_decode_partial", "kvq_decode_merge", "kvq_validate_tables",
            "kvq_last_device_error", "kvq_allocator_create", "kvq_allocator_destroy",
-           "kvq_alloc_pages", "kvq_free_pages", "kvq_allocator_free_count"]
+           "kvq_alloc_pages", "kvq_free_pages", "kvq_allocator_free_count", "kvq_decode_attn_noalloc"]
 
 
 class KvqError(RuntimeError):
@@ -64,6 +64,7 @@ def _load() -> ctypes.CDLL:
     L.kvq_decode_partial.argtypes = dec
     L.kvq_decode_merge.argtypes = dec
     L.kvq_validate_tables.argtypes = [cachep, P, P, i32, i32, P]
+    L.kvq_decode_attn_noalloc.argtypes = [cachep, P, P, P, P, i32, i32, i32, ctypes.c_float, P]
     L.kvq_last_device_error.argtypes = [P]
     L.kvq_allocator_create.argtypes, L.kvq_allocator_create.restype = [i32, ctypes.c_uint64], P
     L.kvq_allocator_destroy.argtypes, L.kvq_allocator_destroy.restype = [P], None
@@ -190,6 +191,22 @@ def decode_attn(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
     q[B, Hq, d] (bf16) over the quantized cache."""
     _decode_call(lib.kvq_decode_attn, "kvq_decode_attn", cache, q, block_table, seq_lens, out,
                  workspace, softmax_scale, stream)
+    return out
+
+
+def decode_attn_noalloc(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                        seq_lens: torch.Tensor, out: torch.Tensor, softmax_scale: float = 0.0,
+                        stream=None) -> torch.Tensor:
+    """kvq_decode_attn_noalloc: decode_attn without a workspace, for callers
+    that cannot allocate device memory; it uses the library's own fixed
+    scratch array (KVQ_STATIC_SCRATCH_BYTES per GPU), so calls that overlap
+    on the GPU race on it."""
+    B = seq_lens.numel()
+    if q.dim() != 3 or q.shape[0] != B or tuple(out.shape) != tuple(q.shape) or block_table.shape[0] != B:
+        raise ValueError("kvq_decode_attn_noalloc: shapes of q, out, block_table, seq_lens do not agree")
+    _check(lib.kvq_decode_attn_noalloc(ctypes.byref(cache.struct), _ptr(q), _ptr(block_table), _ptr(seq_lens),
+                                       _ptr(out), B, q.shape[1], block_table.shape[1], float(softmax_scale),
+                                       _stream(stream)), "kvq_decode_attn_noalloc")
     return out
 
 

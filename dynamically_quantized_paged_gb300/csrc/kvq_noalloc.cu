@@ -1,0 +1,61 @@
+// kvq_noalloc.cu -- kvq_decode_attn_noalloc: decode attention for callers
+// that cannot allocate device memory.
+//
+// Some callers must not call cudaMalloc: code that runs inside another
+// framework's memory pool (a direct allocation bypasses the pool's accounting
+// and fails once the pool holds the device memory), and latency-critical
+// paths that cannot accept the implicit device synchronization an allocation
+// may bring.  kvq_decode_attn asks them for a workspace; this entry point
+// instead uses a fixed scratch array that lives in the library itself.
+//
+// The array is a file-scope __device__ object of KVQ_STATIC_SCRATCH_BYTES
+// bytes: every GPU that loads the library holds it until the process exits.
+// In host code its name is only a host-side stand-in, so the device address
+// is fetched with cudaGetSymbolAddress, once per device, with that device
+// current, on the first call made on that device.  Nothing in it has to start
+// at zero (the decode writes every partial before reading it), and every call
+// shares it: two calls whose kernels overlap on the GPU race on it.
+#include <mutex>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_STATIC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[MAX_DEVICES];
+
+// Device address of the scratch array on the current device (set up on the
+// first call per device); nullptr if the device or the lookup fails.
+void* scratch_on_current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
+        g_scratch_ptr[dev] = ptr;
+    }
+    return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const void* q,
+                                              const int32_t* block_table, const int32_t* seq_lens,
+                                              float* out, int32_t num_seqs, int32_t num_q_heads,
+                                              int32_t max_pages_per_seq, float softmax_scale,
+                                              kvq_stream_t stream) {
+    size_t need = 0;
+    const kvq_status st = kvq_decode_workspace_bytes(cache, num_seqs, num_q_heads, max_pages_per_seq, &need);
+    if (st != KVQ_OK) return st;
+    if (need > (size_t)KVQ_STATIC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;  // beyond the fixed array
+    void* scratch = scratch_on_current_device();
+    if (!scratch) return KVQ_ERR_CUDA;
+    return kvq_decode_attn(cache, q, block_table, seq_lens, out, num_seqs, num_q_heads, max_pages_per_seq,
+                           softmax_scale, scratch, (size_t)KVQ_STATIC_SCRATCH_BYTES, stream);
+}

@@ -15,7 +15,9 @@
  * Conventions shared by every call:
  *  - Every pointer argument named as device memory must be device memory of
  *    the current CUDA device, allocated and owned by the caller.  The library
- *    allocates no device memory and keeps no pointer after a call returns.
+ *    calls no allocator and keeps no pointer after a call returns; its own
+ *    device memory is static: a per-device error word, and the fixed scratch
+ *    array of kvq_decode_attn_noalloc.
  *  - Device buffers must start on a 16-byte boundary (kvq_append,
  *    kvq_decode_*: the page pools, q, k, v, out, workspace).
  *  - Calls that launch work are asynchronous on `stream` (a cudaStream_t;
@@ -189,6 +191,33 @@ kvq_status kvq_validate_tables(const kvq_cache* cache, const int32_t* block_tabl
  * flags: KVQ_OK, KVQ_ERR_BAD_TABLE or KVQ_ERR_DEVICE_TIMEOUT (the latter wins
  * when both are set), or KVQ_ERR_CUDA if the synchronization failed. */
 kvq_status kvq_last_device_error(kvq_stream_t stream);
+
+/* ---- decode without a caller-provided workspace -----------------------------
+ * The pages have no counterpart to this call; it is a convenience of this
+ * library.  It is kvq_decode_attn for callers that cannot allocate device
+ * memory: code running inside another framework's memory pool (a direct
+ * cudaMalloc would bypass the pool's accounting and fail once the pool holds
+ * the device memory) and latency-critical paths that cannot accept the
+ * device synchronization an allocation may bring.
+ *
+ * Instead of a workspace it uses a scratch array of KVQ_STATIC_SCRATCH_BYTES
+ * bytes compiled into the library: every GPU that loads the library holds
+ * that memory until the process exits.  The call allocates nothing.  Its
+ * first call on a device looks up the array's device address (set-up, once
+ * per device, with that device current); make that first call before any
+ * stream capture.  Every call shares the array and leaves its contents
+ * behind; nothing in it needs to start at zero.  Calls whose kernels overlap
+ * on the GPU (other streams, other host threads) race on the array: keep
+ * them ordered.  Returns KVQ_ERR_WORKSPACE, launching nothing, if this
+ * problem would need more scratch than the array holds (kvq_decode_workspace_bytes
+ * reports the need).  Other arguments, rules and errors are those of
+ * kvq_decode_attn. */
+#define KVQ_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+
+kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                                   const int32_t* seq_lens, float* out, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t max_pages_per_seq,
+                                   float softmax_scale, kvq_stream_t stream);
 
 /* ---- host page allocator ([P3] "How vLLM Implements KV Cache
  * Optimization": pages are handed out on demand, only used pages cost
