@@ -19,12 +19,11 @@
 // kernel combines them.  Slices are a function of logical positions only, so
 // physical page placement cannot change the result.
 //
-// Inside a CTA: warp 4 is the producer.  For every unit it looks up the
-// physical page in the block table and issues 1-D bulk copies (TMA) of the K
-// codes, V codes and scales (and INT4 zero-points) of those 16 tokens into a
-// stage of a per-consumer-warp ring, completing on an mbarrier; the query
-// rows of each piece are bulk-copied too.  Warps 0-3 consume units round
-// robin:
+// Inside a CTA (4 warps, no producer warp): every warp streams its own
+// contiguous share of each piece's units through a ring of shared-memory
+// stages with 16-byte cp.async gathers (all 32 lanes issue; page ids come from
+// the block table in 32-entry register batches, the next batch prefetched),
+// keeping STAGES-1 units in flight, and consumes them:
 //  * scores: each lane holds 16 channels of the G query rows as fp16 and
 //    turns 16 codes into fp16 with byte permutes (INT8, INT4: exact integer
 //    plus a constant bias removed once per score) or the E4M3 converter;
@@ -33,9 +32,13 @@
 //    per lane, and the per-token scale is applied once;
 //  * online softmax in base 2 directly on those lanes (max over the unit by
 //    two shuffles), weights p*scale to shared memory;
-//  * values: each lane owns 8 channels x G heads of fp32 accumulators,
+//  * values: each lane owns 8 (or 4) channels x G heads of fp32 accumulators,
 //    updated with packed fp32x2 FMAs on exactly converted codes.
-// At the end of a piece the four warps' states are combined in shared memory.
+// The query rows of a piece travel in the stage of the warp's first unit of
+// that piece.  At the end of a piece the four warps' states are combined in
+// shared memory.  One 1-D bulk copy per issuing thread completes only every
+// few hundred ns on this GPU, so per-lane cp.async gathers, issued by every
+// warp, are what keeps enough bytes in flight.
 #pragma once
 
 #include "kvq_device.cuh"
@@ -47,20 +50,23 @@ template <int SCHEME, int D, int G>
 struct DecodeCfg {
     static constexpr bool INT4 = SCHEME == KVQ_INT4_ASYM_G32;
     static constexpr bool INT8 = SCHEME == KVQ_INT8_SYM_TOKEN;
+    static constexpr int WARPS = DECODE_WARPS;
+    static constexpr int THREADS = 32 * WARPS;
     static constexpr int CB = INT4 ? D / 2 : D;        // code bytes per token row
     static constexpr int NGR = D / 32;                 // INT4 groups per row
     static constexpr int MB = INT4 ? NGR * 2 : 4;      // bytes per token in one scale/zero array
-    // stage layout (bytes)
+    static constexpr int Q_BYTES = G * D * 2;          // the query rows of one (sequence, KV head)
+    // stage layout (bytes): K codes, V codes, K scales, V scales, [K zeros, V zeros], query rows
     static constexpr int KC = 0;
     static constexpr int VC = KC + UNIT * CB;
     static constexpr int KS = VC + UNIT * CB;
     static constexpr int VS = KS + UNIT * MB;
     static constexpr int KZ = VS + UNIT * MB;
     static constexpr int VZ = KZ + (INT4 ? UNIT * MB : 0);
-    static constexpr int STAGE = VZ + (INT4 ? UNIT * MB : 0);
-    static constexpr uint32_t STAGE_TX = STAGE;  // bytes one stage receives
-    static constexpr int STAGES = STAGE >= 4096 ? 3 : 4;  // ring depth per consumer warp
-    // occupancy target: CTAs per SM the register budget is compiled for
+    static constexpr int QO = VZ + (INT4 ? UNIT * MB : 0);
+    static constexpr int STAGE = QO + Q_BYTES;
+    static constexpr int STAGES = (STAGE >= 4096) ? 3 : 4;  // ring depth per warp: STAGES-1 units in flight
+    // occupancy the register budget is compiled for (CTAs per SM)
     static constexpr int MIN_CTAS = (G >= 8) ? 2 : 3;
     // scores: KL lanes per token, CPL channels per lane, TPP tokens per pass
     static constexpr int CPL = (D == 64 && G == 8) ? 8 : 16;
@@ -72,29 +78,24 @@ struct DecodeCfg {
     static constexpr bool TWO_ACC = G <= 2;  // a second accumulator set for more ILP when registers allow
     // values: VCH channels per lane, VL lanes per token, VT token groups
     static constexpr int VCH = (G >= 8 && D == 128) ? 4 : 8;
-    static constexpr int VP = VCH / 2;  // fp32 pairs per head per lane
     static constexpr int VL = D / VCH;
     static constexpr int VT = 32 / VL;
-    static constexpr int V_UNROLL = (G >= 8) ? 2 : UNIT / VT;  // token loop unrolling (register pressure)
+    static constexpr int V_UNROLL = (G >= 8) ? 4 : UNIT / VT;  // token loop unrolling (register pressure)
     // shared memory layout (bytes)
     static constexpr int OFF_STAGES = 0;
-    static constexpr int OFF_Q = OFF_STAGES + CONSUMER_WARPS * STAGES * STAGE;
-    static constexpr int Q_BYTES = G * D * 2;
-    static constexpr int OFF_CO = OFF_Q + 2 * Q_BYTES;
-    static constexpr int OFF_CM = OFF_CO + CONSUMER_WARPS * G * D * 4;
-    static constexpr int OFF_CL = OFF_CM + CONSUMER_WARPS * G * 4;
-    static constexpr int OFF_W = (OFF_CL + CONSUMER_WARPS * G * 4 + 15) / 16 * 16;
-    // per warp: weight pairs Wt[UNIT][G] (w, w) as 8 bytes, then alpha[G]
-    static constexpr int W_BYTES = (UNIT * G * 8 + G * 4 + 15) / 16 * 16;
-    static constexpr int OFF_BAR = OFF_W + CONSUMER_WARPS * W_BYTES;
-    static constexpr int NBAR = 2 * CONSUMER_WARPS * STAGES + 4;
-    static constexpr int OFF_BAD = OFF_BAR + NBAR * 8;  // per stage "page id was invalid" marks
-    static constexpr int OFF_MISC = OFF_BAD + CONSUMER_WARPS * STAGES * 4;
+    static constexpr int OFF_CO = OFF_STAGES + WARPS * STAGES * STAGE;
+    static constexpr int OFF_CM = OFF_CO + WARPS * G * D * 4;
+    static constexpr int OFF_CL = OFF_CM + WARPS * G * 4;
+    static constexpr int OFF_W = (OFF_CL + WARPS * G * 4 + 15) / 16 * 16;
+    // per warp: weights Wt[UNIT][G] (fp32), then alpha[G]
+    static constexpr int W_BYTES = (UNIT * G * 4 + G * 4 + 15) / 16 * 16;
+    static constexpr int OFF_MISC = OFF_W + WARPS * W_BYTES;
     static constexpr int OFF_PLAN = OFF_MISC + 16;
     static size_t smem_bytes(int B) { return OFF_PLAN + (size_t)(B + 1) * 4; }
     static_assert(G <= KL, "each lane must end the reduction holding one head");
-    static_assert(STAGE % 16 == 0 && Q_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
-    static_assert(OFF_Q % 16 == 0 && OFF_CO % 16 == 0 && OFF_W % 16 == 0, "alignment");
+    static_assert(STAGE % 16 == 0 && Q_BYTES % 16 == 0 && (UNIT * MB) % 16 == 0, "16-byte copies");
+    static_assert(OFF_CO % 16 == 0 && OFF_W % 16 == 0, "alignment");
+    static_assert(4 * (UNIT * MB / 16) <= 32, "one lane per 16 bytes of scales and zeros");
 };
 
 // ---- the split plan ------------------------------------------------------------
@@ -126,11 +127,11 @@ __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefi
         local += u;
     }
     // exclusive scan of the per-thread sums by warp 0
-    __shared__ int tsum[DECODE_THREADS];
+    __shared__ int tsum[32 * DECODE_WARPS];
     tsum[tid] = local;
     __syncthreads();
     if (tid < 32) {
-        constexpr int PER = (DECODE_THREADS + 31) / 32;
+        constexpr int PER = DECODE_WARPS;
         int v[PER];
         int s = 0;
 #pragma unroll
@@ -247,55 +248,45 @@ struct PieceWalk {
 // Transpose-reduction across the KL lanes that share a token: N values per
 // lane in, one (fully summed) value out; the lane ends with head
 // (lane % KL) / (KL / G).
-template <int N, int OFF>
-__device__ __forceinline__ void transpose_reduce(float* v, int lane) {
+template <typename T, int N, int OFF>
+__device__ __forceinline__ void transpose_reduce(T* v, int lane) {
     if constexpr (OFF >= 1) {
         if constexpr (N > 1) {
             const bool upper = (lane & OFF) != 0;
 #pragma unroll
             for (int i = 0; i < N / 2; ++i) {
-                const float send = upper ? v[i] : v[i + N / 2];
-                const float keep = upper ? v[i + N / 2] : v[i];
+                const T send = upper ? v[i] : v[i + N / 2];
+                const T keep = upper ? v[i + N / 2] : v[i];
                 v[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
             }
-            transpose_reduce<N / 2, OFF / 2>(v, lane);
+            transpose_reduce<T, N / 2, OFF / 2>(v, lane);
         } else {
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], OFF);
-            transpose_reduce<1, OFF / 2>(v, lane);
+            transpose_reduce<T, 1, OFF / 2>(v, lane);
         }
     }
 }
 
+// This warp's contiguous share [a, b) of a piece's units.
+__device__ __forceinline__ void warp_range(const Piece& pc, int warp, int& a, int& b) {
+    const int n = pc.u_hi - pc.u_lo;
+    const int per = (n + DECODE_WARPS - 1) / DECODE_WARPS;
+    a = pc.u_lo + warp * per;
+    b = min(pc.u_hi, a + per);
+    if (a > b) a = b;
+}
+
 template <int SCHEME, int D, int G>
-__global__ void __launch_bounds__(DECODE_THREADS, (DecodeCfg<SCHEME, D, G>::MIN_CTAS))
+__global__ void __launch_bounds__(DecodeCfg<SCHEME, D, G>::THREADS, (DecodeCfg<SCHEME, D, G>::MIN_CTAS))
 decode_partial_kernel(const DecodeParams p) {
     using C = DecodeCfg<SCHEME, D, G>;
     constexpr int STAGES_ = C::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint64_t* full = bars;                                   // [CW][STAGES]
-    uint64_t* empty = bars + CONSUMER_WARPS * STAGES_;       // [CW][STAGES]
-    uint64_t* qfull = bars + 2 * CONSUMER_WARPS * STAGES_;   // [2]
-    uint64_t* qempty = qfull + 2;                            // [2]
-    int32_t* bad = reinterpret_cast<int32_t*>(smem + C::OFF_BAD);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
     int64_t* misc = reinterpret_cast<int64_t*>(smem + C::OFF_MISC);
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + C::OFF_PLAN);
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < CONSUMER_WARPS * STAGES_; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&qfull[i], 1);
-            mbar_init(&qempty[i], CONSUMER_WARPS);
-        }
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
     const Plan plan = build_plan(p, prefix, misc);  // contains __syncthreads
     if (blockIdx.x == 0) {
         // publish the plan for the merge kernel: [U, S] then prefix[0..B]
@@ -309,95 +300,114 @@ decode_partial_kernel(const DecodeParams p) {
     }
     const int Hkv = p.c.num_kv_heads;
     const int P = p.c.page_size;
+    const uint64_t pol_kv = l2_evict_first_policy();  // pages are read once
+    const uint64_t pol_q = l2_evict_normal_policy();  // query rows are shared by the CTA's warps
+    uint8_t* ring = smem + C::OFF_STAGES + warp * STAGES_ * C::STAGE;
 
-    if (warp == CONSUMER_WARPS) {
-        // ------------------------------------------------------------ producer
-        const uint64_t pol = l2_evict_first_policy();
-        int cnt0 = 0, cnt1 = 0, cnt2 = 0, cnt3 = 0;
-        PieceWalk walk;
-        walk.begin(plan, prefix, blockIdx.x);
-        int pi = 0;
-        for (; !walk.done(); walk.next(), ++pi) {
-            const Piece pc = walk.get(p);
-            if (lane == 0 && !*abort_flag) {
-                const int qs = pi & 1;
-                if (!mbar_wait(&qempty[qs], ((pi >> 1) & 1) ^ 1)) {
-                    flag_error(p.err, ERR_TIMEOUT);
-                    *abort_flag = 1;
-                } else {
-                    mbar_arrive_expect_tx(&qfull[qs], C::Q_BYTES);
-                    bulk_load(smem + C::OFF_Q + qs * C::Q_BYTES,
-                              p.q + ((int64_t)pc.b * p.Hq + (int64_t)pc.h * G) * D, C::Q_BYTES,
-                              &qfull[qs], pol);
-                }
+    // ---------------------------------------------------------------- feed
+    // Issues this warp's units, in the order the compute loop below consumes
+    // them, STAGES-1 units ahead.  Every call commits exactly one cp.async
+    // group (empty once the units run out).
+    PieceWalk fw;
+    fw.begin(plan, prefix, blockIdx.x);
+    Piece fpc;
+    fpc.b = fpc.h = fpc.u_lo = fpc.u_hi = fpc.len = fpc.slot = 0;
+    fpc.whole = false;
+    int fu = 0, fua = 0, fub = 0;
+    int flp = 0, foff = 0;  // logical page of unit fu and its token offset inside the page
+    bool fdone = true;
+    auto feed_seek = [&]() {
+        fdone = true;
+        while (!fw.done()) {
+            fpc = fw.get(p);
+            warp_range(fpc, warp, fua, fub);
+            if (fua < fub) {
+                fu = fua;
+                flp = (fu * UNIT) / P;  // once per piece; then advanced incrementally
+                foff = (fu * UNIT) - flp * P;
+                fdone = false;
+                return;
             }
-            const int32_t* bt_row = p.block_table + (int64_t)pc.b * p.max_pages;
-            int batch0 = -1;  // first logical page of the loaded batch
-            int pid = -1;
-            for (int ub = pc.u_lo; ub < pc.u_hi; ub += CONSUMER_WARPS) {
+            fw.next();
+        }
+    };
+    feed_seek();
+    int bt_b = -1, bt0 = 0, pid = -1, pid_next = -1;  // block-table batch [bt0, bt0 + 32) and the next one
+    uint32_t badmask = 0;                             // stages whose page id was outside the pool
+    int ist = 0;                                      // stage the next issue fills
+    auto issue_one = [&]() {
+        if (!fdone) {
+            const int st = ist;
+            uint8_t* stg = ring + st * C::STAGE;
+            const int lp = flp;  // logical page of this unit
+            const int32_t* bt_row = p.block_table + (int64_t)fpc.b * p.max_pages;
+            if (fpc.b != bt_b || lp < bt0 || lp >= bt0 + 64) {
+                bt_b = fpc.b;
+                bt0 = lp;
+                pid = (bt0 + lane < p.max_pages) ? __ldg(bt_row + bt0 + lane) : -1;
+                pid_next = (bt0 + 32 + lane < p.max_pages) ? __ldg(bt_row + bt0 + 32 + lane) : -1;
+            } else if (lp >= bt0 + 32) {
+                bt0 += 32;
+                pid = pid_next;
+                pid_next = (bt0 + 32 + lane < p.max_pages) ? __ldg(bt_row + bt0 + 32 + lane) : -1;
+            }
+            const int page = __shfl_sync(0xffffffffu, pid, lp - bt0);
+            if (fu == fua) {  // the piece's query rows travel with the warp's first unit
+                const uint8_t* qsrc =
+                    reinterpret_cast<const uint8_t*>(p.q + ((int64_t)fpc.b * p.Hq + (int64_t)fpc.h * G) * D);
+                constexpr int NQ = C::Q_BYTES / 16;
 #pragma unroll
-                for (int w = 0; w < CONSUMER_WARPS; ++w) {
-                    const int u = ub + w;
-                    if (u >= pc.u_hi) break;
-                    const int lp = (u * UNIT) / P;  // logical page
-                    if (batch0 < 0 || lp >= batch0 + 32) {
-                        batch0 = lp;
-                        const int k = batch0 + lane;
-                        pid = (k < p.max_pages) ? __ldg(bt_row + k) : -1;
-                    }
-                    const int page = __shfl_sync(0xffffffffu, pid, lp - batch0);
-                    int& cnt = (w == 0) ? cnt0 : (w == 1) ? cnt1 : (w == 2) ? cnt2 : cnt3;
-                    if (lane == 0 && !*abort_flag) {
-                        const int st = cnt % STAGES_;
-                        const int k = cnt / STAGES_;
-                        const int bi = w * STAGES_ + st;
-                        if (!mbar_wait(&empty[bi], (k & 1) ^ 1)) {
-                            flag_error(p.err, ERR_TIMEOUT);
-                            *abort_flag = 1;
-                        } else if (page < 0 || page >= p.c.num_pages) {
-                            flag_error(p.err, ERR_BAD_TABLE);
-                            bad[bi] = 1;
-                            mbar_arrive(&full[bi]);  // completes the phase with no data
-                        } else {
-                            bad[bi] = 0;
-                            const int64_t row = ((int64_t)page * Hkv + pc.h) * P + (u * UNIT) % P;
-                            uint8_t* st_ptr = smem + C::OFF_STAGES + bi * C::STAGE;
-                            mbar_arrive_expect_tx(&full[bi], C::STAGE_TX);
-                            bulk_load(st_ptr + C::KC, p.c.k_codes + row * C::CB, UNIT * C::CB, &full[bi], pol);
-                            bulk_load(st_ptr + C::VC, p.c.v_codes + row * C::CB, UNIT * C::CB, &full[bi], pol);
-                            bulk_load(st_ptr + C::KS, static_cast<const uint8_t*>(p.c.k_scales) + row * C::MB,
-                                      UNIT * C::MB, &full[bi], pol);
-                            bulk_load(st_ptr + C::VS, static_cast<const uint8_t*>(p.c.v_scales) + row * C::MB,
-                                      UNIT * C::MB, &full[bi], pol);
-                            if constexpr (C::INT4) {
-                                bulk_load(st_ptr + C::KZ, static_cast<const uint8_t*>(p.c.k_zeros) + row * C::MB,
-                                          UNIT * C::MB, &full[bi], pol);
-                                bulk_load(st_ptr + C::VZ, static_cast<const uint8_t*>(p.c.v_zeros) + row * C::MB,
-                                          UNIT * C::MB, &full[bi], pol);
-                            }
-                        }
-                    }
-                    ++cnt;
+                for (int k = 0; k < (NQ + 31) / 32; ++k) {
+                    const int i = k * 32 + lane;
+                    if (NQ % 32 == 0 || i < NQ) cp_async16(stg + C::QO + 16 * i, qsrc + 16 * i, pol_q);
                 }
             }
-            __syncwarp();
+            if (page >= 0 && page < p.c.num_pages) {
+                badmask &= ~(1u << st);
+                const int64_t row = ((int64_t)page * Hkv + fpc.h) * P + foff;
+                const uint8_t* kc = p.c.k_codes + row * C::CB;
+                const uint8_t* vc = p.c.v_codes + row * C::CB;
+                constexpr int NC = UNIT * C::CB / 16;  // 16-byte pieces of one code run
+#pragma unroll
+                for (int k = 0; k < (NC + 31) / 32; ++k) {
+                    const int i = k * 32 + lane;
+                    if (NC % 32 == 0 || i < NC) {
+                        cp_async16(stg + C::KC + 16 * i, kc + 16 * i, pol_kv);
+                        cp_async16(stg + C::VC + 16 * i, vc + 16 * i, pol_kv);
+                    }
+                }
+                constexpr int NS = UNIT * C::MB / 16;  // 16-byte pieces of one scale (or zero) run
+                const int which = lane / NS, part = lane % NS;
+                const void* src = nullptr;
+                int dst = 0;
+                if (which == 0) { src = p.c.k_scales; dst = C::KS; }
+                else if (which == 1) { src = p.c.v_scales; dst = C::VS; }
+                else if (C::INT4 && which == 2) { src = p.c.k_zeros; dst = C::KZ; }
+                else if (C::INT4 && which == 3) { src = p.c.v_zeros; dst = C::VZ; }
+                if (src) cp_async16(stg + dst + 16 * part, static_cast<const uint8_t*>(src) + row * C::MB + 16 * part, pol_kv);
+            } else {
+                badmask |= (1u << st);
+                if (lane == 0) flag_error(p.err, ERR_BAD_TABLE);
+            }
+            foff += UNIT;
+            if (foff == P) {
+                foff = 0;
+                ++flp;
+            }
+            if (++fu == fub) {
+                fw.next();
+                feed_seek();
+            }
         }
-        // After a timeout, let every copy already issued land before the CTA's
-        // shared memory can be reused (bounded again).
-        if (lane == 0 && *abort_flag) {
-            const int cnts[4] = {cnt0, cnt1, cnt2, cnt3};
-            for (int w = 0; w < CONSUMER_WARPS; ++w)
-                for (int k = (cnts[w] > STAGES_ ? cnts[w] - STAGES_ : 0); k < cnts[w]; ++k)
-                    mbar_wait(&full[w * STAGES_ + k % STAGES_], (k / STAGES_) & 1);
-        }
-        return;
-    }
+        cp_async_commit();
+        ist = (ist + 1 == STAGES_) ? 0 : ist + 1;
+    };
 
-    // ---------------------------------------------------------------- consumers
-    const int tid = threadIdx.x;  // 0 .. 127
+    // ---------------------------------------------------------------- compute
+    const int tid = threadIdx.x;
     uint8_t* wbase = smem + C::OFF_W + warp * C::W_BYTES;
-    uint64_t* Wt = reinterpret_cast<uint64_t*>(wbase);             // [UNIT][G] (w, w)
-    float* AL = reinterpret_cast<float*>(wbase + UNIT * G * 8);    // [G]
+    float* Wt = reinterpret_cast<float*>(wbase);                   // [UNIT][G]
+    float* AL = reinterpret_cast<float*>(wbase + UNIT * G * 4);    // [G]
     float* CO = reinterpret_cast<float*>(smem + C::OFF_CO);
     float* CM = reinterpret_cast<float*>(smem + C::OFF_CM);
     float* CL = reinterpret_cast<float*>(smem + C::OFF_CL);
@@ -411,91 +421,106 @@ decode_partial_kernel(const DecodeParams p) {
     const int v_tok = lane / C::VL;
     const float qk_scale = p.q_scale;  // softmax scale * log2(e)
 
-    int cnt = 0;
+#pragma unroll 1
+    for (int i = 0; i < STAGES_ - 1; ++i) issue_one();  // prologue
+    int cst = 0;  // stage the next computed unit sits in
     PieceWalk walk;
     walk.begin(plan, prefix, blockIdx.x);
-    int pi = 0;
-    for (; !walk.done(); walk.next(), ++pi) {
+    for (; !walk.done(); walk.next()) {
         const Piece pc = walk.get(p);
-        // ---- query rows of this piece -> fp16 pairs in registers
-        uint32_t qh[G][C::QW];
-        float qsum[G];         // INT4: sum of the query over this lane's channels, per head
-        float my_qsum = 0.0f;  // INT8: sum of the query over all channels, this lane's head
-        {
-            const int qs = pi & 1;
-            if (!*abort_flag && !mbar_wait(&qfull[qs], (pi >> 1) & 1)) {
-                flag_error(p.err, ERR_TIMEOUT);
-                *abort_flag = 1;
-            }
-            const uint16_t* qb = reinterpret_cast<const uint16_t*>(smem + C::OFF_Q + qs * C::Q_BYTES);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float qf[C::CPL];
-#pragma unroll
-                for (int j = 0; j < C::CPL; j += 8) {
-                    const uint4 raw = *reinterpret_cast<const uint4*>(qb + g * D + k_c0 + j);
-                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        qf[j + 2 * i] = __half2float(__float2half_rn(bf16_bits_to_float(w4[i] & 0xFFFFu)));
-                        qf[j + 2 * i + 1] = __half2float(__float2half_rn(bf16_bits_to_float(w4[i] >> 16)));
-                    }
-                }
-                float s = 0.0f;
-#pragma unroll
-                for (int j = 0; j < C::CPL; ++j) s += qf[j];
-                qsum[g] = s;
-#pragma unroll
-                for (int i = 0; i < C::QW; ++i) {
-                    int a, b2;
-                    if constexpr (C::INT4) {  // pair (s, s+4) inside each 8-channel word
-                        a = (i / 4) * 8 + (i % 4);
-                        b2 = a + 4;
-                    } else {                  // consecutive channels
-                        a = 2 * i;
-                        b2 = 2 * i + 1;
-                    }
-                    const __half2 h = __floats2half2_rn(qf[a], qf[b2]);
-                    qh[g][i] = *reinterpret_cast<const uint32_t*>(&h);
-                }
-            }
-            if constexpr (C::INT8) {  // full-row sums for the bias correction
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int off = C::KL / 2; off >= 1; off >>= 1) qsum[g] += __shfl_xor_sync(0xffffffffu, qsum[g], off);
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    if (g == k_head) my_qsum = qsum[g];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&qempty[qs]);
-        }
-
+        int ua, ub;
+        warp_range(pc, warp, ua, ub);
+        uint32_t qw[G][C::QW];  // query: INT8/INT4 fixed-point bytes, FP8 fp16 pairs
+        float sq[G];            // INT4: fixed-point step per head
+        float qisum[G];         // INT4: sum of this lane's fixed-point query channels, per head
+        float my_sq = 0.0f;     // INT8: fixed-point step of this lane's head times the softmax scale
         float m_run = -INFINITY, l_run = 0.0f;
-        uint64_t o[G][C::VP];
+        float o[G][C::VCH];
         float zacc[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             zacc[g] = 0.0f;
+            sq[g] = 0.0f;
+            qisum[g] = 0.0f;
 #pragma unroll
-            for (int j = 0; j < C::VP; ++j) o[g][j] = 0ull;
+            for (int j = 0; j < C::VCH; ++j) o[g][j] = 0.0f;
         }
 
-        for (int j = warp; j < pc.u_hi - pc.u_lo; j += CONSUMER_WARPS, ++cnt) {
-            const int st = cnt % STAGES_;
-            const int bi = warp * STAGES_ + st;
-            bool ok = !*abort_flag;
-            if (ok && !mbar_wait(&full[bi], (cnt / STAGES_) & 1)) {
-                flag_error(p.err, ERR_TIMEOUT);
-                *abort_flag = 1;
-                ok = false;
+        for (int u = ua; u < ub; ++u) {
+            issue_one();
+            cp_async_wait<STAGES_ - 1>();  // this unit's group has landed
+            __syncwarp();
+            const int st = cst;
+            cst = (cst + 1 == STAGES_) ? 0 : cst + 1;
+            const uint8_t* stg = ring + st * C::STAGE;
+            if (u == ua) {
+                // ---- query rows of this piece -> fp16 pairs in registers
+                const uint16_t* qb = reinterpret_cast<const uint16_t*>(stg + C::QO);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float qf[C::CPL];
+#pragma unroll
+                    for (int j = 0; j < C::CPL; j += 8) {
+                        const uint4 raw = *reinterpret_cast<const uint4*>(qb + g * D + k_c0 + j);
+                        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            qf[j + 2 * i] = bf16_bits_to_float(w4[i] & 0xFFFFu);
+                            qf[j + 2 * i + 1] = bf16_bits_to_float(w4[i] >> 16);
+                        }
+                    }
+                    if constexpr (C::INT8 || C::INT4) {
+                        // 16-bit fixed point per (query head): q ~ sq * qi, qi = 256 hi + lo,
+                        // hi a signed byte, lo an unsigned byte (error <= sq / 2 per element)
+                        float amax = 0.0f;
+#pragma unroll
+                        for (int j = 0; j < C::CPL; ++j) amax = fmaxf(amax, fabsf(qf[j]));
+#pragma unroll
+                        for (int off = C::KL / 2; off >= 1; off >>= 1)
+                            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                        const float inv = amax > 0.0f ? 32767.0f / amax : 0.0f;
+                        const float sqg = amax / 32767.0f;
+                        int qi[C::CPL];
+                        int isum = 0;
+#pragma unroll
+                        for (int j = 0; j < C::CPL; ++j) {
+                            qi[j] = __float2int_rn(qf[j] * inv);
+                            isum += qi[j];
+                        }
+                        auto hb = [&](int j) { return (uint32_t)((qi[j] >> 8) & 0xFF); };
+                        auto lb = [&](int j) { return (uint32_t)(qi[j] & 0xFF); };
+                        if constexpr (C::INT8) {  // consecutive channels, hi words then lo words
+                            constexpr int NQW = C::CPL / 4;
+#pragma unroll
+                            for (int i = 0; i < NQW; ++i) {
+                                qw[g][i] = hb(4 * i) | (hb(4 * i + 1) << 8) | (hb(4 * i + 2) << 16) | (hb(4 * i + 3) << 24);
+                                qw[g][NQW + i] = lb(4 * i) | (lb(4 * i + 1) << 8) | (lb(4 * i + 2) << 16) | (lb(4 * i + 3) << 24);
+                            }
+                            if (g == k_head) my_sq = sqg * qk_scale;
+                        } else {  // per 8-channel word: even-channel and odd-channel bytes
+#pragma unroll
+                            for (int i = 0; i < C::CPL / 8; ++i) {
+                                const int b0 = 8 * i;
+                                qw[g][4 * i + 0] = hb(b0) | (hb(b0 + 2) << 8) | (hb(b0 + 4) << 16) | (hb(b0 + 6) << 24);
+                                qw[g][4 * i + 1] = hb(b0 + 1) | (hb(b0 + 3) << 8) | (hb(b0 + 5) << 16) | (hb(b0 + 7) << 24);
+                                qw[g][4 * i + 2] = lb(b0) | (lb(b0 + 2) << 8) | (lb(b0 + 4) << 16) | (lb(b0 + 6) << 24);
+                                qw[g][4 * i + 3] = lb(b0 + 1) | (lb(b0 + 3) << 8) | (lb(b0 + 5) << 16) | (lb(b0 + 7) << 24);
+                            }
+                            sq[g] = sqg;
+                            qisum[g] = (float)isum;
+                        }
+                    } else {  // FP8: the query as fp16 pairs of consecutive channels
+#pragma unroll
+                        for (int i = 0; i < C::QW; ++i) {
+                            const __half2 h = __floats2half2_rn(qf[2 * i], qf[2 * i + 1]);
+                            qw[g][i] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                    }
+                }
             }
-            const int tok0 = (pc.u_lo + j) * UNIT;
-            int n_valid = pc.len - tok0;
+            int n_valid = pc.len - u * UNIT;
             n_valid = n_valid > UNIT ? UNIT : n_valid;
-            if (!ok || bad[bi]) n_valid = 0;
-            const uint8_t* stg = smem + C::OFF_STAGES + bi * C::STAGE;
+            if (badmask & (1u << st)) n_valid = 0;
 
             if (n_valid > 0) {
                 // ---- scores for G heads x UNIT tokens
@@ -503,18 +528,72 @@ decode_partial_kernel(const DecodeParams p) {
 #pragma unroll
                 for (int pass = 0; pass < C::PASSES; ++pass) {
                     const int t = pass * C::TPP + k_tok;
-                    constexpr int NA1 = C::TWO_ACC ? G : 1;
-                    float acc[G], acc1[NA1];
+                    float s;
+                    if constexpr (C::INT8) {
+                        const int8_t* src8 = reinterpret_cast<const int8_t*>(stg + C::KC + t * D + k_c0);
+                        int wv[C::CPL / 4];
+                        if constexpr (C::CPL == 16) {
+                            const int4 r = *reinterpret_cast<const int4*>(src8);
+                            wv[0] = r.x; wv[1] = r.y; wv[2] = r.z; wv[3] = r.w;
+                        } else {
+                            const int2 r = *reinterpret_cast<const int2*>(src8);
+                            wv[0] = r.x; wv[1] = r.y;
+                        }
+                        constexpr int NQW = C::CPL / 4;
+                        int ai[G];
 #pragma unroll
-                    for (int g = 0; g < G; ++g) acc[g] = 0.0f;
+                        for (int g = 0; g < G; ++g) {
+                            int ah = 0, al = 0;
 #pragma unroll
-                    for (int g = 0; g < NA1; ++g) acc1[g] = 0.0f;
-                    // acc[g] (+ acc1[g]) += q_g . c over this lane's channels
-                    auto dot2 = [&](int g, uint32_t q2, uint32_t c2) {
-                        if constexpr (C::TWO_ACC) mfma_h2(q2, c2, acc[g], acc1[g % NA1]);
-                        else mfma_h2_1(q2, c2, acc[g]);
-                    };
-                    if constexpr (!C::INT4) {
+                            for (int i = 0; i < NQW; ++i) {
+                                ah = dp4a_ss((int)qw[g][i], wv[i], ah);
+                                al = dp4a_us(qw[g][NQW + i], wv[i], al);
+                            }
+                            ai[g] = ah * 256 + al;  // exact: |sum| < 2^30
+                        }
+                        transpose_reduce<int, G, C::KL / 2>(ai, lane);
+                        s = (float)ai[0] * (my_sq * reinterpret_cast<const float*>(stg + C::KS)[t]);
+                    } else if constexpr (C::INT4) {
+                        const uint8_t* src = stg + C::KC + t * (D / 2) + k_c0 / 2;
+                        uint32_t wv[C::CPL / 8];
+                        if constexpr (C::CPL == 16) {
+                            const uint2 r = *reinterpret_cast<const uint2*>(src);
+                            wv[0] = r.x; wv[1] = r.y;
+                        } else {
+                            wv[0] = *reinterpret_cast<const uint32_t*>(src);
+                        }
+                        uint32_t ev[C::CPL / 8], od[C::CPL / 8];
+#pragma unroll
+                        for (int i = 0; i < C::CPL / 8; ++i) {
+                            ev[i] = wv[i] & 0x0F0F0F0Fu;         // even channels as bytes
+                            od[i] = (wv[i] >> 4) & 0x0F0F0F0Fu;  // odd channels as bytes
+                        }
+                        const int gi = t * C::NGR + k_c0 / 32;
+                        const float ks = __half2float(reinterpret_cast<const __half*>(stg + C::KS)[gi]);
+                        const float kz = __half2float(reinterpret_cast<const __half*>(stg + C::KZ)[gi]);
+                        float part[G];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            int ah = 0, al = 0;
+#pragma unroll
+                            for (int i = 0; i < C::CPL / 8; ++i) {
+                                ah = dp4a_su((int)qw[g][4 * i + 0], ev[i], ah);
+                                ah = dp4a_su((int)qw[g][4 * i + 1], od[i], ah);
+                                al = dp4a_uu(qw[g][4 * i + 2], ev[i], al);
+                                al = dp4a_uu(qw[g][4 * i + 3], od[i], al);
+                            }
+                            // sum_j q_j (scale * code_j + zero) over this lane's channels
+                            part[g] = sq[g] * fmaf(ks, (float)(ah * 256 + al), kz * qisum[g]);
+                        }
+                        transpose_reduce<float, G, C::KL / 2>(part, lane);
+                        s = part[0] * qk_scale;
+                    } else {
+                        constexpr int NA1 = C::TWO_ACC ? G : 1;
+                        float acc[G], acc1[NA1];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) acc[g] = 0.0f;
+#pragma unroll
+                        for (int g = 0; g < NA1; ++g) acc1[g] = 0.0f;
                         const uint8_t* src = stg + C::KC + t * D + k_c0;
                         uint32_t wv[C::CPL / 4];
                         if constexpr (C::CPL == 16) {
@@ -526,58 +605,24 @@ decode_partial_kernel(const DecodeParams p) {
                         }
 #pragma unroll
                         for (int i = 0; i < C::CPL / 4; ++i) {
-                            uint32_t c01, c23;
-                            if constexpr (C::INT8) {
-                                const uint32_t u = wv[i] ^ 0x80808080u;
-                                c01 = s8x2_to_h2_biased(u, 0);
-                                c23 = s8x2_to_h2_biased(u, 1);
-                            } else {
-                                c01 = e4m3x2_to_h2(wv[i]);
-                                c23 = e4m3x2_to_h2(wv[i] >> 16);
-                            }
+                            const uint32_t c01 = e4m3x2_to_h2(wv[i]);
+                            const uint32_t c23 = e4m3x2_to_h2(wv[i] >> 16);
 #pragma unroll
                             for (int g = 0; g < G; ++g) {
-                                dot2(g, qh[g][2 * i], c01);
-                                dot2(g, qh[g][2 * i + 1], c23);
+                                if constexpr (C::TWO_ACC) {
+                                    mfma_h2(qw[g][2 * i], c01, acc[g], acc1[g % NA1]);
+                                    mfma_h2(qw[g][2 * i + 1], c23, acc[g], acc1[g % NA1]);
+                                } else {
+                                    mfma_h2_1(qw[g][2 * i], c01, acc[g]);
+                                    mfma_h2_1(qw[g][2 * i + 1], c23, acc[g]);
+                                }
                             }
                         }
                         if constexpr (C::TWO_ACC) {
 #pragma unroll
                             for (int g = 0; g < G; ++g) acc[g] += acc1[g % NA1];
                         }
-                    } else {
-                        const uint8_t* src = stg + C::KC + t * (D / 2) + k_c0 / 2;
-                        uint32_t wv[C::CPL / 8];
-                        if constexpr (C::CPL == 16) {
-                            const uint2 r = *reinterpret_cast<const uint2*>(src);
-                            wv[0] = r.x; wv[1] = r.y;
-                        } else {
-                            wv[0] = *reinterpret_cast<const uint32_t*>(src);
-                        }
-#pragma unroll
-                        for (int i = 0; i < C::CPL / 8; ++i) {
-#pragma unroll
-                            for (int s = 0; s < 4; ++s) {
-                                const uint32_t c2 = u4pair_to_h2_biased(wv[i], s);
-#pragma unroll
-                                for (int g = 0; g < G; ++g) dot2(g, qh[g][4 * i + s], c2);
-                            }
-                        }
-                        const int gi = t * C::NGR + k_c0 / 32;
-                        const float ks = __half2float(reinterpret_cast<const __half*>(stg + C::KS)[gi]);
-                        const float kz = __half2float(reinterpret_cast<const __half*>(stg + C::KZ)[gi]);
-                        const float zc = fmaf(-U4_H2_BIAS, ks, kz);  // zero - 1024 * scale
-#pragma unroll
-                        for (int g = 0; g < G; ++g)
-                            acc[g] = fmaf(ks, C::TWO_ACC ? acc[g] + acc1[g % NA1] : acc[g], zc * qsum[g]);
-                    }
-                    transpose_reduce<G, C::KL / 2>(acc, lane);
-                    float s;
-                    if constexpr (C::INT8) {
-                        s = fmaf(-S8_H2_BIAS, my_qsum, acc[0]) * (reinterpret_cast<const float*>(stg + C::KS)[t] * qk_scale);
-                    } else if constexpr (C::INT4) {
-                        s = acc[0] * qk_scale;
-                    } else {
+                        transpose_reduce<float, G, C::KL / 2>(acc, lane);
                         s = acc[0] * (reinterpret_cast<const float*>(stg + C::KS)[t] * qk_scale);
                     }
                     sc[pass] = (t < n_valid) ? s : -INFINITY;
@@ -599,7 +644,7 @@ decode_partial_kernel(const DecodeParams p) {
                     if (k_writer) {
                         float wv = pr;
                         if constexpr (!C::INT4) wv = (t < n_valid) ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
-                        Wt[t * G + k_head] = f2pack(wv, wv);
+                        Wt[t * G + k_head] = wv;
                     }
                 }
                 l_run = l_run * alpha + psum;
@@ -612,19 +657,17 @@ decode_partial_kernel(const DecodeParams p) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         const float a = AL[g];
-                        const uint64_t a2 = f2pack(a, a);
                         zacc[g] *= a;
 #pragma unroll
-                        for (int jj = 0; jj < C::VP; ++jj) o[g][jj] = fmul2(o[g][jj], a2);
+                        for (int jj = 0; jj < C::VCH; ++jj) o[g][jj] *= a;
                     }
                 }
 #pragma unroll(C::V_UNROLL)
                 for (int k = 0; k < UNIT / C::VT; ++k) {
                     const int t = v_tok + k * C::VT;
                     if (t < n_valid) {
-                        uint64_t c2[C::VP];
+                        float c[C::VCH];  // this lane's codes of token t, exactly as fp32
                         if constexpr (C::INT8) {
-                            const uint64_t bias = f2pack(-8388736.0f, -8388736.0f);
                             uint32_t words[C::VCH / 4];
                             if constexpr (C::VCH == 8) {
                                 const uint2 r = *reinterpret_cast<const uint2*>(stg + C::VC + t * D + v_c0);
@@ -634,13 +677,7 @@ decode_partial_kernel(const DecodeParams p) {
                                 words[0] = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * D + v_c0);
                             }
 #pragma unroll
-                            for (int i = 0; i < C::VCH / 4; ++i) {
-                                const uint32_t u = words[i] ^ 0x80808080u;
-                                c2[2 * i] = fadd2(f2pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
-                                                         __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))), bias);
-                                c2[2 * i + 1] = fadd2(f2pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
-                                                             __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))), bias);
-                            }
+                            for (int i = 0; i < C::VCH / 4; ++i) s8x4_to_float(words[i], c + 4 * i);
                         } else if constexpr (!C::INT4) {
                             uint32_t words[C::VCH / 4];
                             if constexpr (C::VCH == 8) {
@@ -651,51 +688,47 @@ decode_partial_kernel(const DecodeParams p) {
                                 words[0] = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * D + v_c0);
                             }
 #pragma unroll
-                            for (int i = 0; i < C::VP; ++i) {
-                                const uint32_t hw = e4m3x2_to_h2(words[i / 2] >> (16 * (i % 2)));
-                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw));
-                                c2[i] = f2pack(f.x, f.y);
-                            }
+                            for (int i = 0; i < C::VCH / 4; ++i) e4m3x4_to_float(words[i], c + 4 * i);
                         } else {
                             uint32_t r;
                             if constexpr (C::VCH == 8) r = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * (D / 2) + v_c0 / 2);
                             else r = *reinterpret_cast<const uint16_t*>(stg + C::VC + t * (D / 2) + v_c0 / 2);
-                            const uint64_t bias = f2pack(-8388608.0f, -8388608.0f);
 #pragma unroll
-                            for (int i = 0; i < C::VP; ++i) {
-                                const float lo = __uint_as_float(((r >> (8 * i)) & 0xFu) | 0x4B000000u);
-                                const float hi = __uint_as_float(((r >> (8 * i + 4)) & 0xFu) | 0x4B000000u);
-                                c2[i] = fadd2(f2pack(lo, hi), bias);
+                            for (int i = 0; i < C::VCH; ++i)
+                                c[i] = __uint_as_float(((r >> (4 * i)) & 0xFu) | 0x4B000000u) - 8388608.0f;
+                        }
+                        float wg[G];
+#pragma unroll
+                        for (int g = 0; g < G; g += 4) {
+                            if constexpr (G >= 4) {
+                                const float4 w4 = *reinterpret_cast<const float4*>(Wt + t * G + g);
+                                wg[g] = w4.x; wg[g + 1] = w4.y; wg[g + 2] = w4.z; wg[g + 3] = w4.w;
+                            } else {
+#pragma unroll
+                                for (int gg = 0; gg < G; ++gg) wg[gg] = Wt[t * G + gg];
                             }
                         }
                         if constexpr (!C::INT4) {
 #pragma unroll
-                            for (int g = 0; g < G; ++g) {
-                                const uint64_t w2 = Wt[t * G + g];
+                            for (int g = 0; g < G; ++g)
 #pragma unroll
-                                for (int jj = 0; jj < C::VP; ++jj) o[g][jj] = ffma2(c2[jj], w2, o[g][jj]);
-                            }
+                                for (int jj = 0; jj < C::VCH; ++jj) o[g][jj] = fmaf(wg[g], c[jj], o[g][jj]);
                         } else {
                             const int gi = t * C::NGR + v_c0 / 32;
                             const float vs = __half2float(reinterpret_cast<const __half*>(stg + C::VS)[gi]);
                             const float vz = __half2float(reinterpret_cast<const __half*>(stg + C::VZ)[gi]);
-                            const uint64_t s2 = f2pack(vs, vs);
 #pragma unroll
                             for (int g = 0; g < G; ++g) {
-                                const uint64_t w2 = Wt[t * G + g];
-                                float wl, wh;
-                                f2unpack(w2, wl, wh);
-                                zacc[g] = fmaf(wl, vz, zacc[g]);
-                                const uint64_t a2 = fmul2(w2, s2);
+                                zacc[g] = fmaf(wg[g], vz, zacc[g]);
+                                const float a = wg[g] * vs;
 #pragma unroll
-                                for (int jj = 0; jj < C::VP; ++jj) o[g][jj] = ffma2(c2[jj], a2, o[g][jj]);
+                                for (int jj = 0; jj < C::VCH; ++jj) o[g][jj] = fmaf(a, c[jj], o[g][jj]);
                             }
                         }
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[bi]);
         }
 
         // ---- per-warp state -> shared memory
@@ -704,46 +737,37 @@ decode_partial_kernel(const DecodeParams p) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
 #pragma unroll
-            for (int jj = 0; jj < C::VP; ++jj) {
-                float lo, hi;
-                f2unpack(o[g][jj], lo, hi);
-                lo += zacc[g];
-                hi += zacc[g];
+            for (int jj = 0; jj < C::VCH; ++jj) {
+                float v = o[g][jj] + zacc[g];
 #pragma unroll
-                for (int off = C::VL; off < 32; off <<= 1) {
-                    lo += __shfl_xor_sync(0xffffffffu, lo, off);
-                    hi += __shfl_xor_sync(0xffffffffu, hi, off);
-                }
-                o[g][jj] = f2pack(lo, hi);
+                for (int off = C::VL; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                o[g][jj] = v;
             }
         }
         if (v_tok == 0) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float f[C::VCH];
-#pragma unroll
-                for (int jj = 0; jj < C::VP; ++jj) f2unpack(o[g][jj], f[2 * jj], f[2 * jj + 1]);
                 float* dst = CO + (warp * G + g) * D + v_c0;
 #pragma unroll
                 for (int jj = 0; jj < C::VCH; jj += 4)
-                    *reinterpret_cast<float4*>(dst + jj) = make_float4(f[jj], f[jj + 1], f[jj + 2], f[jj + 3]);
+                    *reinterpret_cast<float4*>(dst + jj) = make_float4(o[g][jj], o[g][jj + 1], o[g][jj + 2], o[g][jj + 3]);
             }
         }
         if (k_writer && k_tok == 0) {
             CM[warp * G + k_head] = m_run;
             CL[warp * G + k_head] = l_run;
         }
-        named_barrier_sync(1, 32 * CONSUMER_WARPS);
+        __syncthreads();
         // ---- combine the warps; final row or split partial
-        for (int idx = tid; idx < G * D; idx += 32 * CONSUMER_WARPS) {
+        for (int idx = tid; idx < G * D; idx += C::THREADS) {
             const int g = idx / D;
             const int jj = idx % D;
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < CONSUMER_WARPS; ++w) M = fmaxf(M, CM[w * G + g]);
+            for (int w = 0; w < C::WARPS; ++w) M = fmaxf(M, CM[w * G + g]);
             float L = 0.0f, O = 0.0f;
 #pragma unroll
-            for (int w = 0; w < CONSUMER_WARPS; ++w) {
+            for (int w = 0; w < C::WARPS; ++w) {
                 const float mw = CM[w * G + g];
                 const float f = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - M);
                 L = fmaf(CL[w * G + g], f, L);
@@ -759,8 +783,9 @@ decode_partial_kernel(const DecodeParams p) {
                 }
             }
         }
-        named_barrier_sync(1, 32 * CONSUMER_WARPS);
+        __syncthreads();
     }
+    cp_async_wait<0>();
 }
 
 // ---- K3: merge ------------------------------------------------------------------
@@ -829,7 +854,7 @@ int decode_ctas_per_sm_t(int B) {
     using C = DecodeCfg<SCHEME, D, G>;
     if (configure_decode_t<SCHEME, D, G>() != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partial_kernel<SCHEME, D, G>, DECODE_THREADS,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partial_kernel<SCHEME, D, G>, C::THREADS,
                                                       C::smem_bytes(B)) != cudaSuccess)
         return 0;
     return n;
@@ -840,7 +865,7 @@ cudaError_t launch_decode_partial_t(const DecodeParams& p, cudaStream_t s) {
     using C = DecodeCfg<SCHEME, D, G>;
     cudaError_t e = configure_decode_t<SCHEME, D, G>();
     if (e != cudaSuccess) return e;
-    decode_partial_kernel<SCHEME, D, G><<<p.n_ctas, DECODE_THREADS, C::smem_bytes(p.B), s>>>(p);
+    decode_partial_kernel<SCHEME, D, G><<<p.n_ctas, C::THREADS, C::smem_bytes(p.B), s>>>(p);
     return cudaGetLastError();
 }
 

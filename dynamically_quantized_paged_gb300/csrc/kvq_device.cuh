@@ -84,6 +84,13 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
+// L2 policy for data several CTAs read (the query rows): normal eviction.
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 1-D bulk copy global -> shared through the TMA unit, completing on `bar`
 // (complete_tx).  dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -93,6 +100,20 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared (bypassing L1), with an L2
+// cache-policy hint; completion is tracked per warp-thread with commit /
+// wait groups (no spin loops).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
@@ -186,6 +207,29 @@ __device__ __forceinline__ void mfma_h2_1(uint32_t q2, uint32_t c2, float& acc) 
         "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
         : "+f"(acc)
         : "r"(q2), "r"(c2));
+}
+
+// 4-way byte dot products accumulated in int32 (dp4a).  Suffixes give the
+// signedness of (a, b): s = signed bytes, u = unsigned bytes.
+__device__ __forceinline__ int dp4a_ss(int a, int b, int c) {
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_su(int a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
 // Two int8 codes (bytes 2k, 2k+1 of w) -> fp16 pair holding 1152 + code,

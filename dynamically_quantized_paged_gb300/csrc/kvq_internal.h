@@ -16,9 +16,8 @@ constexpr unsigned ERR_TIMEOUT = 2u;
 // Tokens per pipeline stage ("unit").  Pages are a multiple of it, so a unit
 // never straddles two pages and split boundaries fall on unit boundaries.
 constexpr int UNIT = 16;
-// Decode CTA: one producer warp (bulk copies) + CONSUMER_WARPS compute warps.
-constexpr int CONSUMER_WARPS = 4;
-constexpr int DECODE_THREADS = 32 * (CONSUMER_WARPS + 1);
+// Decode CTA: DECODE_WARPS warps, each feeding and consuming its own ring.
+constexpr int DECODE_WARPS = 4;
 constexpr int MAX_SEQS = 4096;     // per decode call (the plan lives in shared memory)
 constexpr int MIN_SLICE_UNITS = 8; // smallest per-CTA share of the work, in units
 
