@@ -2,7 +2,7 @@
 
 A step is one pass of the whole hot path over one batch: quantize-append of
 the step's new tokens (kvq_append) and split-K fused-dequant decode attention
-with its merge (kvq_decode_partial + kvq_decode_merge), for every layer of the
+with its merge (kvq_decode_attn: one launch), for every layer of the
 workload.  Pages come from the library's host allocator (scattered ids).
 Inputs are resident in HBM when the timed region starts; L2 is flushed (a
 256 MB write) before every timed step, outside the timed events.
@@ -235,7 +235,7 @@ class Bench:
         st = kvq.last_device_error()
         if st != kvq.OK:
             raise RuntimeError(f"set-up failed: {kvq.status_string(st)}")
-        self.launches_per_step = 3 * w.layers
+        self.launches_per_step = 2 * w.layers  # quantize-append + fused decode per layer
 
     def _rows(self, layer, b, s0, s1):
         k, v = inp.kv_rows(self.w, layer, b, s0, s1)
@@ -254,10 +254,9 @@ class Bench:
             kvq.append(c, slots, k_new[layer], v_new[layer])
             if events is not None:
                 events[layer][0].record()
-            kvq.decode_partial(c, q[layer], bt, lens, out, self.ws)
+            kvq.decode_attn(c, q[layer], bt, lens, out, self.ws)  # one launch, splits merged in place
             if events is not None:
                 events[layer][1].record()
-            kvq.decode_merge(c, q[layer], bt, lens, out, self.ws)
 
     def run(self, steps: int, warmup: int, barrier):
         torch = self.torch
@@ -480,7 +479,7 @@ def main(argv=None):
             "decode_tokens_per_s": round(world * w.batch / (ms_per_step * 1e-3), 1),
             "append_tokens_per_s_step": round(world * nb["append_tokens"] / (ms_per_step * 1e-3), 1),
             "algorithmic_bytes_per_step": nb["step"],
-            "roofline": {"kernel": "decode_partial_kernel (split-K fused-dequant decode)",
+            "roofline": {"kernel": "decode_partial_kernel (split-K fused-dequant decode, merge fused)",
                          "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",

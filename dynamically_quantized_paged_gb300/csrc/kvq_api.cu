@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+#include <chrono>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -75,6 +77,21 @@ int gqa_ratio(const kvq_cache* c, int32_t Hq) {
     return (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
 }
 
+// Generation tag of a decode call: the fused merge counts arrivals per
+// segment in workspace words tagged with it, so the workspace needs no
+// zeroing.  Starts from a clock-derived value and never repeats within 2^32
+// calls of one process.
+uint32_t next_generation() {
+    static std::atomic<uint32_t> g{0};
+    static std::atomic<bool> seeded{false};
+    if (!seeded.exchange(true)) {
+        const uint32_t seed = (uint32_t)std::chrono::steady_clock::now().time_since_epoch().count();
+        g.store(seed | 1u);
+    }
+    uint32_t v = g.fetch_add(2);
+    return v ? v : g.fetch_add(2);
+}
+
 // The persistent decode grid: resident CTAs per SM (occupancy of this kernel
 // configuration at this batch size) times the SM count.
 int n_ctas_for(const kvq_cache* c, int G, int B) {
@@ -104,7 +121,7 @@ kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* 
     if (dev < 0) return KVQ_ERR_CUDA;
     const int n_ctas = n_ctas_for(cache, G, B);
     if (n_ctas <= 0) return KVQ_ERR_CUDA;
-    const size_t need = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, B);
+    const size_t need = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, B, cache->num_kv_heads);
     if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     unsigned* err = kvq::device_error_word();
     if (!err) return KVQ_ERR_CUDA;
@@ -123,6 +140,10 @@ kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* 
     p.n_ctas = n_ctas;
     p.q_scale = scale * 1.4426950408889634f;  // log2(e): the kernel works in base 2
     p.err = err;
+    p.fuse_merge = 0;
+    p.gen = next_generation();
+    p.seg_ctr = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) +
+                                                      kvq::decode_counter_offset(n_ctas, G, cache->head_dim, B));
     return KVQ_OK;
 }
 
@@ -248,7 +269,7 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_seqs,
     if (G == 0) return KVQ_ERR_UNSUPPORTED;
     const int n_ctas = n_ctas_for(cache, G, num_seqs);
     if (n_ctas <= 0) return KVQ_ERR_CUDA;
-    *bytes = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, num_seqs);
+    *bytes = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, num_seqs, cache->num_kv_heads);
     return KVQ_OK;
 }
 
@@ -290,8 +311,8 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const int32_t*
                                    max_pages_per_seq, softmax_scale, workspace, workspace_bytes, p, G);
     if (st != KVQ_OK || num_seqs == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    p.fuse_merge = 1;  // one launch: splits are merged by the CTA that finishes them last
     if (kvq::launch_decode_partial(p, G, s) != cudaSuccess) return KVQ_ERR_CUDA;
-    if (kvq::launch_decode_merge(p, G, s) != cudaSuccess) return KVQ_ERR_CUDA;
     return KVQ_OK;
 }
 

@@ -15,8 +15,10 @@
 // equal slices of S units; a CTA walks the segment pieces of its slice.  A
 // piece that is a whole segment yields the final output row directly; a
 // segment cut by slice boundaries leaves one partial (running max m, sum l,
-// unnormalized o) per CTA that touches it, at most two per CTA, and the merge
-// kernel combines them.  Slices are a function of logical positions only, so
+// unnormalized o) per CTA that touches it, at most two per CTA.  In the
+// one-launch form the CTA that delivers a segment's last partial (counted in
+// a generation-tagged workspace word) merges them; in the two-launch form the
+// merge kernel does.  Slices are a function of logical positions only, so
 // physical page placement cannot change the result.
 //
 // Inside a CTA (4 warps, no producer warp): every warp streams its own
@@ -276,6 +278,63 @@ __device__ __forceinline__ void warp_range(const Piece& pc, int warp, int& a, in
     if (a > b) a = b;
 }
 
+// Log-sum-exp merge of the split partials of segment (b, h), whose units
+// span [a, a + units) of the work line cut into slices of S units: over the
+// CTAs c_first..c_last that touched it (slot 2c, or 2c+1 when the segment is
+// not the first piece of CTA c's slice), an online merge
+//   M' = max(M, m_c), L' = L 2^(M - M') + l_c 2^(m_c - M'),
+//   O' = O 2^(M - M') + o_c 2^(m_c - M'),   out = O / L.
+// One warp per query head, four channels per lane, eight partials in flight.
+// Loads bypass L1: the partials may come from other CTAs of the same launch.
+template <int D, int G>
+__device__ __forceinline__ void merge_segment(const DecodeParams& p, int b, int h, int64_t a, int64_t units,
+                                              int64_t S, int tid, int nthreads) {
+    constexpr int UNROLL = 8;
+    const int64_t e = a + units;
+    const int64_t c_first = a / S, c_last = (e - 1) / S;
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
+    const int j0 = lane * 4;
+    for (int g = warp; g < G; g += nwarps) {
+        float M = -INFINITY, L = 0.0f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t c0 = c_first; c0 <= c_last; c0 += UNROLL) {
+            float mk[UNROLL], lk[UNROLL];
+            float4 ok[UNROLL];
+#pragma unroll
+            for (int k = 0; k < UNROLL; ++k) {
+                const int64_t c = c0 + k;
+                mk[k] = -INFINITY;
+                lk[k] = 0.0f;
+                ok[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c <= c_last) {
+                    const int64_t slot = (c == c_first && a != c * S) ? 2 * c + 1 : 2 * c;
+                    mk[k] = __ldcg(p.ws_m + slot * G + g);
+                    lk[k] = __ldcg(p.ws_l + slot * G + g);
+                    if (j0 < D) ok[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (slot * G + g) * D + j0));
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < UNROLL; ++k) {
+                if (mk[k] == -INFINITY) continue;  // a partial with no tokens
+                const float nm = fmaxf(M, mk[k]);
+                const float fa = (M == -INFINITY) ? 0.0f : fast_exp2(M - nm);
+                const float fb = fast_exp2(mk[k] - nm);
+                L = fmaf(L, fa, lk[k] * fb);
+                O.x = fmaf(O.x, fa, ok[k].x * fb);
+                O.y = fmaf(O.y, fa, ok[k].y * fb);
+                O.z = fmaf(O.z, fa, ok[k].z * fb);
+                O.w = fmaf(O.w, fa, ok[k].w * fb);
+                M = nm;
+            }
+        }
+        if (j0 < D) {
+            const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+            float* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G + g) * D + j0;
+            *reinterpret_cast<float4*>(out) = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+        }
+    }
+}
+
 template <int SCHEME, int D, int G>
 __global__ void __launch_bounds__(DecodeCfg<SCHEME, D, G>::THREADS, (DecodeCfg<SCHEME, D, G>::MIN_CTAS))
 decode_partial_kernel(const DecodeParams p) {
@@ -300,6 +359,14 @@ decode_partial_kernel(const DecodeParams p) {
     }
     const int Hkv = p.c.num_kv_heads;
     const int P = p.c.page_size;
+    if (p.fuse_merge) {  // empty sequences get zero rows (no CTA's slice touches them)
+        for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+            if (prefix[b + 1] != prefix[b]) continue;
+            float* row = p.out + (int64_t)b * p.Hq * D;
+            for (int i = threadIdx.x; i < p.Hq * D; i += blockDim.x) row[i] = 0.0f;
+        }
+    }
+    __shared__ int s_last;  // this CTA delivered the last partial of the current segment
     const uint64_t pol_kv = l2_evict_first_policy();  // pages are read once
     const uint64_t pol_q = l2_evict_normal_policy();  // query rows are shared by the CTA's warps
     uint8_t* ring = smem + C::OFF_STAGES + warp * STAGES_ * C::STAGE;
@@ -783,6 +850,33 @@ decode_partial_kernel(const DecodeParams p) {
                 }
             }
         }
+        if (p.fuse_merge && !pc.whole) {
+            // Count this CTA's arrival on the segment; the CTA that brings the
+            // last partial merges them all.  The counter's upper half holds the
+            // call's generation, so stale values from earlier calls read as 0.
+            __threadfence();
+            __syncthreads();
+            const int64_t units = prefix[pc.b + 1] - prefix[pc.b];
+            const int64_t a = (int64_t)Hkv * prefix[pc.b] + (int64_t)pc.h * units;
+            if (tid == 0) {
+                const unsigned long long n = (unsigned long long)((a + units - 1) / plan.S - a / plan.S + 1);
+                unsigned long long* ctr = p.seg_ctr + (int64_t)pc.b * Hkv + pc.h;
+                const unsigned long long tag = (unsigned long long)p.gen << 32;
+                unsigned long long old = atomicAdd(ctr, 0ull), want;
+                while (true) {  // lock-free: a failed swap means another CTA's succeeded
+                    want = ((old & 0xFFFFFFFF00000000ull) == tag) ? old + 1 : (tag | 1ull);
+                    const unsigned long long seen = atomicCAS(ctr, old, want);
+                    if (seen == old) break;
+                    old = seen;
+                }
+                s_last = ((want & 0xFFFFFFFFull) == n) ? 1 : 0;
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                merge_segment<D, G>(p, pc.b, pc.h, a, units, plan.S, tid, C::THREADS);
+            }
+        }
         __syncthreads();
     }
     cp_async_wait<0>();
@@ -801,33 +895,14 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
     const int64_t S = wsplan[1];
     const int32_t* prefix = reinterpret_cast<const int32_t*>(wsplan + 2);
     const int units = prefix[b + 1] - prefix[b];
-    float* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D;
     if (units == 0) {
+        float* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D;
         for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = 0.0f;
         return;
     }
     const int64_t a = (int64_t)p.c.num_kv_heads * prefix[b] + (int64_t)h * units;
-    const int64_t e = a + units;
-    const int64_t c_first = a / S, c_last = (e - 1) / S;
-    if (c_first == c_last) return;
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int g = idx / D;
-        const int jj = idx % D;
-        float M = -INFINITY;
-        for (int64_t c = c_first; c <= c_last; ++c) {
-            const int64_t slot = (c == c_first && a != c * S) ? 2 * c + 1 : 2 * c;
-            M = fmaxf(M, p.ws_m[slot * G + g]);
-        }
-        float L = 0.0f, O = 0.0f;
-        for (int64_t c = c_first; c <= c_last; ++c) {
-            const int64_t slot = (c == c_first && a != c * S) ? 2 * c + 1 : 2 * c;
-            const float mc = p.ws_m[slot * G + g];
-            const float f = (mc == -INFINITY) ? 0.0f : fast_exp2(mc - M);
-            L = fmaf(p.ws_l[slot * G + g], f, L);
-            O = fmaf(p.ws_o[(slot * G + g) * D + jj], f, O);
-        }
-        out[g * D + jj] = (L > 0.0f) ? O / L : 0.0f;
-    }
+    if (a / S == (a + units - 1) / S) return;  // finished inside one CTA's slice
+    merge_segment<D, G>(p, b, h, a, units, S, threadIdx.x, blockDim.x);
 }
 
 // Shared memory attribute per device, set once (host-only state).

@@ -59,15 +59,25 @@ struct DecodeParams {
     int n_ctas;
     float q_scale;  // softmax scale * log2(e), folded into q
     unsigned* err;
+    int fuse_merge;                     // 1: the last CTA of a split segment merges it in place
+    uint32_t gen;                       // call generation tagging the arrival counters
+    unsigned long long* seg_ctr;        // [B * Hkv] arrival counters: (gen << 32) | arrivals
 };
 
 // Workspace layout for n_ctas persistent CTAs (two partial slots each):
 // o [2 n_ctas][G][D], m [2 n_ctas][G], l [2 n_ctas][G] (fp32), then the
-// published plan: int64 U, int64 S, int32 prefix[B + 1].
-inline size_t decode_workspace_bytes(int n_ctas, int G, int D, int B) {
+// published plan: int64 U, int64 S, int32 prefix[B + 1], then (8-byte
+// aligned) one uint64 arrival counter per (sequence, KV head) segment.
+inline size_t decode_plan_offset(int n_ctas, int G, int D) {
     const size_t slots = 2 * (size_t)n_ctas;
-    return slots * G * D * sizeof(float) + 2 * slots * G * sizeof(float) + 16 +
-           ((size_t)B + 1) * sizeof(int32_t);
+    return slots * G * D * sizeof(float) + 2 * slots * G * sizeof(float);
+}
+inline size_t decode_counter_offset(int n_ctas, int G, int D, int B) {
+    const size_t end_plan = decode_plan_offset(n_ctas, G, D) + 16 + ((size_t)B + 1) * sizeof(int32_t);
+    return (end_plan + 7) / 8 * 8;
+}
+inline size_t decode_workspace_bytes(int n_ctas, int G, int D, int B, int Hkv) {
+    return decode_counter_offset(n_ctas, G, D, B) + (size_t)B * Hkv * sizeof(unsigned long long);
 }
 
 cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaStream_t s);

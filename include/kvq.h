@@ -157,17 +157,21 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_seqs,
  * Query head g reads KV head g / (num_q_heads / num_kv_heads); the ratio must
  * be 1, 2, 4 or 8.  num_seqs <= 4096.  The work is split over a persistent
  * grid along logical token positions only, so the output does not depend on
- * which physical pages hold the tokens.  Two launches: kvq_decode_partial then
- * kvq_decode_merge. */
+ * which physical pages hold the tokens.  One launch: a (sequence, KV head)
+ * whose tokens are split across CTAs is merged by the CTA that delivers its
+ * last partial (arrivals are counted in workspace words tagged with a per-call
+ * generation, so the workspace needs no zeroing).  kvq_decode_partial followed
+ * by kvq_decode_merge is the equivalent two-launch form and gives bitwise the
+ * same output. */
 kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const int32_t* block_table,
                            const int32_t* seq_lens, float* out, int32_t num_seqs,
                            int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
                            void* workspace, size_t workspace_bytes, kvq_stream_t stream);
 
-/* The first of kvq_decode_attn's two launches: every (sequence, KV head)
- * whose tokens one CTA covers entirely gets its final output row; the rest
- * leave split partials (max, sum, unnormalized output) in the workspace.
- * Same arguments and rules as kvq_decode_attn. */
+/* The first launch of the two-launch form of kvq_decode_attn: every
+ * (sequence, KV head) whose tokens one CTA covers entirely gets its final
+ * output row; the rest leave split partials (max, sum, unnormalized output)
+ * in the workspace.  Same arguments and rules as kvq_decode_attn. */
 kvq_status kvq_decode_partial(const kvq_cache* cache, const void* q, const int32_t* block_table,
                               const int32_t* seq_lens, float* out, int32_t num_seqs,
                               int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,

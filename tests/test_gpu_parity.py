@@ -100,6 +100,22 @@ def test_page_permutation_is_bitwise_invariant():
     assert np.array_equal(a.decode(), b.decode())
 
 
+def test_workspace_garbage_is_harmless():
+    """The workspace needs no initialization: arbitrary bytes in it (stale
+    arrival counters included) must not change the result."""
+    w = small("int8", 32, 8, 128, 16)
+    lens = np.array([9000, 40, 2000, 0, 777], np.int32)
+    case = Case(w, lens)
+    ref = case.oracle_decode()
+    for fill in (0x00, 0xFF, 0xA5):
+        out = torch.full((len(lens), 32, 128), float("nan"), dtype=torch.float32, device=DEV)
+        ws = kvq.alloc_workspace(case.g, len(lens), 32, case.bt.shape[1], device=DEV)
+        ws.fill_(fill)
+        kvq.decode_attn(case.g, dev_bits(case.q), dev(case.bt), dev(lens), out, ws)
+        assert kvq.last_device_error() == kvq.OK
+        assert_attn_close(out.cpu().numpy().astype(np.float64), ref, f"fill {fill:#x}")
+
+
 def test_two_launch_form_matches_one_call():
     w = small("int4", 32, 4, 128, 32)
     case = Case(w, np.array([5000, 70, 2300], np.int32), oracle_seqs=[])
