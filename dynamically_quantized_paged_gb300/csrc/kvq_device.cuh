@@ -1,6 +1,6 @@
 // kvq_device.cuh -- device-side building blocks shared by the kernels:
-// error flags, mbarrier / 1-D bulk-copy (TMA) wrappers with bounded waits,
-// and exact code -> float conversions.
+// error flags, 16-byte cp.async copies with L2 policies, exact code -> float
+// conversions, mixed-precision and dp4a dot-product steps.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -13,68 +13,12 @@
 
 namespace kvq {
 
-// A wait on an mbarrier gives up after this many nanoseconds.  A copy of a
-// few KB completes in microseconds; two seconds means the copy will not come.
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
-
 __device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
     if (err) atomicOr(err, bit);
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_timer_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-                 : "memory");
-}
-
-// Makes initialized mbarriers visible to the async (bulk-copy) proxy.
-__device__ __forceinline__ void fence_barrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
-                     smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Waits for the phase with the given parity to complete.  Returns false if
-// it did not within WAIT_LIMIT_NS; the caller then records ERR_TIMEOUT and
-// stops waiting from then on (it never blocks without a limit).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
-    }
 }
 
 // L2 policy for data read exactly once (the KV pages): evict first.
@@ -91,17 +35,6 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
     return pol;
 }
 
-// 1-D bulk copy global -> shared through the TMA unit, completing on `bar`
-// (complete_tx).  dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
 // 16-byte asynchronous copy global -> shared (bypassing L1), with an L2
 // cache-policy hint; completion is tracked per warp-thread with commit /
 // wait groups (no spin loops).
@@ -114,10 +47,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -150,40 +79,6 @@ __device__ __forceinline__ void e4m3x4_to_float(uint32_t w, float f[4]) {
     f[1] = a.y;
     f[2] = b.x;
     f[3] = b.y;
-}
-
-// Eight 4-bit codes (one word; byte j holds channels 2j (low nibble) and
-// 2j+1) -> eight floats 0..15, exactly, by the same mantissa-placement trick.
-__device__ __forceinline__ void u4x8_to_float(uint32_t w, float f[8]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        f[i] = __uint_as_float(((w >> (4 * i)) & 0xFu) | 0x4B000000u) - 8388608.0f;
-    }
-}
-
-// ---- packed fp32 pairs (sm_100+ .f32x2 arithmetic) ------------------------
-__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
 }
 
 // Two mixed-precision FMAs: acc0 += lo(q2) * lo(c2), acc1 += hi(q2) * hi(c2),
@@ -232,25 +127,11 @@ __device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
-// Two int8 codes (bytes 2k, 2k+1 of w) -> fp16 pair holding 1152 + code,
-// exactly: flip the sign bit (code + 128) and place the byte in the low
-// mantissa byte of 1024 (fp16 exponent 10, spacing 1).
-__device__ __forceinline__ uint32_t s8x2_to_h2_biased(uint32_t flipped, int k) {
-    return __byte_perm(flipped, 0x64646464u, k == 0 ? 0x4140 : 0x4342);
-}
-constexpr float S8_H2_BIAS = 1152.0f;
-
 // Two E4M3 codes (low 16 bits) -> exact fp16 pair.
 __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t w16) {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w16 & 0xFFFFu), __NV_E4M3);
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
-
-// Nibbles s and s+4 of an 8-code word -> fp16 pair holding 1024 + code.
-__device__ __forceinline__ uint32_t u4pair_to_h2_biased(uint32_t w, int s) {
-    return ((w >> (4 * s)) & 0x000F000Fu) | 0x64006400u;
-}
-constexpr float U4_H2_BIAS = 1024.0f;
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);
