@@ -26,16 +26,22 @@
 // stages with 16-byte cp.async gathers (all 32 lanes issue; page ids come from
 // the block table in 32-entry register batches, the next batch prefetched),
 // keeping STAGES-1 units in flight, and consumes them:
-//  * scores: each lane holds 16 channels of the G query rows as fp16 and
-//    turns 16 codes into fp16 with byte permutes (INT8, INT4: exact integer
-//    plus a constant bias removed once per score) or the E4M3 converter;
-//    mixed-precision FMAs (fp16 x fp16 -> fp32) form partial dots, a
-//    transpose-reduction across the lanes sharing a token leaves one score
-//    per lane, and the per-token scale is applied once;
+//  * scores: each lane holds 16 (or 8) channels of the G query rows.  For
+//    INT8 and INT4 the query is held as 16-bit fixed point per head (a signed
+//    high byte and an unsigned low byte) and the partial dots are exact int32
+//    dp4a sums against the codes; for FP8 the query is fp16 and the codes are
+//    converted to fp16 for mixed-precision FMAs.  A transpose-reduction
+//    across the lanes sharing a token leaves one score per lane, and the
+//    per-token (and per-head) scales are applied once;
 //  * online softmax in base 2 directly on those lanes (max over the unit by
-//    two shuffles), weights p*scale to shared memory;
-//  * values: each lane owns 8 (or 4) channels x G heads of fp32 accumulators,
-//    updated with packed fp32x2 FMAs on exactly converted codes.
+//    two shuffles); the weights p * value scale go to shared memory;
+//  * values: each lane owns 4 (or 8) channels x G heads of fp32 accumulators.
+//    INT8: the unit's weights of each head become 16-bit fixed point
+//    relative to their maximum, the lane transposes the codes of 4
+//    consecutive tokens into one word per channel, dp4a accumulates the
+//    unit in int32 (high byte, times 256, then low byte), and one FMA per
+//    accumulator adds the unit.  FP8, INT4: scalar FMAs on exactly
+//    converted codes (INT4 adds the zero-points once per token).
 // The query rows of a piece travel in the stage of the warp's first unit of
 // that piece.  At the end of a piece the four warps' states are combined in
 // shared memory.  One 1-D bulk copy per issuing thread completes only every
@@ -78,19 +84,25 @@ struct DecodeCfg {
     static constexpr int DUP = KL / G;  // lanes that end holding the same (token, head) score
     static constexpr int QW = CPL / 2;  // fp16 pairs of query per head per lane
     static constexpr bool TWO_ACC = G <= 2;  // a second accumulator set for more ILP when registers allow
-    // values: VCH channels per lane, VL lanes per token, VT token groups
-    static constexpr int VCH = (G >= 8 && D == 128) ? 4 : 8;
+    // values: VCH channels per lane, VL lanes per token, VT token groups.
+    // INT8 values go through dp4a: weights as 16-bit fixed point (hi and lo
+    // bytes) against the codes of 4 consecutive tokens of one channel.
+    static constexpr bool VDP = INT8;
+    static constexpr int VCH = (VDP || (G >= 8 && D == 128)) ? 4 : 8;
     static constexpr int VL = D / VCH;
     static constexpr int VT = 32 / VL;
     static constexpr int V_UNROLL = (G >= 8) ? 4 : UNIT / VT;  // token loop unrolling (register pressure)
+    static constexpr int NBLK = UNIT / 4 / VT;                 // dp4a path: 4-token blocks per lane
     // shared memory layout (bytes)
     static constexpr int OFF_STAGES = 0;
     static constexpr int OFF_CO = OFF_STAGES + WARPS * STAGES * STAGE;
     static constexpr int OFF_CM = OFF_CO + WARPS * G * D * 4;
     static constexpr int OFF_CL = OFF_CM + WARPS * G * 4;
     static constexpr int OFF_W = (OFF_CL + WARPS * G * 4 + 15) / 16 * 16;
-    // per warp: weights Wt[UNIT][G] (fp32), then alpha[G]
-    static constexpr int W_BYTES = (UNIT * G * 4 + G * 4 + 15) / 16 * 16;
+    // per warp: weights (fp32 Wt[UNIT][G], or on the dp4a path the bytes
+    // WB[UNIT/4][hi, lo][G][4 tokens]), then the weights' fixed-point step
+    // WQ[G] (dp4a path), then alpha[G]
+    static constexpr int W_BYTES = (UNIT * G * 4 + 2 * G * 4 + 15) / 16 * 16;
     static constexpr int OFF_MISC = OFF_W + WARPS * W_BYTES;
     static constexpr int OFF_PLAN = OFF_MISC + 16;
     static size_t smem_bytes(int B) { return OFF_PLAN + (size_t)(B + 1) * 4; }
@@ -474,7 +486,9 @@ decode_partial_kernel(const DecodeParams p) {
     const int tid = threadIdx.x;
     uint8_t* wbase = smem + C::OFF_W + warp * C::W_BYTES;
     float* Wt = reinterpret_cast<float*>(wbase);                   // [UNIT][G]
-    float* AL = reinterpret_cast<float*>(wbase + UNIT * G * 4);    // [G]
+    uint8_t* WB = wbase;                                           // dp4a path: weight bytes
+    float* WQ = reinterpret_cast<float*>(wbase + UNIT * G * 4);    // [G]
+    float* AL = WQ + G;                                            // [G]
     float* CO = reinterpret_cast<float*>(smem + C::OFF_CO);
     float* CM = reinterpret_cast<float*>(smem + C::OFF_CM);
     float* CL = reinterpret_cast<float*>(smem + C::OFF_CL);
@@ -703,15 +717,50 @@ decode_partial_kernel(const DecodeParams p) {
                 const float m_new = fmaxf(m_run, mx);
                 const float alpha = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - m_new);
                 float psum = 0.0f;
+                if constexpr (C::VDP) {
+                    // weights W = p * value scale, then 16-bit fixed point per
+                    // (unit, head): W ~ wq * (256 hi + lo), wq = max W / 65535
+                    float wv[C::PASSES];
+                    float wmax = 0.0f;
 #pragma unroll
-                for (int pass = 0; pass < C::PASSES; ++pass) {
-                    const int t = pass * C::TPP + k_tok;
-                    const float pr = (sc[pass] == -INFINITY) ? 0.0f : fast_exp2(sc[pass] - m_new);
-                    psum += pr;
+                    for (int pass = 0; pass < C::PASSES; ++pass) {
+                        const int t = pass * C::TPP + k_tok;
+                        const float pr = (sc[pass] == -INFINITY) ? 0.0f : fast_exp2(sc[pass] - m_new);
+                        psum += pr;
+                        wv[pass] = (t < n_valid) ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
+                        wmax = fmaxf(wmax, wv[pass]);
+                    }
+#pragma unroll
+                    for (int off = C::KL; off < 32; off <<= 1)
+                        wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
+                    // Below 1e-30 the unit's weights are negligible next to the
+                    // running sum (>= 1 after the first token) and are dropped.
+                    const bool live = wmax > 1e-30f;
+                    const float inv = live ? __fdividef(65535.0f, wmax) : 0.0f;
                     if (k_writer) {
-                        float wv = pr;
-                        if constexpr (!C::INT4) wv = (t < n_valid) ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
-                        Wt[t * G + k_head] = wv;
+#pragma unroll
+                        for (int pass = 0; pass < C::PASSES; ++pass) {
+                            const int t = pass * C::TPP + k_tok;
+                            // round to nearest in the low mantissa bits of 2^23 + W * inv;
+                            // W * inv <= 65535 (1 + 2^-22) never rounds up to 65536
+                            const uint32_t bits = __float_as_uint(fmaf(wv[pass], inv, 8388608.0f));
+                            uint8_t* dst = WB + (((t >> 2) * 2) * G + k_head) * 4 + (t & 3);
+                            dst[0] = (uint8_t)(bits >> 8);  // hi byte
+                            dst[G * 4] = (uint8_t)bits;     // lo byte
+                        }
+                        if (k_tok == 0) WQ[k_head] = live ? wmax * (1.0f / 65535.0f) : 0.0f;
+                    }
+                } else {
+#pragma unroll
+                    for (int pass = 0; pass < C::PASSES; ++pass) {
+                        const int t = pass * C::TPP + k_tok;
+                        const float pr = (sc[pass] == -INFINITY) ? 0.0f : fast_exp2(sc[pass] - m_new);
+                        psum += pr;
+                        if (k_writer) {
+                            float wv = pr;
+                            if constexpr (!C::INT4) wv = (t < n_valid) ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
+                            Wt[t * G + k_head] = wv;
+                        }
                     }
                 }
                 l_run = l_run * alpha + psum;
@@ -729,6 +778,70 @@ decode_partial_kernel(const DecodeParams p) {
                         for (int jj = 0; jj < C::VCH; ++jj) o[g][jj] *= a;
                     }
                 }
+                if constexpr (C::VDP) {
+                    // codes of 4 consecutive tokens x this lane's 4 channels,
+                    // transposed to one word per channel (token bytes in order)
+                    uint32_t x[C::NBLK][4];
+#pragma unroll
+                    for (int k = 0; k < C::NBLK; ++k) {
+                        const uint8_t* src = stg + C::VC + (4 * (v_tok + k * C::VT)) * D + v_c0;
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(src);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(src + D);
+                        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(src + 2 * D);
+                        const uint32_t w3 = *reinterpret_cast<const uint32_t*>(src + 3 * D);
+                        const uint32_t a01 = __byte_perm(w0, w1, 0x5140), b01 = __byte_perm(w0, w1, 0x7362);
+                        const uint32_t a23 = __byte_perm(w2, w3, 0x5140), b23 = __byte_perm(w2, w3, 0x7362);
+                        x[k][0] = __byte_perm(a01, a23, 0x5410);
+                        x[k][1] = __byte_perm(a01, a23, 0x7632);
+                        x[k][2] = __byte_perm(b01, b23, 0x5410);
+                        x[k][3] = __byte_perm(b01, b23, 0x7632);
+                    }
+                    // sum over the unit of (256 hi + lo) * code in int32 (|sum| < 2^28),
+                    // then one FMA per accumulator with the step wq
+                    constexpr int GC = G < 4 ? G : 4;
+#pragma unroll
+                    for (int g0 = 0; g0 < G; g0 += GC) {
+                        int acc[GC][4];
+#pragma unroll
+                        for (int gg = 0; gg < GC; ++gg)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) acc[gg][j] = 0;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            if (half == 1) {
+#pragma unroll
+                                for (int gg = 0; gg < GC; ++gg)
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) acc[gg][j] *= 256;
+                            }
+#pragma unroll
+                            for (int k = 0; k < C::NBLK; ++k) {
+                                const int blk = v_tok + k * C::VT;
+                                const uint8_t* wsrc = WB + ((blk * 2 + half) * G + g0) * 4;
+                                uint32_t wq4[GC];
+                                if constexpr (GC == 4) {
+                                    const uint4 r = *reinterpret_cast<const uint4*>(wsrc);
+                                    wq4[0] = r.x; wq4[1] = r.y; wq4[2] = r.z; wq4[3] = r.w;
+                                } else if constexpr (GC == 2) {
+                                    const uint2 r = *reinterpret_cast<const uint2*>(wsrc);
+                                    wq4[0] = r.x; wq4[1] = r.y;
+                                } else {
+                                    wq4[0] = *reinterpret_cast<const uint32_t*>(wsrc);
+                                }
+#pragma unroll
+                                for (int gg = 0; gg < GC; ++gg)
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) acc[gg][j] = dp4a_us(wq4[gg], (int)x[k][j], acc[gg][j]);
+                            }
+                        }
+#pragma unroll
+                        for (int gg = 0; gg < GC; ++gg) {
+                            const float step = WQ[g0 + gg];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) o[g0 + gg][j] = fmaf((float)acc[gg][j], step, o[g0 + gg][j]);
+                        }
+                    }
+                } else {
 #pragma unroll(C::V_UNROLL)
                 for (int k = 0; k < UNIT / C::VT; ++k) {
                     const int t = v_tok + k * C::VT;
@@ -793,6 +906,7 @@ decode_partial_kernel(const DecodeParams p) {
                             }
                         }
                     }
+                }
                 }
             }
             __syncwarp();
