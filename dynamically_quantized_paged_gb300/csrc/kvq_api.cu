@@ -79,8 +79,8 @@ int gqa_ratio(const kvq_cache* c, int32_t Hq) {
 
 // Generation tag of a decode call: the fused merge counts arrivals per
 // segment in workspace words tagged with it, so the workspace needs no
-// zeroing.  Starts from a clock-derived value and never repeats within 2^32
-// calls of one process.
+// zeroing.  Starts from a clock-derived odd value and never repeats
+// within 2^31 calls of one process.
 uint32_t next_generation() {
     static std::atomic<uint32_t> g{0};
     static std::atomic<bool> seeded{false};

@@ -291,59 +291,146 @@ __device__ __forceinline__ void warp_range(const Piece& pc, int warp, int& a, in
 }
 
 // Log-sum-exp merge of the split partials of segment (b, h), whose units
-// span [a, a + units) of the work line cut into slices of S units: over the
-// CTAs c_first..c_last that touched it (slot 2c, or 2c+1 when the segment is
-// not the first piece of CTA c's slice), an online merge
+// span [a, a + units) of the work line cut into slices of S units.  The n
+// CTAs c_first..c_last touched it; CTA c left its partial in slot 2c, or in
+// 2c+1 when the segment is not the first piece of its slice.  Every thread
+// owns float4 elements of the G x D output rows and merges the partials of
+// its head online,
 //   M' = max(M, m_c), L' = L 2^(M - M') + l_c 2^(m_c - M'),
-//   O' = O 2^(M - M') + o_c 2^(m_c - M'),   out = O / L.
-// One warp per query head, four channels per lane, eight partials in flight.
-// Loads bypass L1: the partials may come from other CTAs of the same launch.
+//   O' = O 2^(M - M') + o_c 2^(m_c - M'),   out = O / L,
+// eight partials at a time: each element's o loads are all in flight
+// together, and (m_c, l_c) are loaded once per head by one lane each and
+// shuffled to the lanes of that head.  Loads bypass L1: the partials come
+// from other CTAs of the same launch.  Every thread of the CTA calls this.
 template <int D, int G>
 __device__ __forceinline__ void merge_segment(const DecodeParams& p, int b, int h, int64_t a, int64_t units,
-                                              int64_t S, int tid, int nthreads) {
-    constexpr int UNROLL = 8;
-    const int64_t e = a + units;
-    const int64_t c_first = a / S, c_last = (e - 1) / S;
-    const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
-    const int j0 = lane * 4;
-    for (int g = warp; g < G; g += nwarps) {
-        float M = -INFINITY, L = 0.0f;
-        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int64_t c0 = c_first; c0 <= c_last; c0 += UNROLL) {
-            float mk[UNROLL], lk[UNROLL];
-            float4 ok[UNROLL];
+                                              int64_t S, int tid) {
+    constexpr int NT = 32 * DECODE_WARPS;            // threads of the CTA
+    constexpr int NE = G * D / 4;                    // float4 elements of the output rows
+    constexpr int EPT = (NE + NT - 1) / NT;          // per thread
+    constexpr int LPH = D / 4 < 32 ? D / 4 : 32;     // lanes of a warp that share a head
+    constexpr int UNR = 8;                           // partials per round
+    static_assert(UNR <= LPH, "one lane per partial of a round");
+    const int64_t c_first = a / S, c_last = (a + units - 1) / S;
+    const int n = (int)(c_last - c_first + 1);
+    const bool first_odd = a != c_first * S;
+    const int lane = tid & 31, base = lane / LPH * LPH, sub = lane % LPH;
+    auto slot_of = [&](int i) -> int64_t {
+        const int64_t c = c_first + i;
+        return (i == 0 && first_odd) ? 2 * c + 1 : 2 * c;
+    };
+    int eg[EPT], ej[EPT];
+    float M[EPT], L[EPT];
+    float4 O[EPT];
 #pragma unroll
-            for (int k = 0; k < UNROLL; ++k) {
-                const int64_t c = c0 + k;
-                mk[k] = -INFINITY;
-                lk[k] = 0.0f;
-                ok[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (c <= c_last) {
-                    const int64_t slot = (c == c_first && a != c * S) ? 2 * c + 1 : 2 * c;
-                    mk[k] = __ldcg(p.ws_m + slot * G + g);
-                    lk[k] = __ldcg(p.ws_l + slot * G + g);
-                    if (j0 < D) ok[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (slot * G + g) * D + j0));
+    for (int k = 0; k < EPT; ++k) {
+        const int e = tid + k * NT;
+        eg[k] = e < NE ? e / (D / 4) : -1;
+        ej[k] = (e % (D / 4)) * 4;
+        M[k] = -INFINITY;
+        L[k] = 0.0f;
+        O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int i0 = 0; i0 < n; i0 += UNR) {
+        float my_m[EPT], my_l[EPT];
+        float4 ov[UNR][EPT];
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            my_m[k] = -INFINITY;
+            my_l[k] = 0.0f;
+            if (sub < UNR && i0 + sub < n && eg[k] >= 0) {
+                const int64_t s = slot_of(i0 + sub);
+                my_m[k] = __ldcg(p.ws_m + s * G + eg[k]);
+                my_l[k] = __ldcg(p.ws_l + s * G + eg[k]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const int64_t s = slot_of(i0 + u);
+#pragma unroll
+            for (int k = 0; k < EPT; ++k)
+                if (i0 + u < n && eg[k] >= 0)
+                    ov[u][k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (s * G + eg[k]) * D + ej[k]));
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+#pragma unroll
+            for (int k = 0; k < EPT; ++k) {
+                const float mc = __shfl_sync(0xffffffffu, my_m[k], base + u);
+                const float lc = __shfl_sync(0xffffffffu, my_l[k], base + u);
+                if (mc == -INFINITY) continue;  // no partial, or one with no tokens
+                const float nm = fmaxf(M[k], mc);
+                const float fa = (M[k] == -INFINITY) ? 0.0f : fast_exp2(M[k] - nm);
+                const float fb = fast_exp2(mc - nm);
+                L[k] = fmaf(L[k], fa, lc * fb);
+                O[k].x = fmaf(O[k].x, fa, ov[u][k].x * fb);
+                O[k].y = fmaf(O[k].y, fa, ov[u][k].y * fb);
+                O[k].z = fmaf(O[k].z, fa, ov[u][k].z * fb);
+                O[k].w = fmaf(O[k].w, fa, ov[u][k].w * fb);
+                M[k] = nm;
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+        if (eg[k] < 0) continue;
+        const float inv = (L[k] > 0.0f) ? 1.0f / L[k] : 0.0f;
+        float* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G + eg[k]) * D + ej[k];
+        *reinterpret_cast<float4*>(out) = make_float4(O[k].x * inv, O[k].y * inv, O[k].z * inv, O[k].w * inv);
+    }
+}
+
+// One-launch form, at the end of a piece that is not a whole segment: count
+// this CTA's arrival on the segment; the CTA that brings the last of its n
+// partials merges them.  The counter holds (generation << 32) | arrivals.
+// An arrival adds 1 and reads the old value back in the same atomic; if
+// the old value carries this call's generation, the arrival is counted.
+// Otherwise the word is left over from an earlier call (or is garbage), and
+// the CTA installs (generation << 32) | 1 with a compare-and-swap, or finds
+// that another CTA did and adds again.  Every CTA is counted exactly once.
+// Only the first arrivals of a call can meet a stale word, so the rest take
+// a single atomic and contention stays low even when dozens of CTAs arrive
+// together.  No CTA waits on another.  Kept out of line so that the rarely
+// run merge does not shape the code of the main loop.  Called by every
+// thread of the CTA; `flag` is a shared int.
+template <int D, int G>
+__device__ __noinline__ void arrive_and_merge(const DecodeParams& p, int b, int h, const int32_t* prefix, int64_t S,
+                                              int tid, int* flag) {
+    const int Hkv = p.c.num_kv_heads;
+    __threadfence();
+    __syncthreads();
+    const int64_t units = prefix[b + 1] - prefix[b];
+    const int64_t a = (int64_t)Hkv * prefix[b] + (int64_t)h * units;
+    if (tid == 0) {
+        const unsigned long long n = (unsigned long long)((a + units - 1) / S - a / S + 1);
+        unsigned long long* ctr = p.seg_ctr + (int64_t)b * Hkv + h;
+        const unsigned long long tag = (unsigned long long)p.gen << 32;
+        constexpr unsigned long long HI = 0xFFFFFFFF00000000ull, LO = 0xFFFFFFFFull;
+        const unsigned long long old = atomicAdd(ctr, 1ull);  // the value before this add
+        unsigned long long count;
+        if ((old & HI) == tag) {
+            count = (old & LO) + 1;
+        } else {
+            unsigned long long expect = old + 1;  // the word just after this add, if untouched
+            while (true) {
+                const unsigned long long seen = atomicCAS(ctr, expect, tag | 1ull);
+                if (seen == expect) {  // installed this call's generation, counted as the first
+                    count = 1;
+                    break;
                 }
-            }
-#pragma unroll
-            for (int k = 0; k < UNROLL; ++k) {
-                if (mk[k] == -INFINITY) continue;  // a partial with no tokens
-                const float nm = fmaxf(M, mk[k]);
-                const float fa = (M == -INFINITY) ? 0.0f : fast_exp2(M - nm);
-                const float fb = fast_exp2(mk[k] - nm);
-                L = fmaf(L, fa, lk[k] * fb);
-                O.x = fmaf(O.x, fa, ok[k].x * fb);
-                O.y = fmaf(O.y, fa, ok[k].y * fb);
-                O.z = fmaf(O.z, fa, ok[k].z * fb);
-                O.w = fmaf(O.w, fa, ok[k].w * fb);
-                M = nm;
+                if ((seen & HI) == tag) {  // another arrival installed it: count by adding
+                    count = (atomicAdd(ctr, 1ull) & LO) + 1;
+                    break;
+                }
+                expect = seen;  // other stale adds moved the word: install over it
             }
         }
-        if (j0 < D) {
-            const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
-            float* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G + g) * D + j0;
-            *reinterpret_cast<float4*>(out) = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
-        }
+        *flag = (count == n) ? 1 : 0;
+    }
+    __syncthreads();
+    if (*flag) {
+        __threadfence();
+        merge_segment<D, G>(p, b, h, a, units, S, tid);
     }
 }
 
@@ -964,33 +1051,7 @@ decode_partial_kernel(const DecodeParams p) {
                 }
             }
         }
-        if (p.fuse_merge && !pc.whole) {
-            // Count this CTA's arrival on the segment; the CTA that brings the
-            // last partial merges them all.  The counter's upper half holds the
-            // call's generation, so stale values from earlier calls read as 0.
-            __threadfence();
-            __syncthreads();
-            const int64_t units = prefix[pc.b + 1] - prefix[pc.b];
-            const int64_t a = (int64_t)Hkv * prefix[pc.b] + (int64_t)pc.h * units;
-            if (tid == 0) {
-                const unsigned long long n = (unsigned long long)((a + units - 1) / plan.S - a / plan.S + 1);
-                unsigned long long* ctr = p.seg_ctr + (int64_t)pc.b * Hkv + pc.h;
-                const unsigned long long tag = (unsigned long long)p.gen << 32;
-                unsigned long long old = atomicAdd(ctr, 0ull), want;
-                while (true) {  // lock-free: a failed swap means another CTA's succeeded
-                    want = ((old & 0xFFFFFFFF00000000ull) == tag) ? old + 1 : (tag | 1ull);
-                    const unsigned long long seen = atomicCAS(ctr, old, want);
-                    if (seen == old) break;
-                    old = seen;
-                }
-                s_last = ((want & 0xFFFFFFFFull) == n) ? 1 : 0;
-            }
-            __syncthreads();
-            if (s_last) {
-                __threadfence();
-                merge_segment<D, G>(p, pc.b, pc.h, a, units, plan.S, tid, C::THREADS);
-            }
-        }
+        if (p.fuse_merge && !pc.whole) arrive_and_merge<D, G>(p, pc.b, pc.h, prefix, plan.S, tid, &s_last);
         __syncthreads();
     }
     cp_async_wait<0>();
@@ -1002,7 +1063,7 @@ decode_partial_kernel(const DecodeParams p) {
 // partials of CTAs c_first..c_last:  M = max m_c, L = sum l_c 2^(m_c - M),
 // out = sum o_c 2^(m_c - M) / L.
 template <int D, int G>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(32 * DECODE_WARPS) decode_merge_kernel(const DecodeParams p) {
     const int b = blockIdx.x / p.c.num_kv_heads;
     const int h = blockIdx.x % p.c.num_kv_heads;
     const int64_t* wsplan = reinterpret_cast<const int64_t*>(p.ws_l + 2 * (size_t)p.n_ctas * G);
@@ -1016,7 +1077,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
     }
     const int64_t a = (int64_t)p.c.num_kv_heads * prefix[b] + (int64_t)h * units;
     if (a / S == (a + units - 1) / S) return;  // finished inside one CTA's slice
-    merge_segment<D, G>(p, b, h, a, units, S, threadIdx.x, blockDim.x);
+    merge_segment<D, G>(p, b, h, a, units, S, threadIdx.x);
 }
 
 // Shared memory attribute per device, set once (host-only state).
@@ -1061,7 +1122,7 @@ cudaError_t launch_decode_partial_t(const DecodeParams& p, cudaStream_t s) {
 template <int D, int G>
 cudaError_t launch_decode_merge_t(const DecodeParams& p, cudaStream_t s) {
     const int64_t n = (int64_t)p.B * p.c.num_kv_heads;
-    decode_merge_kernel<D, G><<<(unsigned)n, 128, 0, s>>>(p);
+    decode_merge_kernel<D, G><<<(unsigned)n, 32 * DECODE_WARPS, 0, s>>>(p);
     return cudaGetLastError();
 }
 
