@@ -58,7 +58,9 @@ template <int SCHEME, int D, int G>
 struct DecodeCfg {
     static constexpr bool INT4 = SCHEME == KVQ_INT4_ASYM_G32;
     static constexpr bool INT8 = SCHEME == KVQ_INT8_SYM_TOKEN;
-    static constexpr int WARPS = DECODE_WARPS;
+    // One CTA per SM: with several co-resident CTAs the older CTA's warps win
+    // the issue slots and finish first, leaving the SM under-occupied.
+    static constexpr int WARPS = decode_warps(G);
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int CB = INT4 ? D / 2 : D;        // code bytes per token row
     static constexpr int NGR = D / 32;                 // INT4 groups per row
@@ -74,8 +76,6 @@ struct DecodeCfg {
     static constexpr int QO = VZ + (INT4 ? UNIT * MB : 0);
     static constexpr int STAGE = QO + Q_BYTES;
     static constexpr int STAGES = (STAGE >= 4096) ? 3 : 4;  // ring depth per warp: STAGES-1 units in flight
-    // occupancy the register budget is compiled for (CTAs per SM)
-    static constexpr int MIN_CTAS = (G >= 8) ? 2 : 3;
     // scores: KL lanes per token, CPL channels per lane, TPP tokens per pass
     static constexpr int CPL = (D == 64 && G == 8) ? 8 : 16;
     static constexpr int KL = D / CPL;
@@ -95,10 +95,7 @@ struct DecodeCfg {
     static constexpr int NBLK = UNIT / 4 / VT;                 // dp4a path: 4-token blocks per lane
     // shared memory layout (bytes)
     static constexpr int OFF_STAGES = 0;
-    static constexpr int OFF_CO = OFF_STAGES + WARPS * STAGES * STAGE;
-    static constexpr int OFF_CM = OFF_CO + WARPS * G * D * 4;
-    static constexpr int OFF_CL = OFF_CM + WARPS * G * 4;
-    static constexpr int OFF_W = (OFF_CL + WARPS * G * 4 + 15) / 16 * 16;
+    static constexpr int OFF_W = OFF_STAGES + WARPS * STAGES * STAGE;
     // per warp: weights (fp32 Wt[UNIT][G], or on the dp4a path the bytes
     // WB[UNIT/4][hi, lo][G][4 tokens]), then the weights' fixed-point step
     // WQ[G] (dp4a path), then alpha[G]
@@ -108,7 +105,7 @@ struct DecodeCfg {
     static size_t smem_bytes(int B) { return OFF_PLAN + (size_t)(B + 1) * 4; }
     static_assert(G <= KL, "each lane must end the reduction holding one head");
     static_assert(STAGE % 16 == 0 && Q_BYTES % 16 == 0 && (UNIT * MB) % 16 == 0, "16-byte copies");
-    static_assert(OFF_CO % 16 == 0 && OFF_W % 16 == 0, "alignment");
+    static_assert(OFF_W % 16 == 0, "alignment");
     static_assert(4 * (UNIT * MB / 16) <= 32, "one lane per 16 bytes of scales and zeros");
 };
 
@@ -118,10 +115,14 @@ struct DecodeCfg {
 // U = Hkv * prefix[B]; slice S = max(ceil(U / n_ctas), MIN_SLICE_UNITS).
 struct Plan {
     int B, Hkv;
-    int64_t U, S;
+    int64_t U;
+    int64_t Sw;  // units per warp worker
+    int64_t S;   // units per CTA: its warps' slices laid end to end
 };
 
-// All threads of the block build the plan (prefix sums in shared memory).
+// All threads of the block (NW warps) build the plan (prefix sums in shared
+// memory).
+template <int NW>
 __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefix, int64_t* misc) {
     const int B = p.B;
     const int nthr = blockDim.x;
@@ -141,11 +142,11 @@ __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefi
         local += u;
     }
     // exclusive scan of the per-thread sums by warp 0
-    __shared__ int tsum[32 * DECODE_WARPS];
+    __shared__ int tsum[32 * NW];
     tsum[tid] = local;
     __syncthreads();
     if (tid < 32) {
-        constexpr int PER = DECODE_WARPS;
+        constexpr int PER = NW;
         int v[PER];
         int s = 0;
 #pragma unroll
@@ -183,12 +184,15 @@ __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefi
     pl.B = B;
     pl.Hkv = p.c.num_kv_heads;
     pl.U = (int64_t)pl.Hkv * misc[0];
-    const int64_t S = (pl.U + p.n_ctas - 1) / p.n_ctas;
-    pl.S = S < MIN_SLICE_UNITS ? MIN_SLICE_UNITS : S;
+    const int64_t workers = (int64_t)p.n_ctas * NW;
+    const int64_t Sw = (pl.U + workers - 1) / workers;
+    pl.Sw = Sw < MIN_SLICE_UNITS ? MIN_SLICE_UNITS : Sw;
+    pl.S = pl.Sw * NW;
     return pl;
 }
 
-// One piece of a CTA's slice.
+// One piece of a worker's slice (a worker is a warp, or a CTA when the
+// warps' partials are combined).
 struct Piece {
     int b, h;
     int u_lo, u_hi;   // segment-local units [u_lo, u_hi)
@@ -197,24 +201,25 @@ struct Piece {
     int slot;         // partial slot otherwise
 };
 
-// Walks the segment pieces of one CTA's slice.  Holds only scalars and the
-// shared-memory prefix pointer (nothing that forces a stack frame).
+// Walks the segment pieces of worker k's slice [k S, (k + 1) S).  Holds only
+// scalars and the shared-memory prefix pointer (nothing that forces a stack
+// frame).
 struct PieceWalk {
     const int32_t* prefix;
     int B, Hkv;
-    int64_t x, end;
-    int b, h, idx, cta;
+    int64_t x, end, worker;
+    int b, h, idx;
     __device__ int units(int bb) const { return prefix[bb + 1] - prefix[bb]; }
     __device__ int64_t seg_start(int bb, int hh) const {
         return (int64_t)Hkv * prefix[bb] + (int64_t)hh * units(bb);
     }
-    __device__ void begin(const Plan& pl, const int32_t* pre, int c) {
+    __device__ void begin(const Plan& pl, const int32_t* pre, int64_t k, int64_t S) {
         prefix = pre;
         B = pl.B;
         Hkv = pl.Hkv;
-        cta = c;
-        x = (int64_t)c * pl.S;
-        end = x + pl.S;
+        worker = k;
+        x = k * S;
+        end = x + S;
         if (end > pl.U) end = pl.U;
         idx = 0;
         b = h = 0;
@@ -244,7 +249,7 @@ struct PieceWalk {
         L = L < 0 ? 0 : (L > max_tokens ? max_tokens : L);
         pc.len = (int)L;
         pc.whole = (pc.u_lo == 0 && pc.u_hi == n);
-        pc.slot = 2 * cta + (idx == 0 ? 0 : 1);
+        pc.slot = (int)(2 * worker + (idx == 0 ? 0 : 1));
         return pc;
     }
     __device__ void next() {
@@ -281,43 +286,36 @@ __device__ __forceinline__ void transpose_reduce(T* v, int lane) {
     }
 }
 
-// This warp's contiguous share [a, b) of a piece's units.
-__device__ __forceinline__ void warp_range(const Piece& pc, int warp, int& a, int& b) {
-    const int n = pc.u_hi - pc.u_lo;
-    const int per = (n + DECODE_WARPS - 1) / DECODE_WARPS;
-    a = pc.u_lo + warp * per;
-    b = min(pc.u_hi, a + per);
-    if (a > b) a = b;
-}
-
-// Log-sum-exp merge of the split partials of segment (b, h), whose units
-// span [a, a + units) of the work line cut into slices of S units.  The n
-// CTAs c_first..c_last touched it; CTA c left its partial in slot 2c, or in
-// 2c+1 when the segment is not the first piece of its slice.  Every thread
-// owns float4 elements of the G x D output rows and merges the partials of
-// its head online,
-//   M' = max(M, m_c), L' = L 2^(M - M') + l_c 2^(m_c - M'),
-//   O' = O 2^(M - M') + o_c 2^(m_c - M'),   out = O / L,
+// Log-sum-exp merge of the partials that workers k0..k1 left for the
+// segment starting at work-line unit a.  Workers cut the line in slices of S
+// units; worker k's partial of the segment is in slot 2k, or 2k+1 when the
+// segment is not the first piece of its slice, of the arrays (so, sm, sl).
+// Every thread owns float4 elements of the G x D output rows and merges the
+// partials of its head online,
+//   M' = max(M, m_k), L' = L 2^(M - M') + l_k 2^(m_k - M'),
+//   O' = O 2^(M - M') + o_k 2^(m_k - M'),
 // eight partials at a time: each element's o loads are all in flight
-// together, and (m_c, l_c) are loaded once per head by one lane each and
-// shuffled to the lanes of that head.  Loads bypass L1: the partials come
-// from other CTAs of the same launch.  Every thread of the CTA calls this.
-template <int D, int G>
-__device__ __forceinline__ void merge_segment(const DecodeParams& p, int b, int h, int64_t a, int64_t units,
-                                              int64_t S, int tid) {
-    constexpr int NT = 32 * DECODE_WARPS;            // threads of the CTA
+// together, and (m_k, l_k) are loaded once per head by one lane each and
+// shuffled to the lanes of that head.  The result goes to `row` as O / L
+// (final output rows), or, when row is null, to (dst_o, dst_m, dst_l) as a
+// partial.  Loads bypass L1: the partials come from other warps and CTAs of
+// the same launch.  Every thread of the CTA (NT threads) calls this.
+template <int D, int G, int NT>
+__device__ __forceinline__ void merge_workers(const float* so, const float* sm, const float* sl, int64_t a,
+                                              int64_t S, int64_t k0, int64_t k1, int tid, float* row,
+                                              float* dst_o, float* dst_m, float* dst_l) {
     constexpr int NE = G * D / 4;                    // float4 elements of the output rows
     constexpr int EPT = (NE + NT - 1) / NT;          // per thread
     constexpr int LPH = D / 4 < 32 ? D / 4 : 32;     // lanes of a warp that share a head
     constexpr int UNR = 8;                           // partials per round
     static_assert(UNR <= LPH, "one lane per partial of a round");
-    const int64_t c_first = a / S, c_last = (a + units - 1) / S;
-    const int n = (int)(c_last - c_first + 1);
-    const bool first_odd = a != c_first * S;
+    const int n = (int)(k1 - k0 + 1);
+    const int64_t k_start = a / S;  // the worker whose slice holds the segment's first unit
+    const bool start_odd = a != k_start * S;
     const int lane = tid & 31, base = lane / LPH * LPH, sub = lane % LPH;
     auto slot_of = [&](int i) -> int64_t {
-        const int64_t c = c_first + i;
-        return (i == 0 && first_odd) ? 2 * c + 1 : 2 * c;
+        const int64_t k = k0 + i;
+        return (k == k_start && start_odd) ? 2 * k + 1 : 2 * k;
     };
     int eg[EPT], ej[EPT];
     float M[EPT], L[EPT];
@@ -340,8 +338,8 @@ __device__ __forceinline__ void merge_segment(const DecodeParams& p, int b, int 
             my_l[k] = 0.0f;
             if (sub < UNR && i0 + sub < n && eg[k] >= 0) {
                 const int64_t s = slot_of(i0 + sub);
-                my_m[k] = __ldcg(p.ws_m + s * G + eg[k]);
-                my_l[k] = __ldcg(p.ws_l + s * G + eg[k]);
+                my_m[k] = __ldcg(sm + s * G + eg[k]);
+                my_l[k] = __ldcg(sl + s * G + eg[k]);
             }
         }
 #pragma unroll
@@ -350,7 +348,7 @@ __device__ __forceinline__ void merge_segment(const DecodeParams& p, int b, int 
 #pragma unroll
             for (int k = 0; k < EPT; ++k)
                 if (i0 + u < n && eg[k] >= 0)
-                    ov[u][k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (s * G + eg[k]) * D + ej[k]));
+                    ov[u][k] = __ldcg(reinterpret_cast<const float4*>(so + (s * G + eg[k]) * D + ej[k]));
         }
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
@@ -374,9 +372,91 @@ __device__ __forceinline__ void merge_segment(const DecodeParams& p, int b, int 
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
         if (eg[k] < 0) continue;
-        const float inv = (L[k] > 0.0f) ? 1.0f / L[k] : 0.0f;
-        float* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G + eg[k]) * D + ej[k];
-        *reinterpret_cast<float4*>(out) = make_float4(O[k].x * inv, O[k].y * inv, O[k].z * inv, O[k].w * inv);
+        if (row) {
+            const float inv = (L[k] > 0.0f) ? 1.0f / L[k] : 0.0f;
+            *reinterpret_cast<float4*>(row + eg[k] * D + ej[k]) =
+                make_float4(O[k].x * inv, O[k].y * inv, O[k].z * inv, O[k].w * inv);
+        } else {
+            *reinterpret_cast<float4*>(dst_o + eg[k] * D + ej[k]) = O[k];
+            if (ej[k] == 0) {
+                dst_m[eg[k]] = M[k];
+                dst_l[eg[k]] = L[k];
+            }
+        }
+    }
+}
+
+// A piece of a CTA's slice whose result needs the partials of several warps.
+struct EndPiece {
+    int64_t a;      // work-line unit where the segment starts
+    int64_t units;  // units of the segment
+    int64_t k0;     // first warp worker touching the piece
+    int n;          // warp workers touching it
+    int b, h;
+    int slot;       // CTA partial slot, or -1: the segment ends here (final rows)
+};
+
+// One float4 element (head g, channels j..j+3) of the online log-sum-exp merge
+// of the partials workers k0..k0+n-1 left for the segment starting at unit
+// a (slices of S units; slot rule as in merge_workers).  Called by all 32
+// lanes of a warp together (active = this lane has an element); the lanes
+// that share a head share their (m, l) loads by shuffle.  Writes O / L to
+// row, or (O, M, L) to the destination partial.
+template <int D, int G>
+__device__ __forceinline__ void merge_element(const float* so, const float* sm, const float* sl, int64_t a,
+                                              int64_t S, int64_t k0, int n, int g, int j, int lane, bool active,
+                                              float* row, float* dst_o, float* dst_m, float* dst_l) {
+    constexpr int LPH = D / 4 < 32 ? D / 4 : 32;
+    constexpr int UNR = 8;
+    const int64_t k_start = a / S;
+    const bool start_odd = a != k_start * S;
+    const int base = lane / LPH * LPH, sub = lane % LPH;
+    auto slot_of = [&](int i) -> int64_t {
+        const int64_t k = k0 + i;
+        return (k == k_start && start_odd) ? 2 * k + 1 : 2 * k;
+    };
+    // lanes of one head come from the same piece: n is uniform over them
+    float M = -INFINITY, L = 0.0f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int nmax = __reduce_max_sync(0xffffffffu, active ? n : 0);
+    for (int i0 = 0; i0 < nmax; i0 += UNR) {
+        float my_m = -INFINITY, my_l = 0.0f;
+        if (active && sub < UNR && i0 + sub < n) {
+            const int64_t s = slot_of(i0 + sub);
+            my_m = __ldcg(sm + s * G + g);
+            my_l = __ldcg(sl + s * G + g);
+        }
+        float4 ov[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u)
+            if (active && i0 + u < n)
+                ov[u] = __ldcg(reinterpret_cast<const float4*>(so + (slot_of(i0 + u) * G + g) * D + j));
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const float mc = __shfl_sync(0xffffffffu, my_m, base + u);
+            const float lc = __shfl_sync(0xffffffffu, my_l, base + u);
+            if (!active || i0 + u >= n || mc == -INFINITY) continue;
+            const float nm = fmaxf(M, mc);
+            const float fa = (M == -INFINITY) ? 0.0f : fast_exp2(M - nm);
+            const float fb = fast_exp2(mc - nm);
+            L = fmaf(L, fa, lc * fb);
+            O.x = fmaf(O.x, fa, ov[u].x * fb);
+            O.y = fmaf(O.y, fa, ov[u].y * fb);
+            O.z = fmaf(O.z, fa, ov[u].z * fb);
+            O.w = fmaf(O.w, fa, ov[u].w * fb);
+            M = nm;
+        }
+    }
+    if (!active) return;
+    if (row) {
+        const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+        *reinterpret_cast<float4*>(row + g * D + j) = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    } else {
+        *reinterpret_cast<float4*>(dst_o + g * D + j) = O;
+        if (j == 0) {
+            dst_m[g] = M;
+            dst_l[g] = L;
+        }
     }
 }
 
@@ -393,7 +473,7 @@ __device__ __forceinline__ void merge_segment(const DecodeParams& p, int b, int 
 // together.  No CTA waits on another.  Kept out of line so that the rarely
 // run merge does not shape the code of the main loop.  Called by every
 // thread of the CTA; `flag` is a shared int.
-template <int D, int G>
+template <int D, int G, int NT>
 __device__ __noinline__ void arrive_and_merge(const DecodeParams& p, int b, int h, const int32_t* prefix, int64_t S,
                                               int tid, int* flag) {
     const int Hkv = p.c.num_kv_heads;
@@ -430,12 +510,13 @@ __device__ __noinline__ void arrive_and_merge(const DecodeParams& p, int b, int 
     __syncthreads();
     if (*flag) {
         __threadfence();
-        merge_segment<D, G>(p, b, h, a, units, S, tid);
+        merge_workers<D, G, NT>(p.ws_o, p.ws_m, p.ws_l, a, S, a / S, (a + units - 1) / S, tid,
+                                p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D, nullptr, nullptr, nullptr);
     }
 }
 
 template <int SCHEME, int D, int G>
-__global__ void __launch_bounds__(DecodeCfg<SCHEME, D, G>::THREADS, (DecodeCfg<SCHEME, D, G>::MIN_CTAS))
+__global__ void __launch_bounds__(DecodeCfg<SCHEME, D, G>::THREADS, 1)
 decode_partial_kernel(const DecodeParams p) {
     using C = DecodeCfg<SCHEME, D, G>;
     constexpr int STAGES_ = C::STAGES;
@@ -445,7 +526,7 @@ decode_partial_kernel(const DecodeParams p) {
     int64_t* misc = reinterpret_cast<int64_t*>(smem + C::OFF_MISC);
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + C::OFF_PLAN);
 
-    const Plan plan = build_plan(p, prefix, misc);  // contains __syncthreads
+    const Plan plan = build_plan<C::WARPS>(p, prefix, misc);  // contains __syncthreads
     if (blockIdx.x == 0) {
         // publish the plan for the merge kernel: [U, S] then prefix[0..B]
         int64_t* wsplan = reinterpret_cast<int64_t*>(p.ws_l + 2 * (size_t)p.n_ctas * G);
@@ -474,8 +555,11 @@ decode_partial_kernel(const DecodeParams p) {
     // Issues this warp's units, in the order the compute loop below consumes
     // them, STAGES-1 units ahead.  Every call commits exactly one cp.async
     // group (empty once the units run out).
+    // Every warp is a worker with its own slice of Sw units of the work line;
+    // the CTA's slice is its warps' slices end to end.
+    const int64_t worker = (int64_t)blockIdx.x * C::WARPS + warp;
     PieceWalk fw;
-    fw.begin(plan, prefix, blockIdx.x);
+    fw.begin(plan, prefix, worker, plan.Sw);
     Piece fpc;
     fpc.b = fpc.h = fpc.u_lo = fpc.u_hi = fpc.len = fpc.slot = 0;
     fpc.whole = false;
@@ -486,7 +570,8 @@ decode_partial_kernel(const DecodeParams p) {
         fdone = true;
         while (!fw.done()) {
             fpc = fw.get(p);
-            warp_range(fpc, warp, fua, fub);
+            fua = fpc.u_lo;
+            fub = fpc.u_hi;
             if (fua < fub) {
                 fu = fua;
                 flp = (fu * UNIT) / P;  // once per piece; then advanced incrementally
@@ -576,9 +661,6 @@ decode_partial_kernel(const DecodeParams p) {
     uint8_t* WB = wbase;                                           // dp4a path: weight bytes
     float* WQ = reinterpret_cast<float*>(wbase + UNIT * G * 4);    // [G]
     float* AL = WQ + G;                                            // [G]
-    float* CO = reinterpret_cast<float*>(smem + C::OFF_CO);
-    float* CM = reinterpret_cast<float*>(smem + C::OFF_CM);
-    float* CL = reinterpret_cast<float*>(smem + C::OFF_CL);
     // score-lane coordinates
     const int k_tok = lane / C::KL;
     const int k_c0 = (lane % C::KL) * C::CPL;
@@ -593,11 +675,12 @@ decode_partial_kernel(const DecodeParams p) {
     for (int i = 0; i < STAGES_ - 1; ++i) issue_one();  // prologue
     int cst = 0;  // stage the next computed unit sits in
     PieceWalk walk;
-    walk.begin(plan, prefix, blockIdx.x);
+    walk.begin(plan, prefix, worker, plan.Sw);
     for (; !walk.done(); walk.next()) {
         const Piece pc = walk.get(p);
         int ua, ub;
-        warp_range(pc, warp, ua, ub);
+        ua = pc.u_lo;
+        ub = pc.u_hi;
         uint32_t qw[G][C::QW];  // query: INT8/INT4 fixed-point bytes, FP8 fp16 pairs
         float sq[G];            // INT4: fixed-point step per head
         float qisum[G];         // INT4: sum of this lane's fixed-point query channels, per head
@@ -999,7 +1082,9 @@ decode_partial_kernel(const DecodeParams p) {
             __syncwarp();
         }
 
-        // ---- per-warp state -> shared memory
+        // ---- end of this warp's piece: sum l over the token groups and o over
+        // the lanes that share channels; a segment inside this warp's slice
+        // is final, any other piece leaves a partial in the warp's slot
 #pragma unroll
         for (int off = C::KL; off < 32; off <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
 #pragma unroll
@@ -1012,49 +1097,87 @@ decode_partial_kernel(const DecodeParams p) {
                 o[g][jj] = v;
             }
         }
-        if (v_tok == 0) {
+        if (pc.whole) {
+            float* row = p.out + ((int64_t)pc.b * p.Hq + (int64_t)pc.h * G) * D;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float* dst = CO + (warp * G + g) * D + v_c0;
+                const float lg = __shfl_sync(0xffffffffu, l_run, g * C::DUP);  // lane g*DUP holds head g
+                const float inv = (lg > 0.0f) ? 1.0f / lg : 0.0f;
+                if (v_tok == 0) {
 #pragma unroll
-                for (int jj = 0; jj < C::VCH; jj += 4)
-                    *reinterpret_cast<float4*>(dst + jj) = make_float4(o[g][jj], o[g][jj + 1], o[g][jj + 2], o[g][jj + 3]);
-            }
-        }
-        if (k_writer && k_tok == 0) {
-            CM[warp * G + k_head] = m_run;
-            CL[warp * G + k_head] = l_run;
-        }
-        __syncthreads();
-        // ---- combine the warps; final row or split partial
-        for (int idx = tid; idx < G * D; idx += C::THREADS) {
-            const int g = idx / D;
-            const int jj = idx % D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < C::WARPS; ++w) M = fmaxf(M, CM[w * G + g]);
-            float L = 0.0f, O = 0.0f;
-#pragma unroll
-            for (int w = 0; w < C::WARPS; ++w) {
-                const float mw = CM[w * G + g];
-                const float f = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - M);
-                L = fmaf(CL[w * G + g], f, L);
-                O = fmaf(CO[(w * G + g) * D + jj], f, O);
-            }
-            if (pc.whole) {
-                p.out[((int64_t)pc.b * p.Hq + (int64_t)pc.h * G + g) * D + jj] = (L > 0.0f) ? O / L : 0.0f;
-            } else {
-                p.ws_o[((int64_t)pc.slot * G + g) * D + jj] = O;
-                if (jj == 0) {
-                    p.ws_m[pc.slot * G + g] = M;
-                    p.ws_l[pc.slot * G + g] = L;
+                    for (int jj = 0; jj < C::VCH; jj += 4)
+                        *reinterpret_cast<float4*>(row + g * D + v_c0 + jj) =
+                            make_float4(o[g][jj] * inv, o[g][jj + 1] * inv, o[g][jj + 2] * inv, o[g][jj + 3] * inv);
                 }
             }
+        } else {
+            const int64_t slot = pc.slot;
+            if (v_tok == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float* dst = p.wp_o + (slot * G + g) * D + v_c0;
+#pragma unroll
+                    for (int jj = 0; jj < C::VCH; jj += 4)
+                        *reinterpret_cast<float4*>(dst + jj) = make_float4(o[g][jj], o[g][jj + 1], o[g][jj + 2], o[g][jj + 3]);
+                }
+            }
+            if (k_writer && k_tok == 0) {
+                p.wp_m[slot * G + k_head] = m_run;
+                p.wp_l[slot * G + k_head] = l_run;
+            }
         }
-        if (p.fuse_merge && !pc.whole) arrive_and_merge<D, G>(p, pc.b, pc.h, prefix, plan.S, tid, &s_last);
-        __syncthreads();
     }
+
+    // ---- the CTA's pieces that span more than one warp's slice, or that
+    // continue in another CTA: combine the partials its warps left, all such
+    // pieces at once (at most one per warp boundary plus the two ends)
     cp_async_wait<0>();
+    __syncthreads();  // all warps' rows and partials are written; the rings are idle
+    EndPiece* eps = reinterpret_cast<EndPiece*>(smem + C::OFF_STAGES);
+    static_assert((C::WARPS + 1) * sizeof(EndPiece) <= (size_t)C::WARPS * STAGES_ * C::STAGE, "room for the list");
+    __shared__ int s_np;
+    if (tid == 0) {
+        int np = 0;
+        PieceWalk cw;
+        cw.begin(plan, prefix, blockIdx.x, plan.S);
+        for (; !cw.done(); cw.next()) {
+            const Piece pc = cw.get(p);
+            const int64_t units = prefix[pc.b + 1] - prefix[pc.b];
+            const int64_t a = (int64_t)Hkv * prefix[pc.b] + (int64_t)pc.h * units;
+            const int64_t k0 = (a + pc.u_lo) / plan.Sw, k1 = (a + pc.u_hi - 1) / plan.Sw;
+            if (pc.whole && k0 == k1) continue;  // inside one warp's slice: already final
+            EndPiece& e = eps[np++];
+            e.a = a;
+            e.units = units;
+            e.k0 = k0;
+            e.n = (int)(k1 - k0 + 1);
+            e.b = pc.b;
+            e.h = pc.h;
+            e.slot = pc.whole ? -1 : pc.slot;
+        }
+        s_np = np;
+    }
+    __syncthreads();
+    const int np = s_np;
+    constexpr int NE = G * D / 4;  // float4 elements of one piece's G output rows
+    for (int i0 = warp * 32; i0 < np * NE; i0 += C::THREADS) {  // warp-uniform trip count
+        const int it = i0 + lane;
+        const EndPiece& e = eps[(it < np * NE ? it : i0) / NE];
+        const int elem = it % NE;
+        merge_element<D, G>(p.wp_o, p.wp_m, p.wp_l, e.a, plan.Sw, e.k0, e.n, elem / (D / 4), (elem % (D / 4)) * 4,
+                            lane, it < np * NE,
+                            e.slot < 0 ? p.out + ((int64_t)e.b * p.Hq + (int64_t)e.h * G) * D : nullptr,
+                            e.slot < 0 ? nullptr : p.ws_o + (int64_t)e.slot * G * D,
+                            e.slot < 0 ? nullptr : p.ws_m + (int64_t)e.slot * G,
+                            e.slot < 0 ? nullptr : p.ws_l + (int64_t)e.slot * G);
+    }
+    if (p.fuse_merge) {
+        __syncthreads();  // the CTA's partials are written
+        for (int i = 0; i < np; ++i) {
+            const EndPiece e = eps[i];
+            if (e.slot >= 0) arrive_and_merge<D, G, C::THREADS>(p, e.b, e.h, prefix, plan.S, tid, &s_last);
+        }
+    }
 }
 
 // ---- K3: merge ------------------------------------------------------------------
@@ -1063,7 +1186,7 @@ decode_partial_kernel(const DecodeParams p) {
 // partials of CTAs c_first..c_last:  M = max m_c, L = sum l_c 2^(m_c - M),
 // out = sum o_c 2^(m_c - M) / L.
 template <int D, int G>
-__global__ void __launch_bounds__(32 * DECODE_WARPS) decode_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(MERGE_THREADS) decode_merge_kernel(const DecodeParams p) {
     const int b = blockIdx.x / p.c.num_kv_heads;
     const int h = blockIdx.x % p.c.num_kv_heads;
     const int64_t* wsplan = reinterpret_cast<const int64_t*>(p.ws_l + 2 * (size_t)p.n_ctas * G);
@@ -1077,7 +1200,8 @@ __global__ void __launch_bounds__(32 * DECODE_WARPS) decode_merge_kernel(const D
     }
     const int64_t a = (int64_t)p.c.num_kv_heads * prefix[b] + (int64_t)h * units;
     if (a / S == (a + units - 1) / S) return;  // finished inside one CTA's slice
-    merge_segment<D, G>(p, b, h, a, units, S, threadIdx.x);
+    merge_workers<D, G, MERGE_THREADS>(p.ws_o, p.ws_m, p.ws_l, a, S, a / S, (a + units - 1) / S, threadIdx.x,
+                                       p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D, nullptr, nullptr, nullptr);
 }
 
 // Shared memory attribute per device, set once (host-only state).
@@ -1122,7 +1246,7 @@ cudaError_t launch_decode_partial_t(const DecodeParams& p, cudaStream_t s) {
 template <int D, int G>
 cudaError_t launch_decode_merge_t(const DecodeParams& p, cudaStream_t s) {
     const int64_t n = (int64_t)p.B * p.c.num_kv_heads;
-    decode_merge_kernel<D, G><<<(unsigned)n, 32 * DECODE_WARPS, 0, s>>>(p);
+    decode_merge_kernel<D, G><<<(unsigned)n, MERGE_THREADS, 0, s>>>(p);
     return cudaGetLastError();
 }
 

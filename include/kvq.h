@@ -216,7 +216,7 @@ kvq_status kvq_last_device_error(kvq_stream_t stream);
  * problem would need more scratch than the array holds (kvq_decode_workspace_bytes
  * reports the need).  Other arguments, rules and errors are those of
  * kvq_decode_attn. */
-#define KVQ_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+#define KVQ_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 
 kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const void* q, const int32_t* block_table,
                                    const int32_t* seq_lens, float* out, int32_t num_seqs,

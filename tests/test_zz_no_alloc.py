@@ -32,7 +32,7 @@ def test_noalloc_matches_workspace_call_twice(scheme, Hq, Hkv):
     q, bt, sl = dev_bits(case.q), dev(case.bt), dev(lens)
     ref = case.decode()  # kvq_decode_attn with a torch-allocated workspace
     need = kvq.decode_workspace_bytes(case.g, len(lens), Hq, bt.shape[1])
-    assert need <= 8 << 20
+    assert need <= 16 << 20  # KVQ_STATIC_SCRATCH_BYTES
     for _ in range(2):
         out = torch.full((len(lens), Hq, 128), float("nan"), dtype=torch.float32, device=DEV)
         st = kvq.lib.kvq_decode_attn_noalloc(ctypes.byref(case.g.struct), ctypes.c_void_p(q.data_ptr()),
