@@ -460,59 +460,42 @@ __device__ __forceinline__ void merge_element(const float* so, const float* sm, 
     }
 }
 
-// One-launch form, at the end of a piece that is not a whole segment: count
-// this CTA's arrival on the segment; the CTA that brings the last of its n
-// partials merges them.  The counter holds (generation << 32) | arrivals.
-// An arrival adds 1 and reads the old value back in the same atomic; if
-// the old value carries this call's generation, the arrival is counted.
-// Otherwise the word is left over from an earlier call (or is garbage), and
-// the CTA installs (generation << 32) | 1 with a compare-and-swap, or finds
-// that another CTA did and adds again.  Every CTA is counted exactly once.
-// Only the first arrivals of a call can meet a stale word, so the rest take
-// a single atomic and contention stays low even when dozens of CTAs arrive
-// together.  No CTA waits on another.  Kept out of line so that the rarely
-// run merge does not shape the code of the main loop.  Called by every
-// thread of the CTA; `flag` is a shared int.
-template <int D, int G, int NT>
-__device__ __noinline__ void arrive_and_merge(const DecodeParams& p, int b, int h, const int32_t* prefix, int64_t S,
-                                              int tid, int* flag) {
-    const int Hkv = p.c.num_kv_heads;
-    __threadfence();
-    __syncthreads();
-    const int64_t units = prefix[b + 1] - prefix[b];
-    const int64_t a = (int64_t)Hkv * prefix[b] + (int64_t)h * units;
-    if (tid == 0) {
-        const unsigned long long n = (unsigned long long)((a + units - 1) / S - a / S + 1);
-        unsigned long long* ctr = p.seg_ctr + (int64_t)b * Hkv + h;
-        const unsigned long long tag = (unsigned long long)p.gen << 32;
-        constexpr unsigned long long HI = 0xFFFFFFFF00000000ull, LO = 0xFFFFFFFFull;
-        const unsigned long long old = atomicAdd(ctr, 1ull);  // the value before this add
-        unsigned long long count;
-        if ((old & HI) == tag) {
-            count = (old & LO) + 1;
-        } else {
-            unsigned long long expect = old + 1;  // the word just after this add, if untouched
-            while (true) {
-                const unsigned long long seen = atomicCAS(ctr, expect, tag | 1ull);
-                if (seen == expect) {  // installed this call's generation, counted as the first
-                    count = 1;
-                    break;
-                }
-                if ((seen & HI) == tag) {  // another arrival installed it: count by adding
-                    count = (atomicAdd(ctr, 1ull) & LO) + 1;
-                    break;
-                }
-                expect = seen;  // other stale adds moved the word: install over it
+// One-launch form: count one CTA's arrival on segment (b, h), which n CTAs
+// touch; returns true for the CTA that brings the last partial (it merges
+// them).  The counter holds (generation << 32) | arrivals.  An arrival adds 1
+// and reads the old value back in the same atomic; if the old value carries
+// this call's generation, the arrival is counted.  Otherwise the word is left
+// over from an earlier call (or is garbage), and the CTA installs
+// (generation << 32) | 1 with a compare-and-swap, or finds that another CTA
+// did and adds again.  Every CTA is counted exactly once.  Only the first
+// arrivals of a call can meet a stale word, so the rest take a single atomic
+// and contention stays low even when dozens of CTAs arrive together.  No CTA
+// waits on another.  One thread calls this, after the CTA's partial is
+// written and fenced.  Kept out of line: it is off the main loop's path.
+static __device__ __noinline__ bool count_arrival(const DecodeParams& p, int b, int h, unsigned long long n) {
+    unsigned long long* ctr = p.seg_ctr + (int64_t)b * p.c.num_kv_heads + h;
+    const unsigned long long tag = (unsigned long long)p.gen << 32;
+    constexpr unsigned long long HI = 0xFFFFFFFF00000000ull, LO = 0xFFFFFFFFull;
+    const unsigned long long old = atomicAdd(ctr, 1ull);  // the value before this add
+    unsigned long long count;
+    if ((old & HI) == tag) {
+        count = (old & LO) + 1;
+    } else {
+        unsigned long long expect = old + 1;  // the word just after this add, if untouched
+        while (true) {
+            const unsigned long long seen = atomicCAS(ctr, expect, tag | 1ull);
+            if (seen == expect) {  // installed this call's generation, counted as the first
+                count = 1;
+                break;
             }
+            if ((seen & HI) == tag) {  // another arrival installed it: count by adding
+                count = (atomicAdd(ctr, 1ull) & LO) + 1;
+                break;
+            }
+            expect = seen;  // other stale adds moved the word: install over it
         }
-        *flag = (count == n) ? 1 : 0;
     }
-    __syncthreads();
-    if (*flag) {
-        __threadfence();
-        merge_workers<D, G, NT>(p.ws_o, p.ws_m, p.ws_l, a, S, a / S, (a + units - 1) / S, tid,
-                                p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D, nullptr, nullptr, nullptr);
-    }
+    return count == n;
 }
 
 template <int SCHEME, int D, int G>
@@ -546,7 +529,6 @@ decode_partial_kernel(const DecodeParams p) {
             for (int i = threadIdx.x; i < p.Hq * D; i += blockDim.x) row[i] = 0.0f;
         }
     }
-    __shared__ int s_last;  // this CTA delivered the last partial of the current segment
     const uint64_t pol_kv = l2_evict_first_policy();  // pages are read once
     const uint64_t pol_q = l2_evict_normal_policy();  // query rows are shared by the CTA's warps
     uint8_t* ring = smem + C::OFF_STAGES + warp * STAGES_ * C::STAGE;
@@ -1172,10 +1154,31 @@ decode_partial_kernel(const DecodeParams p) {
                             e.slot < 0 ? nullptr : p.ws_l + (int64_t)e.slot * G);
     }
     if (p.fuse_merge) {
-        __syncthreads();  // the CTA's partials are written
-        for (int i = 0; i < np; ++i) {
-            const EndPiece e = eps[i];
-            if (e.slot >= 0) arrive_and_merge<D, G, C::THREADS>(p, e.b, e.h, prefix, plan.S, tid, &s_last);
+        // count this CTA's arrivals on the (at most two) segments it shares
+        // with other CTAs, all at once; then merge, element-parallel, those
+        // for which it brought the last partial
+        __threadfence();
+        __syncthreads();  // the CTA's partials are written and visible
+        if (tid < np) {
+            EndPiece& e = eps[tid];
+            if (e.slot >= 0) {
+                const unsigned long long n =
+                    (unsigned long long)((e.a + e.units - 1) / plan.S - e.a / plan.S + 1);
+                if (!count_arrival(p, e.b, e.h, n)) e.slot = -2;  // not the last: nothing to merge
+            } else {
+                e.slot = -2;  // final rows already written above
+            }
+        }
+        __syncthreads();
+        __threadfence();  // see the other CTAs' partials
+        for (int i0 = warp * 32; i0 < np * NE; i0 += C::THREADS) {
+            const int it = i0 + lane;
+            const EndPiece& e = eps[(it < np * NE ? it : i0) / NE];
+            const int elem = it % NE;
+            const int64_t k0 = e.a / plan.S, n = (e.a + e.units - 1) / plan.S - k0 + 1;
+            merge_element<D, G>(p.ws_o, p.ws_m, p.ws_l, e.a, plan.S, k0, e.slot == -2 ? 0 : (int)n,
+                                elem / (D / 4), (elem % (D / 4)) * 4, lane, it < np * NE && e.slot != -2,
+                                p.out + ((int64_t)e.b * p.Hq + (int64_t)e.h * G) * D, nullptr, nullptr, nullptr);
         }
     }
 }
