@@ -37,10 +37,11 @@
 //    two shuffles); the weights p * value scale go to shared memory;
 //  * values: each lane owns 4 (or 8) channels x G heads of fp32 accumulators.
 //    INT8: the unit's weights of each head become 16-bit fixed point
-//    relative to their maximum, the lane transposes the codes of 4
-//    consecutive tokens into one word per channel, dp4a accumulates the
-//    unit in int32 (high byte, times 256, then low byte), and one FMA per
-//    accumulator adds the unit.  FP8, INT4: scalar FMAs on exactly
+//    relative to their maximum; the V codes are stored with 4 consecutive
+//    tokens of a channel in one word, so one 16-byte load gives a lane its 4
+//    channels of a 4-token block; dp4a accumulates the unit in int32 (high
+//    byte, times 256, then low byte), and one FMA per accumulator adds the
+//    unit.  FP8, INT4: scalar FMAs on exactly
 //    converted codes (INT4 adds the zero-points once per token).
 // The query rows of a piece travel in the stage of the warp's first unit of
 // that piece.  At the end of a piece the four warps' states are combined in
@@ -931,22 +932,16 @@ decode_partial_kernel(const DecodeParams p) {
                     }
                 }
                 if constexpr (C::VDP) {
-                    // codes of 4 consecutive tokens x this lane's 4 channels,
-                    // transposed to one word per channel (token bytes in order)
+                    // V codes are stored 4 tokens x 1 channel per word: one
+                    // 16-byte load gives this lane's 4 channels of a 4-token block
                     uint32_t x[C::NBLK][4];
 #pragma unroll
                     for (int k = 0; k < C::NBLK; ++k) {
-                        const uint8_t* src = stg + C::VC + (4 * (v_tok + k * C::VT)) * D + v_c0;
-                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(src);
-                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(src + D);
-                        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(src + 2 * D);
-                        const uint32_t w3 = *reinterpret_cast<const uint32_t*>(src + 3 * D);
-                        const uint32_t a01 = __byte_perm(w0, w1, 0x5140), b01 = __byte_perm(w0, w1, 0x7362);
-                        const uint32_t a23 = __byte_perm(w2, w3, 0x5140), b23 = __byte_perm(w2, w3, 0x7362);
-                        x[k][0] = __byte_perm(a01, a23, 0x5410);
-                        x[k][1] = __byte_perm(a01, a23, 0x7632);
-                        x[k][2] = __byte_perm(b01, b23, 0x5410);
-                        x[k][3] = __byte_perm(b01, b23, 0x7632);
+                        const uint4 r = *reinterpret_cast<const uint4*>(stg + C::VC + (v_tok + k * C::VT) * (4 * D) + 4 * v_c0);
+                        x[k][0] = r.x;
+                        x[k][1] = r.y;
+                        x[k][2] = r.z;
+                        x[k][3] = r.w;
                     }
                     // sum over the unit of (256 hi + lo) * code in int32 (|sum| < 2^28),
                     // then one FMA per accumulator with the step wq

@@ -97,7 +97,7 @@ class Case:
         names = ["k_codes", "v_codes", "k_scales", "v_scales"] + (["k_zeros", "v_zeros"] if w.scheme == "int4" else [])
         rows = None if full else self.used_rows()
         for name in names:
-            g = getattr(self.g, name).cpu().numpy()
+            g = self.g.codes_rowmajor(name[0]).reshape(-1) if "codes" in name else getattr(self.g, name).cpu().numpy()
             o = getattr(self.o, name).view(np.uint8)
             width = cb if "codes" in name else mb
             if rows is not None:
