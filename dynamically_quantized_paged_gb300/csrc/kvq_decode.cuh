@@ -471,8 +471,9 @@ __device__ __forceinline__ void merge_element(const float* so, const float* sm, 
 // did and adds again.  Every CTA is counted exactly once.  Only the first
 // arrivals of a call can meet a stale word, so the rest take a single atomic
 // and contention stays low even when dozens of CTAs arrive together.  No CTA
-// waits on another.  One thread calls this, after the CTA's partial is
-// written and fenced.  Kept out of line: it is off the main loop's path.
+// waits on another.  The generation is odd, so a cleared word is stale.  One
+// thread calls this, after the CTA's partial is written and fenced.  Kept out
+// of line: it is off the main loop's path.
 static __device__ __noinline__ bool count_arrival(const DecodeParams& p, int b, int h, unsigned long long n) {
     unsigned long long* ctr = p.seg_ctr + (int64_t)b * p.c.num_kv_heads + h;
     const unsigned long long tag = (unsigned long long)p.gen << 32;
@@ -496,6 +497,10 @@ static __device__ __noinline__ bool count_arrival(const DecodeParams& p, int b, 
             expect = seen;  // other stale adds moved the word: install over it
         }
     }
+    // The last arrival clears the word: no other CTA touches it again in this
+    // call, and a cleared word reads as stale to the next call, so a replayed
+    // call (same generation) starts over too.
+    if (count == n) atomicExch(ctr, 0ull);
     return count == n;
 }
 

@@ -164,9 +164,11 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_seqs,
  * which physical pages hold the tokens.  One launch: a (sequence, KV head)
  * whose tokens are split across CTAs is merged by the CTA that delivers its
  * last partial (arrivals are counted in workspace words tagged with a per-call
- * generation, so the workspace needs no zeroing).  kvq_decode_partial followed
- * by kvq_decode_merge is the equivalent two-launch form and gives bitwise the
- * same output. */
+ * generation, so the workspace needs no zeroing; the last arrival clears its
+ * word, so a recorded call can be replayed, e.g. from a CUDA graph, as long
+ * as no two calls sharing a workspace run at the same time).
+ * kvq_decode_partial followed by kvq_decode_merge is the equivalent
+ * two-launch form and gives bitwise the same output. */
 kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const int32_t* block_table,
                            const int32_t* seq_lens, float* out, int32_t num_seqs,
                            int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,

@@ -199,3 +199,32 @@ def test_append_slot_outside_pool_is_flagged_and_negative_slots_skipped():
     bt = np.array([[0, 1, 7]], np.int32)
     kvq.append(g, dev(np.array([1], np.int64)), dev_bits(k[:1]), dev_bits(v[:1]), block_table=dev(bt))
     assert kvq.last_device_error() == 4
+
+
+def test_graph_replay_matches_eager_call():
+    """A decode_attn captured in a CUDA graph and replayed several times on
+    one workspace gives the eager call's output bit for bit (the arrival
+    counters are cleared by each call, so the replayed generation is
+    harmless)."""
+    w = small("int8", 32, 8, 128, 16)
+    lens = np.array([9000, 40, 2000, 0, 777, 3000], np.int32)
+    case = Case(w, lens, oracle_seqs=[])
+    ref = case.decode()
+    q, bt, sl = dev_bits(case.q), dev(case.bt), dev(lens)
+    out = torch.full((len(lens), 32, 128), float("nan"), dtype=torch.float32, device=DEV)
+    ws = kvq.alloc_workspace(case.g, len(lens), 32, case.bt.shape[1], device=DEV)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):  # warm-up outside capture (sets kernel attributes)
+        kvq.decode_attn(case.g, q, bt, sl, out, ws, stream=stream)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        kvq.decode_attn(case.g, q, bt, sl, out, ws, stream=stream)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert kvq.last_device_error() == kvq.OK
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), ref)
