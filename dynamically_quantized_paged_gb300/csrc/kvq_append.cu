@@ -21,9 +21,36 @@ namespace kvq {
 namespace {
 
 constexpr int APPEND_THREADS = 256;
+constexpr int APPEND_UNROLL = 4;  // rows per lane group whose loads are issued together
+
+// RNE(fl(x / s)) as an integer, for |x / s| <= 128.  With r = RN(1/s),
+// y = RN(x r) lies within 1.5 * 2^-23 * |x / s| (< 2^-15 here) of fl(x / s),
+// so unless y is within 2^-14 of a half-integer both round to the same
+// integer; near one, the quotient is computed exactly.
+__device__ __forceinline__ int rne_quotient(float x, float s, float r) {
+    const float y = __fmul_rn(x, r);
+    const float c = rintf(y);
+    if (fabsf(__fsub_rn(y, c)) < 0.5f - 0x1p-14f) return (int)c;
+    return __float2int_rn(__fdiv_rn(x, s));
+}
+
+// fl(x / s) where only its E4M3 rounding matters: y = RN(x r) is within 3
+// fp32 ulps of fl(x / s); E4M3 rounding (3 mantissa bits) can only differ
+// if y is within a few ulps of a midpoint between E4M3 values (fp32 mantissa
+// bits 19..0 = 0x80000) or in the E4M3 subnormal range; there the exact
+// quotient is used.
+__device__ __forceinline__ float e4m3_quotient(float x, float s, float r) {
+    const float y = __fmul_rn(x, r);
+    const uint32_t bits = __float_as_uint(y);
+    const int e = (int)((bits >> 23) & 0xFFu);
+    const int low = (int)(bits & 0xFFFFFu);
+    const bool near_mid = abs(low - 0x80000) <= 8;
+    const bool tiny = e < 127 - 6 && y != 0.0f;
+    return (near_mid || tiny) ? __fdiv_rn(x, s) : y;
+}
 
 template <int SCHEME, int D>
-__global__ void __launch_bounds__(APPEND_THREADS) append_kernel(AppendParams p) {
+__global__ void __launch_bounds__(APPEND_THREADS, 4) append_kernel(AppendParams p) {
     constexpr int LPR = D / 8;     // lanes per row
     constexpr int RPW = 32 / LPR;  // rows per warp
     const int lane = threadIdx.x & 31;
@@ -32,115 +59,130 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(AppendParams p) 
     const int64_t rows = (int64_t)p.num_tokens * H * 2;
     const int64_t warp_id = ((int64_t)blockIdx.x * APPEND_THREADS + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * APPEND_THREADS) >> 5;
+    const int64_t stride = nwarps * RPW;
 
-    for (int64_t r0 = warp_id * RPW; r0 < rows; r0 += nwarps * RPW) {
-        const int64_t r = r0 + lane / LPR;
-        const bool in_range = r < rows;
-        const int64_t t = r / (2 * H);
-        const int h = (int)((r >> 1) % H);
-        const int kv = (int)(r & 1);
-        int64_t slot = in_range ? __ldg(p.slot_mapping + t) : -1;
-        if (slot >= p.num_slots) {
-            if (li == 0) flag_error(p.err, ERR_BAD_TABLE);
-            slot = -1;
-        }
-        const bool valid = slot >= 0;
-
-        float x[8];
-        if (valid) {
-            const uint16_t* src = (kv ? p.v : p.k) + (t * H + h) * D + li * 8;
-            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int64_t r0 = warp_id * RPW + lane / LPR; r0 < rows; r0 += stride * APPEND_UNROLL) {
+        // issue every load of APPEND_UNROLL rows before using any of them
+        int64_t slot[APPEND_UNROLL];
+        uint4 raw[APPEND_UNROLL];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                x[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
-                x[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+        for (int u = 0; u < APPEND_UNROLL; ++u) {
+            const int64_t r = r0 + u * stride;
+            slot[u] = -1;
+            raw[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows) {
+                const int64_t t = r / (2 * H);
+                const int h = (int)((r >> 1) % H);
+                const int kv = (int)(r & 1);
+                slot[u] = __ldg(p.slot_mapping + t);
+                raw[u] = __ldg(reinterpret_cast<const uint4*>((kv ? p.v : p.k) + (t * H + h) * D + li * 8));
             }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = 0.0f;
         }
-        // pool row of this (slot, head): [page][head][offset]
-        const int64_t page = valid ? slot / p.page_size : 0;
-        const int64_t prow = (page * H + h) * p.page_size + (valid ? slot % p.page_size : 0);
-
-        if constexpr (SCHEME == KVQ_INT8_SYM_TOKEN || SCHEME == KVQ_FP8E4M3_TOKEN) {
-            float a = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
+        for (int u = 0; u < APPEND_UNROLL; ++u) {
+            const int64_t r = r0 + u * stride;
+            const int h = (int)((r >> 1) % H);
+            const int kv = (int)(r & 1);
+            int64_t sl = r < rows ? slot[u] : -1;
+            if (sl >= p.num_slots) {
+                if (li == 0) flag_error(p.err, ERR_BAD_TABLE);
+                sl = -1;
+            }
+            const bool valid = sl >= 0;
+            float x[8];
+            {
+                const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
-            for (int off = LPR / 2; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-            constexpr float QMAX = SCHEME == KVQ_INT8_SYM_TOKEN ? 127.0f : 448.0f;
-            const bool zero_row = (a == 0.0f);
-            const float scale = zero_row ? 1.0f : __fdiv_rn(a, QMAX);
-            uint32_t lo = 0, hi = 0;
-            if (!zero_row) {
-                if constexpr (SCHEME == KVQ_INT8_SYM_TOKEN) {
-                    uint32_t b[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        int q = __float2int_rn(__fdiv_rn(x[i], scale));
-                        q = max(-127, min(127, q));
-                        b[i] = (uint32_t)(q & 0xFF);
-                    }
-                    lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-                    hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
-                } else {
-                    uint32_t pr[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 y = make_float2(__fdiv_rn(x[2 * i], scale), __fdiv_rn(x[2 * i + 1], scale));
-                        pr[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
-                    }
-                    lo = pr[0] | (pr[1] << 16);
-                    hi = pr[2] | (pr[3] << 16);
+                for (int i = 0; i < 4; ++i) {
+                    x[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
+                    x[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
                 }
             }
-            if (valid) {
-                if (SCHEME == KVQ_INT8_SYM_TOKEN && kv) {
-                    // V codes: 4 consecutive tokens of a channel side by side
-                    // (the row-major offset of a 4-token block is unchanged)
-                    const int64_t off = prow % p.page_size;
-                    uint8_t* dst = p.v_codes + (prow - off) * D + (off / 4) * (4 * D) + (li * 8) * 4 + (off % 4);
+            // pool row of this (slot, head): [page][head][offset]
+            const int64_t page = valid ? sl / p.page_size : 0;
+            const int64_t prow = (page * H + h) * p.page_size + (valid ? sl % p.page_size : 0);
+
+            if constexpr (SCHEME == KVQ_INT8_SYM_TOKEN || SCHEME == KVQ_FP8E4M3_TOKEN) {
+                float a = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) dst[4 * i] = (uint8_t)((i < 4 ? lo : hi) >> (8 * (i & 3)));
-                } else {
-                    uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * D + li * 8;
-                    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+                for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
+#pragma unroll
+                for (int off = LPR / 2; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+                constexpr float QMAX = SCHEME == KVQ_INT8_SYM_TOKEN ? 127.0f : 448.0f;
+                const bool zero_row = (a == 0.0f);
+                const float scale = zero_row ? 1.0f : __fdiv_rn(a, QMAX);
+                const float rcp = __frcp_rn(scale);
+                uint32_t lo = 0, hi = 0;
+                if (!zero_row) {
+                    if constexpr (SCHEME == KVQ_INT8_SYM_TOKEN) {
+                        uint32_t b[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            int q = rne_quotient(x[i], scale, rcp);
+                            q = max(-127, min(127, q));
+                            b[i] = (uint32_t)(q & 0xFF);
+                        }
+                        lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+                        hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+                    } else {
+                        uint32_t pr[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 y = make_float2(e4m3_quotient(x[2 * i], scale, rcp),
+                                                         e4m3_quotient(x[2 * i + 1], scale, rcp));
+                            pr[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+                        }
+                        lo = pr[0] | (pr[1] << 16);
+                        hi = pr[2] | (pr[3] << 16);
+                    }
                 }
-                if (li == 0) static_cast<float*>(kv ? p.v_scales : p.k_scales)[prow] = scale;
-            }
-        } else {  // INT4 asymmetric, groups of 32 channels = 4 lanes
-            float mn = x[0], mx = x[0];
+                if (valid) {
+                    if (SCHEME == KVQ_INT8_SYM_TOKEN && kv) {
+                        // V codes: 4 consecutive tokens of a channel side by side
+                        // (the row-major offset of a 4-token block is unchanged)
+                        const int64_t off = prow % p.page_size;
+                        uint8_t* dst = p.v_codes + (prow - off) * D + (off / 4) * (4 * D) + (li * 8) * 4 + (off % 4);
 #pragma unroll
-            for (int i = 1; i < 8; ++i) {
-                mn = fminf(mn, x[i]);
-                mx = fmaxf(mx, x[i]);
-            }
+                        for (int i = 0; i < 8; ++i) dst[4 * i] = (uint8_t)((i < 4 ? lo : hi) >> (8 * (i & 3)));
+                    } else {
+                        uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * D + li * 8;
+                        *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+                    }
+                    if (li == 0) static_cast<float*>(kv ? p.v_scales : p.k_scales)[prow] = scale;
+                }
+            } else {  // INT4 asymmetric, groups of 32 channels = 4 lanes
+                float mn = x[0], mx = x[0];
 #pragma unroll
-            for (int off = 2; off >= 1; off >>= 1) {
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            }
-            const __half zh = __float2half_rd(mn);
-            const float zf = __half2float(zh);
-            __half sh = __float2half_ru(__fdiv_rn(__fsub_rn(mx, zf), 15.0f));
-            if (__half2float(sh) == 0.0f) sh = __float2half(1.0f);
-            const float sf = __half2float(sh);
-            uint32_t packed = 0;
+                for (int i = 1; i < 8; ++i) {
+                    mn = fminf(mn, x[i]);
+                    mx = fmaxf(mx, x[i]);
+                }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                int q = __float2int_rn(__fdiv_rn(__fsub_rn(x[i], zf), sf));
-                q = max(0, min(15, q));
-                packed |= (uint32_t)q << (4 * i);
-            }
-            if (valid) {
-                uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * (D / 2) + li * 4;
-                *reinterpret_cast<uint32_t*>(dst) = packed;
-                if ((li & 3) == 0) {
-                    const int64_t gi = prow * (D / 32) + li / 4;
-                    static_cast<__half*>(kv ? p.v_scales : p.k_scales)[gi] = sh;
-                    static_cast<__half*>(kv ? p.v_zeros : p.k_zeros)[gi] = zh;
+                for (int off = 2; off >= 1; off >>= 1) {
+                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                }
+                const __half zh = __float2half_rd(mn);
+                const float zf = __half2float(zh);
+                __half sh = __float2half_ru(__fdiv_rn(__fsub_rn(mx, zf), 15.0f));
+                if (__half2float(sh) == 0.0f) sh = __float2half(1.0f);
+                const float sf = __half2float(sh);
+                const float rcp = __frcp_rn(sf);
+                uint32_t packed = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    int q = rne_quotient(__fsub_rn(x[i], zf), sf, rcp);
+                    q = max(0, min(15, q));
+                    packed |= (uint32_t)q << (4 * i);
+                }
+                if (valid) {
+                    uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * (D / 2) + li * 4;
+                    *reinterpret_cast<uint32_t*>(dst) = packed;
+                    if ((li & 3) == 0) {
+                        const int64_t gi = prow * (D / 32) + li / 4;
+                        static_cast<__half*>(kv ? p.v_scales : p.k_scales)[gi] = sh;
+                        static_cast<__half*>(kv ? p.v_zeros : p.k_zeros)[gi] = zh;
+                    }
                 }
             }
         }
@@ -171,10 +213,13 @@ __global__ void validate_kernel(int num_pages, int page_size, const int32_t* blo
 
 template <int SCHEME, int D>
 cudaError_t launch_append_t(const AppendParams& p, cudaStream_t s) {
+    // as many CTAs as there are row groups (small appends are latency-bound),
+    // at most one wave of 4 resident CTAs per SM (then each lane group loops,
+    // APPEND_UNROLL rows at a time)
     constexpr int RPB = (APPEND_THREADS / 32) * (32 / (D / 8));
     const int64_t rows = (int64_t)p.num_tokens * p.num_kv_heads * 2;
     int64_t blocks = (rows + RPB - 1) / RPB;
-    const int64_t cap = (int64_t)device_sm_count() * 16;
+    const int64_t cap = (int64_t)device_sm_count() * 4;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     append_kernel<SCHEME, D><<<(unsigned)blocks, APPEND_THREADS, 0, s>>>(p);
