@@ -77,9 +77,15 @@ struct DecodeCfg {
     static constexpr int QO = VZ + (INT4 ? UNIT * MB : 0);
     static constexpr int STAGE = QO + Q_BYTES;
     static constexpr int STAGES = (STAGE >= 4096) ? 3 : 4;  // ring depth per warp: STAGES-1 units in flight
-    // scores: KL lanes per token, CPL channels per lane, TPP tokens per pass
-    static constexpr int CPL = (D == 64 && G == 8) ? 8 : 16;
-    static constexpr int KL = D / CPL;
+    // scores: KL lanes per token, CPL channels per lane, TPP tokens per pass.
+    // INT8: each lane takes ONE query head (DUP = KL / G lanes per head) and
+    // D / DUP of its channels, so its dot product needs no transpose across
+    // heads, only a sum over the DUP lanes.  FP8 / INT4: each lane takes 16
+    // (or 8) channels of all G heads and a transpose-reduction sorts them out.
+    static constexpr bool SHEAD = INT8;
+    static constexpr int CPL = SHEAD ? D * G / 8 : ((D == 64 && G == 8) ? 8 : 16);
+    static constexpr int KL = SHEAD ? 8 : D / CPL;
+    static constexpr int QROWS = SHEAD ? 1 : G;  // query rows held per lane
     static constexpr int TPP = 32 / KL;
     static constexpr int PASSES = UNIT / TPP;
     static constexpr int DUP = KL / G;  // lanes that end holding the same (token, head) score
@@ -651,7 +657,7 @@ decode_partial_kernel(const DecodeParams p) {
     float* AL = WQ + G;                                            // [G]
     // score-lane coordinates
     const int k_tok = lane / C::KL;
-    const int k_c0 = (lane % C::KL) * C::CPL;
+    const int k_c0 = (C::SHEAD ? (lane % C::KL) % C::DUP : lane % C::KL) * C::CPL;
     const int k_head = (lane % C::KL) / C::DUP;
     const bool k_writer = (lane % C::DUP) == 0;
     // value-lane coordinates
@@ -669,7 +675,7 @@ decode_partial_kernel(const DecodeParams p) {
         int ua, ub;
         ua = pc.u_lo;
         ub = pc.u_hi;
-        uint32_t qw[G][C::QW];  // query: INT8/INT4 fixed-point bytes, FP8 fp16 pairs
+        uint32_t qw[C::QROWS][C::QW];  // query: INT8/INT4 fixed-point bytes, FP8 fp16 pairs
         float sq[G];            // INT4: fixed-point step per head
         float qisum[G];         // INT4: sum of this lane's fixed-point query channels, per head
         float my_sq = 0.0f;     // INT8: fixed-point step of this lane's head times the softmax scale
@@ -692,11 +698,51 @@ decode_partial_kernel(const DecodeParams p) {
             const int st = cst;
             cst = (cst + 1 == STAGES_) ? 0 : cst + 1;
             const uint8_t* stg = ring + st * C::STAGE;
-            if (u == ua) {
+            if (u == ua && C::SHEAD) {
+                // ---- this lane's head of the query -> 16-bit fixed point bytes:
+                // q ~ sq * qi, qi = 256 hi + lo (hi a signed byte, lo an unsigned
+                // byte; error <= sq / 2 per element), sq from the head's max |q|
+                const uint16_t* qrow = reinterpret_cast<const uint16_t*>(stg + C::QO) + k_head * D + k_c0;
+                float amax = 0.0f;
+#pragma unroll
+                for (int j = 0; j < C::CPL; j += 8) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(qrow + j);
+                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w4[i] & 0xFFFFu)),
+                                                 fabsf(bf16_bits_to_float(w4[i] >> 16))));
+                }
+#pragma unroll
+                for (int off = C::DUP / 2; off >= 1; off >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                const float inv = amax > 0.0f ? 32767.0f / amax : 0.0f;
+                my_sq = (amax / 32767.0f) * qk_scale;
+                constexpr int NQW = C::CPL / 4;
+#pragma unroll
+                for (int j = 0; j < C::CPL; j += 8) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(qrow + j);
+                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                    int qi[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        qi[2 * i] = __float2int_rn(bf16_bits_to_float(w4[i] & 0xFFFFu) * inv);
+                        qi[2 * i + 1] = __float2int_rn(bf16_bits_to_float(w4[i] >> 16) * inv);
+                    }
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int* v = qi + 4 * h2;
+                        qw[0][j / 4 + h2] = ((uint32_t)(v[0] >> 8) & 0xFF) | (((uint32_t)(v[1] >> 8) & 0xFF) << 8) |
+                                            (((uint32_t)(v[2] >> 8) & 0xFF) << 16) | (((uint32_t)(v[3] >> 8) & 0xFF) << 24);
+                        qw[0][NQW + j / 4 + h2] = ((uint32_t)v[0] & 0xFF) | (((uint32_t)v[1] & 0xFF) << 8) |
+                                                  (((uint32_t)v[2] & 0xFF) << 16) | (((uint32_t)v[3] & 0xFF) << 24);
+                    }
+                }
+            } else if (u == ua) {
                 // ---- query rows of this piece -> fp16 pairs in registers
                 const uint16_t* qb = reinterpret_cast<const uint16_t*>(stg + C::QO);
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < C::QROWS; ++g) {
                     float qf[C::CPL];
 #pragma unroll
                     for (int j = 0; j < C::CPL; j += 8) {
@@ -708,7 +754,7 @@ decode_partial_kernel(const DecodeParams p) {
                             qf[j + 2 * i + 1] = bf16_bits_to_float(w4[i] >> 16);
                         }
                     }
-                    if constexpr (C::INT8 || C::INT4) {
+                    if constexpr (C::INT4) {
                         // 16-bit fixed point per (query head): q ~ sq * qi, qi = 256 hi + lo,
                         // hi a signed byte, lo an unsigned byte (error <= sq / 2 per element)
                         float amax = 0.0f;
@@ -728,15 +774,7 @@ decode_partial_kernel(const DecodeParams p) {
                         }
                         auto hb = [&](int j) { return (uint32_t)((qi[j] >> 8) & 0xFF); };
                         auto lb = [&](int j) { return (uint32_t)(qi[j] & 0xFF); };
-                        if constexpr (C::INT8) {  // consecutive channels, hi words then lo words
-                            constexpr int NQW = C::CPL / 4;
-#pragma unroll
-                            for (int i = 0; i < NQW; ++i) {
-                                qw[g][i] = hb(4 * i) | (hb(4 * i + 1) << 8) | (hb(4 * i + 2) << 16) | (hb(4 * i + 3) << 24);
-                                qw[g][NQW + i] = lb(4 * i) | (lb(4 * i + 1) << 8) | (lb(4 * i + 2) << 16) | (lb(4 * i + 3) << 24);
-                            }
-                            if (g == k_head) my_sq = sqg * qk_scale;
-                        } else {  // per 8-channel word: even-channel and odd-channel bytes
+                        {  // per 8-channel word: even-channel and odd-channel bytes
 #pragma unroll
                             for (int i = 0; i < C::CPL / 8; ++i) {
                                 const int b0 = 8 * i;
@@ -769,29 +807,40 @@ decode_partial_kernel(const DecodeParams p) {
                     const int t = pass * C::TPP + k_tok;
                     float s;
                     if constexpr (C::INT8) {
+                        // this lane's head over its CPL channels of token t, in
+                        // NA independent dp4a chains (high and low query bytes)
                         const int8_t* src8 = reinterpret_cast<const int8_t*>(stg + C::KC + t * D + k_c0);
-                        int wv[C::CPL / 4];
-                        if constexpr (C::CPL == 16) {
-                            const int4 r = *reinterpret_cast<const int4*>(src8);
-                            wv[0] = r.x; wv[1] = r.y; wv[2] = r.z; wv[3] = r.w;
-                        } else {
-                            const int2 r = *reinterpret_cast<const int2*>(src8);
-                            wv[0] = r.x; wv[1] = r.y;
-                        }
                         constexpr int NQW = C::CPL / 4;
-                        int ai[G];
+                        constexpr int NA = NQW < 4 ? NQW : 4;
+                        int ah[NA], al[NA];
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            int ah = 0, al = 0;
+                        for (int j = 0; j < NA; ++j) ah[j] = al[j] = 0;
 #pragma unroll
-                            for (int i = 0; i < NQW; ++i) {
-                                ah = dp4a_ss((int)qw[g][i], wv[i], ah);
-                                al = dp4a_us(qw[g][NQW + i], wv[i], al);
+                        for (int i = 0; i < NQW; i += NA) {
+                            int wv[NA];
+                            if constexpr (NA == 4) {
+                                const int4 r = *reinterpret_cast<const int4*>(src8 + 4 * i);
+                                wv[0] = r.x; wv[1] = r.y; wv[2] = r.z; wv[3] = r.w;
+                            } else {
+                                const int2 r = *reinterpret_cast<const int2*>(src8 + 4 * i);
+                                wv[0] = r.x; wv[1] = r.y;
                             }
-                            ai[g] = ah * 256 + al;  // exact: |sum| < 2^30
+#pragma unroll
+                            for (int j = 0; j < NA; ++j) {
+                                ah[j] = dp4a_ss((int)qw[0][i + j], wv[j], ah[j]);
+                                al[j] = dp4a_us(qw[0][NQW + i + j], wv[j], al[j]);
+                            }
                         }
-                        transpose_reduce<int, G, C::KL / 2>(ai, lane);
-                        s = (float)ai[0] * (my_sq * reinterpret_cast<const float*>(stg + C::KS)[t]);
+                        int hs = 0, ls = 0;
+#pragma unroll
+                        for (int j = 0; j < NA; ++j) {
+                            hs += ah[j];
+                            ls += al[j];
+                        }
+                        int ai = hs * 256 + ls;  // exact: |sum| < 2^30
+#pragma unroll
+                        for (int off = C::DUP / 2; off >= 1; off >>= 1) ai += __shfl_xor_sync(0xffffffffu, ai, off);
+                        s = (float)ai * (my_sq * reinterpret_cast<const float*>(stg + C::KS)[t]);
                     } else if constexpr (C::INT4) {
                         const uint8_t* src = stg + C::KC + t * (D / 2) + k_c0 / 2;
                         uint32_t wv[C::CPL / 8];
