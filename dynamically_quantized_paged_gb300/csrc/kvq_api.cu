@@ -227,6 +227,10 @@ kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_
     if (st != KVQ_OK) return st;
     if (scheme != cache->scheme) return KVQ_ERR_SCHEME_MISMATCH;
     if (num_tokens < 0) return KVQ_ERR_INVALID_ARG;
+    // slots and rows are indexed in 32 bits on the device
+    if ((int64_t)cache->num_pages * cache->page_size >= ((int64_t)1 << 31) ||
+        (int64_t)num_tokens * cache->num_kv_heads * 2 >= ((int64_t)1 << 31))
+        return KVQ_ERR_INVALID_ARG;
     if (block_table && (num_seqs < 0 || max_pages_per_seq < 1 || !aligned(block_table, 4)))
         return KVQ_ERR_INVALID_ARG;
     if (num_tokens > 0) {

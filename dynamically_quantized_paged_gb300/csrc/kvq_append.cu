@@ -71,8 +71,9 @@ __global__ void __launch_bounds__(APPEND_THREADS, 4) append_kernel(AppendParams 
             slot[u] = -1;
             raw[u] = make_uint4(0u, 0u, 0u, 0u);
             if (r < rows) {
-                const int64_t t = r / (2 * H);
-                const int h = (int)((r >> 1) % H);
+                const uint32_t th = (uint32_t)r >> 1;  // token * H + head
+                const int64_t t = th / (uint32_t)H;
+                const int h = (int)(th - (uint32_t)t * (uint32_t)H);
                 const int kv = (int)(r & 1);
                 slot[u] = __ldg(p.slot_mapping + t);
                 raw[u] = __ldg(reinterpret_cast<const uint4*>((kv ? p.v : p.k) + (t * H + h) * D + li * 8));
@@ -81,7 +82,8 @@ __global__ void __launch_bounds__(APPEND_THREADS, 4) append_kernel(AppendParams 
 #pragma unroll
         for (int u = 0; u < APPEND_UNROLL; ++u) {
             const int64_t r = r0 + u * stride;
-            const int h = (int)((r >> 1) % H);
+            const uint32_t th = (uint32_t)r >> 1;
+            const int h = (int)(th % (uint32_t)H);
             const int kv = (int)(r & 1);
             int64_t sl = r < rows ? slot[u] : -1;
             if (sl >= p.num_slots) {
@@ -99,8 +101,9 @@ __global__ void __launch_bounds__(APPEND_THREADS, 4) append_kernel(AppendParams 
                 }
             }
             // pool row of this (slot, head): [page][head][offset]
-            const int64_t page = valid ? sl / p.page_size : 0;
-            const int64_t prow = (page * H + h) * p.page_size + (valid ? sl % p.page_size : 0);
+            const uint32_t pg = valid ? (uint32_t)sl / (uint32_t)p.page_size : 0u;
+            const uint32_t off = valid ? (uint32_t)sl - pg * (uint32_t)p.page_size : 0u;
+            const int64_t prow = ((int64_t)pg * H + h) * p.page_size + off;
 
             if constexpr (SCHEME == KVQ_INT8_SYM_TOKEN || SCHEME == KVQ_FP8E4M3_TOKEN) {
                 float a = 0.0f;
@@ -140,7 +143,6 @@ __global__ void __launch_bounds__(APPEND_THREADS, 4) append_kernel(AppendParams 
                     if (SCHEME == KVQ_INT8_SYM_TOKEN && kv) {
                         // V codes: 4 consecutive tokens of a channel side by side
                         // (the row-major offset of a 4-token block is unchanged)
-                        const int64_t off = prow % p.page_size;
                         uint8_t* dst = p.v_codes + (prow - off) * D + (off / 4) * (4 * D) + (li * 8) * 4 + (off % 4);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) dst[4 * i] = (uint8_t)((i < 4 ? lo : hi) >> (8 * (i & 3)));

@@ -132,6 +132,8 @@ kvq_status kvq_cache_bytes(int32_t scheme, int32_t num_pages, int32_t page_size,
  *                 of the pool) and violations flagged KVQ_ERR_BAD_TABLE; the
  *                 codes are written through slot_mapping either way.
  *   scheme        must equal cache->scheme (else KVQ_ERR_SCHEME_MISMATCH).
+ *   num_pages * page_size and num_tokens * num_kv_heads * 2 must be below
+ *   2^31 (else KVQ_ERR_INVALID_ARG): slots and rows are indexed in 32 bits.
  * Writes, for every token and KV head, the codes and scale (and INT4 zero)
  * at the slot.  num_tokens == 0 launches nothing. */
 kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_t num_seqs,
