@@ -88,10 +88,10 @@ def test_allocator_rejects_bad_frees():
     a.close()
 
 
-def fake_cache(scheme=1, head_dim=128, page_size=16, heads=8, align=256, group=32):
+def fake_cache(scheme=1, head_dim=128, page_size=16, heads=8, align=256, group=32, num_pages=4):
     base = 1 << 20  # never dereferenced: argument checks run before any device access
     p = lambda i: base + i * (1 << 16) + (0 if align >= 16 else align)
-    return kvq.CacheStruct(scheme, 4, page_size, heads, head_dim, group if scheme == 3 else 0,
+    return kvq.CacheStruct(scheme, num_pages, page_size, heads, head_dim, group if scheme == 3 else 0,
                            p(0), p(1), p(2), p(3), p(4) if scheme == 3 else None,
                            p(5) if scheme == 3 else None)
 
@@ -114,6 +114,8 @@ def test_append_argument_errors_before_any_launch():
     c = fake_cache(scheme=3)
     c.k_zeros = None
     assert call_append(c) == 1                                 # INT4 needs zero pools
+    assert call_append(fake_cache(num_pages=1 << 27)) == 1     # 2^31 slots: beyond 32-bit indexing
+    assert call_append(fake_cache(), T=1 << 27) == 1           # 2^31 rows (2^27 tokens x 8 heads x K,V)
 
 
 def call_decode(c, B=2, Hq=32, maxp=4, ws_bytes=1 << 30, q=1 << 24):
