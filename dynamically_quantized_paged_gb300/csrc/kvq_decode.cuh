@@ -11,43 +11,48 @@
 //
 // Decomposition (GB300 design).  The work of one call is the sequence of
 // 16-token units of every (sequence, KV head) "segment", laid end to end in
-// (b, h, unit) order.  A persistent grid of n_ctas CTAs cuts that line into
-// equal slices of S units; a CTA walks the segment pieces of its slice.  A
-// piece that is a whole segment yields the final output row directly; a
-// segment cut by slice boundaries leaves one partial (running max m, sum l,
-// unnormalized o) per CTA that touches it, at most two per CTA.  In the
-// one-launch form the CTA that delivers a segment's last partial (counted in
-// a generation-tagged workspace word) merges them; in the two-launch form the
-// merge kernel does.  Slices are a function of logical positions only, so
-// physical page placement cannot change the result.
+// (b, h, unit) order.  A persistent grid of n_ctas CTAs (one per SM, WARPS
+// warps each) cuts that line into equal slices: every warp is a worker with
+// its own slice of Sw units, and a CTA's slice (S = WARPS * Sw units) is its
+// warps' slices end to end.  A segment that lies inside one warp's slice is
+// finished by that warp (final output rows).  Any other piece of a warp's
+// slice leaves a warp partial (running max m, sum l, unnormalized o) in one
+// of the warp's two slots.  At the end the CTA combines, element-parallel,
+// the warp partials of every piece that spans several of its warps: a
+// segment that ends inside the CTA's slice gets its final rows, one that
+// continues in another CTA gets the CTA's partial (at most two per CTA).  In
+// the one-launch form the CTA that delivers a segment's last CTA partial
+// (counted in a generation-tagged workspace word) merges them; in the
+// two-launch form the merge kernel does.  Slices are a function of logical
+// positions only, so physical page placement cannot change the result.
 //
-// Inside a CTA (4 warps, no producer warp): every warp streams its own
-// contiguous share of each piece's units through a ring of shared-memory
-// stages with 16-byte cp.async gathers (all 32 lanes issue; page ids come from
-// the block table in 32-entry register batches, the next batch prefetched),
-// keeping STAGES-1 units in flight, and consumes them:
-//  * scores: each lane holds 16 (or 8) channels of the G query rows.  For
-//    INT8 and INT4 the query is held as 16-bit fixed point per head (a signed
-//    high byte and an unsigned low byte) and the partial dots are exact int32
-//    dp4a sums against the codes; for FP8 the query is fp16 and the codes are
-//    converted to fp16 for mixed-precision FMAs.  A transpose-reduction
-//    across the lanes sharing a token leaves one score per lane, and the
-//    per-token (and per-head) scales are applied once;
+// Inside a warp (no producer warp): the warp streams its units through its
+// own ring of STAGES shared-memory stages with 16-byte cp.async gathers (all
+// 32 lanes issue; page ids come from the block table in 32-entry register
+// batches, the next batch prefetched), keeping STAGES-1 units in flight, and
+// consumes them:
+//  * scores.  INT8: each lane takes ONE query head and D*G/8 of its
+//    channels, the query held as 16-bit fixed point (a signed high byte and
+//    an unsigned low byte); exact int32 dp4a sums against the codes, summed
+//    over the lanes that share the head.  FP8, INT4: each lane holds 16 (or
+//    8) channels of all G query rows (INT4 as fixed point with dp4a, FP8 as
+//    fp16 with mixed-precision FMAs against exactly converted codes) and a
+//    transpose-reduction across the lanes sharing a token leaves one score
+//    per lane.  The per-token (and per-head) scales are applied once;
 //  * online softmax in base 2 directly on those lanes (max over the unit by
-//    two shuffles); the weights p * value scale go to shared memory;
+//    shuffles); the weights p * value scale go to shared memory;
 //  * values: each lane owns 4 (or 8) channels x G heads of fp32 accumulators.
 //    INT8: the unit's weights of each head become 16-bit fixed point
 //    relative to their maximum; the V codes are stored with 4 consecutive
 //    tokens of a channel in one word, so one 16-byte load gives a lane its 4
 //    channels of a 4-token block; dp4a accumulates the unit in int32 (high
 //    byte, times 256, then low byte), and one FMA per accumulator adds the
-//    unit.  FP8, INT4: scalar FMAs on exactly
-//    converted codes (INT4 adds the zero-points once per token).
+//    unit.  FP8, INT4: scalar FMAs on exactly converted codes (INT4 adds the
+//    zero-points once per token).
 // The query rows of a piece travel in the stage of the warp's first unit of
-// that piece.  At the end of a piece the four warps' states are combined in
-// shared memory.  One 1-D bulk copy per issuing thread completes only every
-// few hundred ns on this GPU, so per-lane cp.async gathers, issued by every
-// warp, are what keeps enough bytes in flight.
+// that piece.  One 1-D bulk copy per issuing thread completes only every few
+// hundred ns on this GPU, so per-lane cp.async gathers, issued by every warp,
+// are what keeps enough bytes in flight.
 #pragma once
 
 #include "kvq_device.cuh"
@@ -119,7 +124,8 @@ struct DecodeCfg {
 // ---- the split plan ------------------------------------------------------------
 // units_b = ceil(min(seq_len_b, max_pages * page_size) / UNIT); segments
 // (b, h) laid out in (b, h) order; prefix[b] = sum of units_b' for b' < b;
-// U = Hkv * prefix[B]; slice S = max(ceil(U / n_ctas), MIN_SLICE_UNITS).
+// U = Hkv * prefix[B]; warp slice Sw = max(ceil(U / (n_ctas * WARPS)),
+// MIN_SLICE_UNITS); CTA slice S = WARPS * Sw.
 struct Plan {
     int B, Hkv;
     int64_t U;
@@ -479,7 +485,10 @@ __device__ __forceinline__ void merge_element(const float* so, const float* sm, 
 // and contention stays low even when dozens of CTAs arrive together.  No CTA
 // waits on another.  The generation is odd, so a cleared word is stale.  One
 // thread calls this, after the CTA's partial is written and fenced.  Kept out
-// of line: it is off the main loop's path.
+// of line: it is off the main loop's path.  Each failed compare-and-swap means
+// another arrival changed the word, so the retries are bounded by the
+// arrivals; a hard cap on them (flagged as a timeout, nothing merged) guards
+// against a word that something outside this call keeps rewriting.
 static __device__ __noinline__ bool count_arrival(const DecodeParams& p, int b, int h, unsigned long long n) {
     unsigned long long* ctr = p.seg_ctr + (int64_t)b * p.c.num_kv_heads + h;
     const unsigned long long tag = (unsigned long long)p.gen << 32;
@@ -490,7 +499,11 @@ static __device__ __noinline__ bool count_arrival(const DecodeParams& p, int b, 
         count = (old & LO) + 1;
     } else {
         unsigned long long expect = old + 1;  // the word just after this add, if untouched
-        while (true) {
+        for (int tries = 0;; ++tries) {
+            if (tries == (1 << 20)) {
+                flag_error(p.err, ERR_TIMEOUT);
+                return false;
+            }
             const unsigned long long seen = atomicCAS(ctr, expect, tag | 1ull);
             if (seen == expect) {  // installed this call's generation, counted as the first
                 count = 1;

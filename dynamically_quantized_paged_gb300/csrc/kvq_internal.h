@@ -21,7 +21,7 @@ constexpr int MERGE_THREADS = 128;
 // Warps of a decode CTA (one CTA per SM) for GQA ratio G.
 constexpr int decode_warps(int G) { return G >= 8 ? 8 : 12; }
 constexpr int MAX_SEQS = 4096;     // per decode call (the plan lives in shared memory)
-constexpr int MIN_SLICE_UNITS = 8; // smallest per-CTA share of the work, in units
+constexpr int MIN_SLICE_UNITS = 8; // smallest per-warp share of the work, in units
 
 struct CacheView {
     int scheme, num_pages, page_size, num_kv_heads, head_dim, group;
