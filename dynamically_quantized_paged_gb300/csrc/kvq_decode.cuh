@@ -112,8 +112,7 @@ struct DecodeCfg {
     // WB[UNIT/4][hi, lo][G][4 tokens]), then the weights' fixed-point step
     // WQ[G] (dp4a path), then alpha[G]
     static constexpr int W_BYTES = (UNIT * G * 4 + 2 * G * 4 + 15) / 16 * 16;
-    static constexpr int OFF_EPS = OFF_W + WARPS * W_BYTES;  // the end-phase piece list (WARPS + 1 entries)
-    static constexpr int OFF_MISC = OFF_EPS + (WARPS + 1) * 48;
+    static constexpr int OFF_MISC = OFF_W + WARPS * W_BYTES;
     static constexpr int OFF_PLAN = OFF_MISC + 16;
     static size_t smem_bytes(int B) { return OFF_PLAN + (size_t)(B + 1) * 4; }
     static_assert(G <= KL, "each lane must end the reduction holding one head");
@@ -121,13 +120,6 @@ struct DecodeCfg {
     static_assert(OFF_W % 16 == 0, "alignment");
     static_assert(4 * (UNIT * MB / 16) <= 32, "one lane per 16 bytes of scales and zeros");
 };
-
-// x / d for 0 <= x, 0 < d: one 32-bit division when both fit in 32 bits
-// (always, short of ~2^32 units of work in one call), else the 64-bit one.
-__device__ __forceinline__ int64_t div_pos(int64_t x, int64_t d) {
-    if ((((uint64_t)x | (uint64_t)d) >> 32) == 0) return (int64_t)((uint32_t)x / (uint32_t)d);
-    return x / d;
-}
 
 // ---- the split plan ------------------------------------------------------------
 // units_b = ceil(min(seq_len_b, max_pages * page_size) / UNIT); segments
@@ -206,7 +198,7 @@ __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefi
     pl.Hkv = p.c.num_kv_heads;
     pl.U = (int64_t)pl.Hkv * misc[0];
     const int64_t workers = (int64_t)p.n_ctas * NW;
-    const int64_t Sw = div_pos(pl.U + workers - 1, workers);
+    const int64_t Sw = (pl.U + workers - 1) / workers;
     pl.Sw = Sw < MIN_SLICE_UNITS ? MIN_SLICE_UNITS : Sw;
     pl.S = pl.Sw * NW;
     return pl;
@@ -252,7 +244,7 @@ struct PieceWalk {
                 else lo = mid + 1;
             }
             b = lo;
-            h = (int)div_pos(x - (int64_t)Hkv * prefix[b], units(b));
+            h = (int)((x - (int64_t)Hkv * prefix[b]) / units(b));
         }
     }
     __device__ bool done() const { return x >= end; }
@@ -331,7 +323,7 @@ __device__ __forceinline__ void merge_workers(const float* so, const float* sm, 
     constexpr int UNR = 8;                           // partials per round
     static_assert(UNR <= LPH, "one lane per partial of a round");
     const int n = (int)(k1 - k0 + 1);
-    const int64_t k_start = div_pos(a, S);  // the worker whose slice holds the segment's first unit
+    const int64_t k_start = a / S;  // the worker whose slice holds the segment's first unit
     const bool start_odd = a != k_start * S;
     const int lane = tid & 31, base = lane / LPH * LPH, sub = lane % LPH;
     auto slot_of = [&](int i) -> int64_t {
@@ -407,34 +399,30 @@ __device__ __forceinline__ void merge_workers(const float* so, const float* sm, 
     }
 }
 
-// A piece of a CTA's slice whose result needs the partials of several warps,
-// with the worker ranges of both merge levels worked out once.
+// A piece of a CTA's slice whose result needs the partials of several warps.
 struct EndPiece {
-    int k0;        // first warp worker touching the piece
-    int n;         // warp workers touching it
-    int kw_start;  // warp worker whose slice holds the segment's first unit
-    int kc0;       // first CTA touching the segment (its slice holds the first unit)
-    int nc;        // CTAs touching it
+    int64_t a;      // work-line unit where the segment starts
+    int64_t units;  // units of the segment
+    int64_t k0;     // first warp worker touching the piece
+    int n;          // warp workers touching it
     int b, h;
-    int slot;      // CTA partial slot, or -1: the segment ends here (final rows)
-    int odd_w;     // the segment starts inside kw_start's slice, not at its start
-    int odd_c;     // the same for CTA kc0's slice
-    int pad[2];
+    int slot;       // CTA partial slot, or -1: the segment ends here (final rows)
 };
 
 // One float4 element (head g, channels j..j+3) of the online log-sum-exp merge
-// of the partials workers k0..k0+n-1 left for a segment whose first unit is
-// in worker k_start's slice, at its start unless start_odd (slot rule as in
-// merge_workers).  Called by all 32
+// of the partials workers k0..k0+n-1 left for the segment starting at unit
+// a (slices of S units; slot rule as in merge_workers).  Called by all 32
 // lanes of a warp together (active = this lane has an element); the lanes
 // that share a head share their (m, l) loads by shuffle.  Writes O / L to
 // row, or (O, M, L) to the destination partial.
 template <int D, int G>
-__device__ __forceinline__ void merge_element(const float* so, const float* sm, const float* sl, int k_start,
-                                              bool start_odd, int64_t k0, int n, int g, int j, int lane,
-                                              bool active, float* row, float* dst_o, float* dst_m, float* dst_l) {
+__device__ __forceinline__ void merge_element(const float* so, const float* sm, const float* sl, int64_t a,
+                                              int64_t S, int64_t k0, int n, int g, int j, int lane, bool active,
+                                              float* row, float* dst_o, float* dst_m, float* dst_l) {
     constexpr int LPH = D / 4 < 32 ? D / 4 : 32;
     constexpr int UNR = 8;
+    const int64_t k_start = a / S;
+    const bool start_odd = a != k_start * S;
     const int base = lane / LPH * LPH, sub = lane % LPH;
     auto slot_of = [&](int i) -> int64_t {
         const int64_t k = k0 + i;
@@ -692,43 +680,6 @@ decode_partial_kernel(const DecodeParams p) {
 
 #pragma unroll 1
     for (int i = 0; i < STAGES_ - 1; ++i) issue_one();  // prologue
-
-    // The CTA's pieces that span more than one warp's slice, or that continue
-    // in another CTA (at most one per warp boundary plus the two ends): listed
-    // by one thread while its first units are in flight, combined at the end.
-    EndPiece* eps = reinterpret_cast<EndPiece*>(smem + C::OFF_EPS);
-    static_assert(sizeof(EndPiece) == 48, "list entry size");
-    if (tid == 0) {
-        int np = 0;
-        PieceWalk cw;
-        cw.begin(plan, prefix, blockIdx.x, plan.S);
-        const int64_t cta_lo = (int64_t)blockIdx.x * plan.S;
-        const int w_lo = blockIdx.x * C::WARPS;
-        for (; !cw.done(); cw.next()) {
-            const int units = cw.units(cw.b);
-            const int64_t a = cw.seg_start(cw.b, cw.h);
-            const int64_t x0 = cw.x, x1 = (a + units < cw.end ? a + units : cw.end);  // piece [x0, x1)
-            const int k0 = w_lo + (int)div_pos(x0 - cta_lo, plan.Sw);
-            const int k1 = w_lo + (int)div_pos(x1 - 1 - cta_lo, plan.Sw);
-            const bool whole = x0 == a && x1 == a + units;
-            if (whole && k0 == k1) continue;  // inside one warp's slice: already final
-            EndPiece& e = eps[np];
-            e.k0 = k0;
-            e.n = k1 - k0 + 1;
-            const int64_t kw = div_pos(a, plan.Sw);
-            e.kw_start = (int)kw;
-            e.odd_w = a != kw * plan.Sw;
-            const int64_t kc = div_pos(a, plan.S);
-            e.kc0 = (int)kc;
-            e.odd_c = a != kc * plan.S;
-            e.nc = (int)(div_pos(a + units - 1, plan.S) - kc + 1);
-            e.b = cw.b;
-            e.h = cw.h;
-            e.slot = whole ? -1 : (int)(2 * (int64_t)blockIdx.x + (cw.idx == 0 ? 0 : 1));
-            ++np;
-        }
-        reinterpret_cast<int*>(misc)[2] = np;
-    }
     int cst = 0;  // stage the next computed unit sits in
     PieceWalk walk;
     walk.begin(plan, prefix, worker, plan.Sw);
@@ -1221,18 +1172,44 @@ decode_partial_kernel(const DecodeParams p) {
         }
     }
 
-    // ---- the listed pieces: combine the partials the warps left, all such
-    // pieces at once
+    // ---- the CTA's pieces that span more than one warp's slice, or that
+    // continue in another CTA: combine the partials its warps left, all such
+    // pieces at once (at most one per warp boundary plus the two ends)
     cp_async_wait<0>();
-    __syncthreads();  // all warps' rows and partials are written; the list is complete
-    const int np = reinterpret_cast<const int*>(misc)[2];
+    __syncthreads();  // all warps' rows and partials are written; the rings are idle
+    EndPiece* eps = reinterpret_cast<EndPiece*>(smem + C::OFF_STAGES);
+    static_assert((C::WARPS + 1) * sizeof(EndPiece) <= (size_t)C::WARPS * STAGES_ * C::STAGE, "room for the list");
+    __shared__ int s_np;
+    if (tid == 0) {
+        int np = 0;
+        PieceWalk cw;
+        cw.begin(plan, prefix, blockIdx.x, plan.S);
+        for (; !cw.done(); cw.next()) {
+            const Piece pc = cw.get(p);
+            const int64_t units = prefix[pc.b + 1] - prefix[pc.b];
+            const int64_t a = (int64_t)Hkv * prefix[pc.b] + (int64_t)pc.h * units;
+            const int64_t k0 = (a + pc.u_lo) / plan.Sw, k1 = (a + pc.u_hi - 1) / plan.Sw;
+            if (pc.whole && k0 == k1) continue;  // inside one warp's slice: already final
+            EndPiece& e = eps[np++];
+            e.a = a;
+            e.units = units;
+            e.k0 = k0;
+            e.n = (int)(k1 - k0 + 1);
+            e.b = pc.b;
+            e.h = pc.h;
+            e.slot = pc.whole ? -1 : pc.slot;
+        }
+        s_np = np;
+    }
+    __syncthreads();
+    const int np = s_np;
     constexpr int NE = G * D / 4;  // float4 elements of one piece's G output rows
     for (int i0 = warp * 32; i0 < np * NE; i0 += C::THREADS) {  // warp-uniform trip count
         const int it = i0 + lane;
         const EndPiece& e = eps[(it < np * NE ? it : i0) / NE];
         const int elem = it % NE;
-        merge_element<D, G>(p.wp_o, p.wp_m, p.wp_l, e.kw_start, e.odd_w != 0, e.k0, e.n, elem / (D / 4),
-                            (elem % (D / 4)) * 4, lane, it < np * NE,
+        merge_element<D, G>(p.wp_o, p.wp_m, p.wp_l, e.a, plan.Sw, e.k0, e.n, elem / (D / 4), (elem % (D / 4)) * 4,
+                            lane, it < np * NE,
                             e.slot < 0 ? p.out + ((int64_t)e.b * p.Hq + (int64_t)e.h * G) * D : nullptr,
                             e.slot < 0 ? nullptr : p.ws_o + (int64_t)e.slot * G * D,
                             e.slot < 0 ? nullptr : p.ws_m + (int64_t)e.slot * G,
@@ -1247,7 +1224,9 @@ decode_partial_kernel(const DecodeParams p) {
         if (tid < np) {
             EndPiece& e = eps[tid];
             if (e.slot >= 0) {
-                if (!count_arrival(p, e.b, e.h, (unsigned long long)e.nc)) e.slot = -2;  // not the last: nothing to merge
+                const unsigned long long n =
+                    (unsigned long long)((e.a + e.units - 1) / plan.S - e.a / plan.S + 1);
+                if (!count_arrival(p, e.b, e.h, n)) e.slot = -2;  // not the last: nothing to merge
             } else {
                 e.slot = -2;  // final rows already written above
             }
@@ -1258,7 +1237,8 @@ decode_partial_kernel(const DecodeParams p) {
             const int it = i0 + lane;
             const EndPiece& e = eps[(it < np * NE ? it : i0) / NE];
             const int elem = it % NE;
-            merge_element<D, G>(p.ws_o, p.ws_m, p.ws_l, e.kc0, e.odd_c != 0, e.kc0, e.slot == -2 ? 0 : e.nc,
+            const int64_t k0 = e.a / plan.S, n = (e.a + e.units - 1) / plan.S - k0 + 1;
+            merge_element<D, G>(p.ws_o, p.ws_m, p.ws_l, e.a, plan.S, k0, e.slot == -2 ? 0 : (int)n,
                                 elem / (D / 4), (elem % (D / 4)) * 4, lane, it < np * NE && e.slot != -2,
                                 p.out + ((int64_t)e.b * p.Hq + (int64_t)e.h * G) * D, nullptr, nullptr, nullptr);
         }
