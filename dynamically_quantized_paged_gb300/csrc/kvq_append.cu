@@ -53,6 +53,9 @@ template <int SCHEME, int D>
 __global__ void __launch_bounds__(APPEND_THREADS, 4) append_kernel(AppendParams p) {
     constexpr int LPR = D / 8;     // lanes per row
     constexpr int RPW = 32 / LPR;  // rows per warp
+    // a decode launched next may be scheduled now (it waits for this grid to
+    // complete before reading anything)
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int li = lane % LPR;
     const int H = p.num_kv_heads;

@@ -529,6 +529,11 @@ decode_partial_kernel(const DecodeParams p) {
     using C = DecodeCfg<SCHEME, D, G>;
     constexpr int STAGES_ = C::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
+    // Launched with programmatic stream serialization: the CTAs may be
+    // resident before the previous kernel in the stream ends; nothing that
+    // kernel may have written (cache, tables, lengths, queries) is read
+    // before it has completed.
+    grid_dependency_wait();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     int64_t* misc = reinterpret_cast<int64_t*>(smem + C::OFF_MISC);
@@ -1304,7 +1309,20 @@ cudaError_t launch_decode_partial_t(const DecodeParams& p, cudaStream_t s) {
     using C = DecodeCfg<SCHEME, D, G>;
     cudaError_t e = configure_decode_t<SCHEME, D, G>();
     if (e != cudaSuccess) return e;
-    decode_partial_kernel<SCHEME, D, G><<<p.n_ctas, C::THREADS, C::smem_bytes(p.B), s>>>(p);
+    // programmatic stream serialization: the grid may be scheduled while the
+    // kernel ahead of it (typically the append) runs; it waits for it in-kernel
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.n_ctas);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::smem_bytes(p.B);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_partial_kernel<SCHEME, D, G>, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

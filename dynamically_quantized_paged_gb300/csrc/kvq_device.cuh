@@ -35,6 +35,14 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
     return pol;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start before the kernel ahead of it in the stream has
+// finished; grid_dependency_wait() returns once that kernel has completed and
+// its memory operations are visible (at once if there is no such kernel).
+// grid_launch_dependents() lets the kernel after this one be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // 16-byte asynchronous copy global -> shared (bypassing L1), with an L2
 // cache-policy hint; completion is tracked per warp-thread with commit /
 // wait groups (no spin loops).

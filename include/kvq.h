@@ -168,7 +168,11 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_seqs,
  * last partial (arrivals are counted in workspace words tagged with a per-call
  * generation, so the workspace needs no zeroing; the last arrival clears its
  * word, so a recorded call can be replayed, e.g. from a CUDA graph, as long
- * as no two calls sharing a workspace run at the same time).
+ * as no two calls sharing a workspace run at the same time).  The kernel is
+ * launched with programmatic stream serialization: its CTAs may become
+ * resident while the kernel ahead of it on the stream (e.g. kvq_append) is
+ * still running, but read no argument and no cache byte before that kernel
+ * has completed.
  * kvq_decode_partial followed by kvq_decode_merge is the equivalent
  * two-launch form and gives bitwise the same output. */
 kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const int32_t* block_table,
