@@ -126,6 +126,26 @@ def job_throughput(bytes_per_rank_step: int, world: int, ms_per_step: float) -> 
 
 
 # ---------------------------------------------------------------- clocks
+STAGE_ALIGN = 256  # byte alignment of each tensor in the host staging buffer
+
+
+def stage_layout(tensors) -> tuple[list, int]:
+    """Byte offsets of `tensors` packed end to end in one staging buffer,
+    each at a STAGE_ALIGN-byte boundary, and the buffer's total size."""
+    offs, total = [], 0
+    for t in tensors:
+        total = (total + STAGE_ALIGN - 1) // STAGE_ALIGN * STAGE_ALIGN
+        offs.append(total)
+        total += t.numel() * t.element_size()
+    return offs, total
+
+
+def stage_view(buf, t, off: int):
+    """The region of the uint8 buffer `buf` at byte offset `off`, viewed with
+    the dtype and shape of `t`."""
+    return buf[off:off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -327,20 +347,12 @@ class Bench:
         tensors the calls take are views of its device twin."""
         torch = self.torch
         srcs = list(self.q) + list(self.k_new) + list(self.v_new) + [self.slots_new, self.bt, self.seq_lens]
-        offs, total = [], 0
-        for t in srcs:
-            total = (total + 255) // 256 * 256
-            offs.append(total)
-            total += t.numel() * t.element_size()
+        offs, total = stage_layout(srcs)
         h_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
         d_buf = torch.empty(total, dtype=torch.uint8, device=self.dev)
-
-        def view(buf, t, off):
-            return buf[off:off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-
         for t, off in zip(srcs, offs):
-            view(h_buf, t, off).copy_(t.cpu())
-        d_views = [view(d_buf, t, off) for t, off in zip(srcs, offs)]
+            stage_view(h_buf, t, off).copy_(t.cpu())
+        d_views = [stage_view(d_buf, t, off) for t, off in zip(srcs, offs)]
         nl = len(self.q)
         d_q, d_k, d_v = d_views[:nl], d_views[nl:2 * nl], d_views[2 * nl:3 * nl]
         d_slots, d_bt, d_lens = d_views[3 * nl:]

@@ -49,3 +49,29 @@ def test_single_rank_is_the_identity():
     import bench
     assert bench.max_over_ranks(2.5, 1) == 2.5
     assert bench.job_throughput(10**9, 1, 1.0) == pytest.approx(1000.0)
+
+
+def test_end_to_end_staging_layout_round_trips():
+    """The end-to-end step stages every input tensor in one pinned buffer:
+    offsets are aligned, regions do not overlap, and each view reads back its
+    tensor exactly."""
+    import torch
+    import bench
+    g = torch.Generator().manual_seed(7)
+    srcs = [torch.randn(3, 5, 8, generator=g).to(torch.bfloat16),
+            torch.randint(0, 1 << 40, (37,), generator=g, dtype=torch.int64),
+            torch.randint(-1, 100, (4, 9), generator=g, dtype=torch.int32),
+            torch.randint(0, 100, (1,), generator=g, dtype=torch.int32),
+            torch.empty(0, dtype=torch.int32)]
+    offs, total = bench.stage_layout(srcs)
+    ends = [o + t.numel() * t.element_size() for o, t in zip(offs, srcs)]
+    assert all(o % bench.STAGE_ALIGN == 0 for o in offs)
+    assert all(e <= o for e, o in zip(ends, offs[1:]))
+    assert total == ends[-1]
+    buf = torch.full((total,), 0xAB, dtype=torch.uint8)
+    for t, o in zip(srcs, offs):
+        bench.stage_view(buf, t, o).copy_(t)
+    for t, o in zip(srcs, offs):
+        v = bench.stage_view(buf, t, o)
+        assert v.dtype == t.dtype and v.shape == t.shape and v.is_contiguous()
+        assert torch.equal(v, t)
