@@ -228,3 +228,50 @@ def test_graph_replay_matches_eager_call():
         torch.cuda.synchronize()
         assert kvq.last_device_error() == kvq.OK
         assert np.array_equal(out.cpu().numpy().astype(np.float64), ref)
+
+
+def test_decode_right_after_append_sees_the_new_tokens():
+    """The decode is launched so that it may be scheduled while the append
+    ahead of it on the stream still runs.  Appending each sequence's newest
+    token and decoding at once, with no synchronization between the two
+    calls, must attend over that token: eagerly, and replayed from a CUDA
+    graph holding both calls."""
+    w = small("int8", 32, 8, 128, 16)
+    full = np.array([3001, 17, 4096, 1, 800, 2500], np.int32)
+    bt, num_pages = inp.page_table(full, w.page_size, w.seed, 3)
+    case = Case(w, full - 1, block_table=bt, num_pages=num_pages)
+    ks, vs, sl = [], [], []
+    for b, L in enumerate(full):
+        k, v = inp.kv_rows(w, 0, b, int(L) - 1, int(L))
+        ks.append(k)
+        vs.append(v)
+        sl.append(inp.slots(bt, b, np.array([L - 1]), w.page_size))
+    k_new, v_new, s_new = np.concatenate(ks), np.concatenate(vs), np.concatenate(sl)
+    assert case.o.append(s_new, k_new, v_new) == 0
+    ref = case.o.decode_attn(case.q, bt, full, w.q_heads, 0.0)
+
+    d_s, d_k, d_v = dev(s_new), dev_bits(k_new), dev_bits(v_new)
+    q, d_bt, d_len = dev_bits(case.q), dev(bt), dev(full)
+    out = torch.full((len(full), w.q_heads, w.head_dim), float("nan"), dtype=torch.float32, device=DEV)
+    ws = kvq.alloc_workspace(case.g, len(full), w.q_heads, bt.shape[1], device=DEV)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        kvq.append(case.g, d_s, d_k, d_v, stream=stream)
+        kvq.decode_attn(case.g, q, d_bt, d_len, out, ws, stream=stream)
+    stream.synchronize()
+    assert kvq.last_device_error() == kvq.OK
+    eager = out.cpu().numpy().astype(np.float64)
+    assert_attn_close(eager, ref, "decode right after append")
+    case.compare_cache(full=True)
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        kvq.append(case.g, d_s, d_k, d_v, stream=stream)
+        kvq.decode_attn(case.g, q, d_bt, d_len, out, ws, stream=stream)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert kvq.last_device_error() == kvq.OK
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), eager)
