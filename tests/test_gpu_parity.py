@@ -275,3 +275,54 @@ def test_decode_right_after_append_sees_the_new_tokens():
         torch.cuda.synchronize()
         assert kvq.last_device_error() == kvq.OK
         assert np.array_equal(out.cpu().numpy().astype(np.float64), eager)
+
+
+def quotient_sweep_rows(D=128):
+    """bf16 rows (as uint16 bits) in which every positive bf16 value x <= a
+    appears, with alternating signs, next to a row maximum a: for a of every
+    one of the 128 bf16 mantissas at three exponents.  With a fixed, the 8-bit
+    scale is a / qmax, so each row sweeps every bf16 quotient x / s the
+    append can meet at that scale mantissa, the ones within a hair of a
+    rounding midpoint included."""
+    rows = []
+    for e in (120, 127, 133):
+        for m in range(128):
+            a = (e << 7) | m
+            xs = np.arange(0, a + 1, dtype=np.uint16)
+            xs[1::2] |= 0x8000
+            n = D - 1
+            pad = (-xs.size) % n
+            xs = np.concatenate([xs, np.zeros(pad, np.uint16)]).reshape(-1, n)
+            r = np.empty((xs.shape[0], D), np.uint16)
+            r[:, 0] = a
+            r[:, 1:] = xs
+            rows.append(r)
+    return np.concatenate(rows)
+
+
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4"])
+def test_append_quotient_sweep_bit_exact(scheme):
+    """The append divides by the scale with a fast reciprocal product and
+    falls back to the exact IEEE quotient only near a rounding midpoint.
+    Over every bf16 value at every scale mantissa (~6.3M quotients; the sign
+    alternates) its codes, scales and zero-points equal the oracle's, which
+    divides exactly every time."""
+    D, P, H = 128, 16, 1
+    rows = quotient_sweep_rows(D)
+    T = rows.shape[0]
+    num_pages = (T + P - 1) // P
+    k = rows.reshape(T, H, D)
+    v = np.ascontiguousarray(k[::-1])
+    slots = np.arange(T, dtype=np.int64)
+    g = kvq.PagedKVCache(scheme, num_pages, P, H, D, device=DEV)
+    o = oracle.OracleCache(scheme, num_pages, P, H, D)
+    kvq.append(g, dev(slots), dev_bits(k), dev_bits(v))
+    assert o.append(slots, k, v) == 0
+    torch.cuda.synchronize()
+    assert kvq.last_device_error() == kvq.OK
+    names = ["k_codes", "v_codes", "k_scales", "v_scales"] + (["k_zeros", "v_zeros"] if scheme == "int4" else [])
+    for name in names:
+        got = g.codes_rowmajor(name[0]).reshape(-1) if "codes" in name else getattr(g, name).cpu().numpy()
+        want = getattr(o, name).view(np.uint8)
+        bad = np.nonzero(got.view(np.uint8) != want)[0]
+        assert bad.size == 0, f"{scheme} {name}: {bad.size} bytes differ, first at {bad[:5]}"
