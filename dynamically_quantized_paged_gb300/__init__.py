@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_SCHEME_MISMAT
 EXPORTS = ["kvq_status_string", "kvq_cache_bytes", "kvq_append", "kvq_decode_workspace_bytes",
            "kvq_decode_attn", "kvq_decode_partial", "kvq_decode_merge", "kvq_validate_tables",
            "kvq_last_device_error", "kvq_allocator_create", "kvq_allocator_destroy",
-           "kvq_alloc_pages", "kvq_free_pages", "kvq_allocator_free_count", "kvq_decode_attn_noalloc"]
+           "kvq_alloc_pages", "kvq_free_pages", "kvq_allocator_free_count", "kvq_decode_attn_noalloc",
+           "kvq_share_pages", "kvq_page_refcount", "kvq_copy_page"]
 
 
 class KvqError(RuntimeError):
@@ -71,6 +72,9 @@ def _load() -> ctypes.CDLL:
     L.kvq_alloc_pages.argtypes = [P, i32, P]
     L.kvq_free_pages.argtypes = [P, i32, P]
     L.kvq_allocator_free_count.argtypes, L.kvq_allocator_free_count.restype = [P], i32
+    L.kvq_share_pages.argtypes = [P, i32, P]
+    L.kvq_page_refcount.argtypes = [P, i32, ctypes.POINTER(ctypes.c_int32)]
+    L.kvq_copy_page.argtypes = [cachep, i32, i32, P]
     for name in EXPORTS:
         getattr(L, name)  # every declared entry point must be exported
     return L
@@ -149,6 +153,11 @@ class PagedKVCache:
     def nbytes(self) -> int:
         return sum(t.numel() for t in (self.k_codes, self.v_codes, self.k_scales, self.v_scales,
                                        self.k_zeros, self.v_zeros) if t is not None)
+
+
+def copy_page(cache: PagedKVCache, src: int, dst: int, stream=None) -> None:
+    """kvq_copy_page: copy-on-write of page src into page dst (every pool)."""
+    _check(lib.kvq_copy_page(ctypes.byref(cache.struct), src, dst, _stream(stream)), "kvq_copy_page")
 
 
 def append(cache: PagedKVCache, slot_mapping: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -258,8 +267,19 @@ class PageAllocator:
         return list(out[:n])
 
     def free(self, pages) -> None:
+        """Drops one reference per listed id (kvq_free_pages)."""
         arr = (ctypes.c_int32 * max(len(pages), 1))(*pages)
         _check(lib.kvq_free_pages(self._h, len(pages), arr), "kvq_free_pages")
+
+    def share(self, pages) -> None:
+        """Adds one reference per listed id (kvq_share_pages)."""
+        arr = (ctypes.c_int32 * max(len(pages), 1))(*pages)
+        _check(lib.kvq_share_pages(self._h, len(pages), arr), "kvq_share_pages")
+
+    def refcount(self, page: int) -> int:
+        out = ctypes.c_int32(0)
+        _check(lib.kvq_page_refcount(self._h, page, ctypes.byref(out)), "kvq_page_refcount")
+        return out.value
 
     @property
     def free_count(self) -> int:

@@ -185,9 +185,29 @@ int device_sm_count() {
 
 struct kvq_allocator {
     int32_t num_pages;
-    std::vector<int32_t> stack;   // free pages; allocation pops from the back
-    std::vector<uint8_t> is_free;
+    std::vector<int32_t> stack;  // free pages; allocation pops from the back
+    std::vector<int32_t> refs;   // references per page (0: free)
 };
+
+namespace {
+
+// Occurrences of each page id among pages[0..n) into cnt (num_pages entries),
+// after checking that every id is inside the pool and held (refs > 0).
+bool count_held(const kvq_allocator* a, int32_t n, const int32_t* pages, std::vector<int32_t>& cnt) {
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t p = pages[i];
+        if (p < 0 || p >= a->num_pages || a->refs[p] <= 0) return false;
+    }
+    try {
+        cnt.assign(a->num_pages, 0);
+    } catch (...) {
+        return false;
+    }
+    for (int32_t i = 0; i < n; ++i) ++cnt[pages[i]];
+    return true;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -344,6 +364,33 @@ kvq_status kvq_validate_tables(const kvq_cache* cache, const int32_t* block_tabl
     return KVQ_OK;
 }
 
+kvq_status kvq_copy_page(const kvq_cache* cache, int32_t src, int32_t dst, kvq_stream_t stream) {
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    if (src < 0 || src >= cache->num_pages || dst < 0 || dst >= cache->num_pages || src == dst)
+        return KVQ_ERR_INVALID_ARG;
+    if (current_device() < 0) return KVQ_ERR_CUDA;
+    // every pool is page-major: a page's rows ([Hkv][page_size], any interleave
+    // inside) are one contiguous block of the same size in each
+    const size_t rows = (size_t)cache->num_kv_heads * cache->page_size;
+    const bool int4 = cache->scheme == KVQ_INT4_ASYM_G32;
+    const size_t code_b = rows * (int4 ? cache->head_dim / 2 : cache->head_dim);
+    const size_t meta_b = rows * (int4 ? (cache->head_dim / 32) * 2 : 4);
+    struct Pool { void* base; size_t bytes; } pools[6] = {
+        {cache->k_codes, code_b}, {cache->v_codes, code_b}, {cache->k_scales, meta_b},
+        {cache->v_scales, meta_b}, {int4 ? cache->k_zeros : nullptr, meta_b},
+        {int4 ? cache->v_zeros : nullptr, meta_b}};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (const Pool& pl : pools) {
+        if (!pl.base) continue;
+        uint8_t* b = static_cast<uint8_t*>(pl.base);
+        if (cudaMemcpyAsync(b + (size_t)dst * pl.bytes, b + (size_t)src * pl.bytes, pl.bytes,
+                            cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return KVQ_ERR_CUDA;
+    }
+    return KVQ_OK;
+}
+
 kvq_status kvq_last_device_error(kvq_stream_t stream) {
     if (current_device() < 0) return KVQ_ERR_CUDA;
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -374,7 +421,7 @@ kvq_allocator* kvq_allocator_create(int32_t num_pages, uint64_t seed) {
     try {
         a->num_pages = num_pages;
         a->stack.resize(num_pages);
-        a->is_free.assign(num_pages, 1);
+        a->refs.assign(num_pages, 0);
     } catch (...) {
         delete a;
         return nullptr;
@@ -398,31 +445,40 @@ kvq_status kvq_alloc_pages(kvq_allocator* a, int32_t n, int32_t* out) {
     for (int32_t i = 0; i < n; ++i) {
         out[i] = a->stack.back();
         a->stack.pop_back();
-        a->is_free[out[i]] = 0;
+        a->refs[out[i]] = 1;
     }
     return KVQ_OK;
 }
 
 kvq_status kvq_free_pages(kvq_allocator* a, int32_t n, const int32_t* pages) {
     if (!a || n < 0 || (n > 0 && !pages)) return KVQ_ERR_INVALID_ARG;
-    std::vector<uint8_t> seen;
-    for (int32_t i = 0; i < n; ++i) {
-        const int32_t p = pages[i];
-        if (p < 0 || p >= a->num_pages || a->is_free[p]) return KVQ_ERR_INVALID_ARG;
-    }
+    std::vector<int32_t> cnt;
+    if (!count_held(a, n, pages, cnt)) return KVQ_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i)
+        if (cnt[pages[i]] > a->refs[pages[i]]) return KVQ_ERR_INVALID_ARG;  // more drops than references
     try {
-        seen.assign(a->num_pages, 0);
+        a->stack.reserve(a->stack.size() + (size_t)n);
     } catch (...) {
         return KVQ_ERR_INVALID_ARG;
     }
-    for (int32_t i = 0; i < n; ++i) {
-        if (seen[pages[i]]) return KVQ_ERR_INVALID_ARG;
-        seen[pages[i]] = 1;
-    }
-    for (int32_t i = 0; i < n; ++i) {
-        a->stack.push_back(pages[i]);
-        a->is_free[pages[i]] = 1;
-    }
+    for (int32_t i = 0; i < n; ++i)
+        if (--a->refs[pages[i]] == 0) a->stack.push_back(pages[i]);
+    return KVQ_OK;
+}
+
+kvq_status kvq_share_pages(kvq_allocator* a, int32_t n, const int32_t* pages) {
+    if (!a || n < 0 || (n > 0 && !pages)) return KVQ_ERR_INVALID_ARG;
+    std::vector<int32_t> cnt;
+    if (!count_held(a, n, pages, cnt)) return KVQ_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i)
+        if ((int64_t)a->refs[pages[i]] + cnt[pages[i]] > INT32_MAX) return KVQ_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i) ++a->refs[pages[i]];
+    return KVQ_OK;
+}
+
+kvq_status kvq_page_refcount(const kvq_allocator* a, int32_t page, int32_t* refs) {
+    if (!a || !refs || page < 0 || page >= a->num_pages) return KVQ_ERR_INVALID_ARG;
+    *refs = a->refs[page];
     return KVQ_OK;
 }
 

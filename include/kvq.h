@@ -240,7 +240,14 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const void* q, const 
  * memory).  The free list starts as the page ids 0..num_pages-1 shuffled by
  * Fisher-Yates driven by SplitMix64(seed), so that physical pages are
  * scattered; allocation pops pages from the end of the list, freeing pushes
- * them back (last freed, first reused).  Host only, not thread-safe. */
+ * them back (last freed, first reused).  Pages are reference counted so
+ * that sequences can share the pages of a common prefix ([P3] "How vLLM
+ * Implements KV Cache Optimization": a prefix that many requests share is
+ * cached once and reused; [P1] "Integrating ... PagedAttention": memory
+ * sharing across the sequences of a batch): a page is allocated with one
+ * reference, kvq_share_pages adds references, kvq_free_pages drops them, and
+ * a page returns to the free list when its last reference is dropped.  Host
+ * only, not thread-safe. */
 typedef struct kvq_allocator kvq_allocator;
 
 /* NULL if num_pages < 1 or the host allocation fails. */
@@ -249,10 +256,30 @@ void kvq_allocator_destroy(kvq_allocator* alloc);
 /* Pops n page ids into out[0..n).  KVQ_ERR_OUT_OF_PAGES (nothing taken) if
  * fewer than n are free. */
 kvq_status kvq_alloc_pages(kvq_allocator* alloc, int32_t n, int32_t* out);
-/* Pushes n page ids back.  KVQ_ERR_INVALID_ARG (nothing freed) if an id is
- * outside the pool, already free, or repeated. */
+/* Drops one reference to each of the n page ids (an id may repeat, once
+ * per reference dropped); pages whose last reference goes are pushed back on
+ * the free list in the order given.  KVQ_ERR_INVALID_ARG (nothing changed) if
+ * an id is outside the pool, free, or repeated more often than it has
+ * references. */
 kvq_status kvq_free_pages(kvq_allocator* alloc, int32_t n, const int32_t* pages);
+/* Adds one reference to each of the n page ids (an id may repeat, once per
+ * reference added), for a sequence that reuses another's prefix pages in its
+ * own block table.  KVQ_ERR_INVALID_ARG (nothing changed) if an id is outside
+ * the pool or free, or a count would pass 2^31 - 1. */
+kvq_status kvq_share_pages(kvq_allocator* alloc, int32_t n, const int32_t* pages);
+/* *refs = the references page holds (0: free).  KVQ_ERR_INVALID_ARG if the
+ * id is outside the pool or refs is NULL. */
+kvq_status kvq_page_refcount(const kvq_allocator* alloc, int32_t page, int32_t* refs);
 int32_t kvq_allocator_free_count(const kvq_allocator* alloc);
+
+/* Copy-on-write of one page: copies every pool's contents of page src (codes,
+ * scales, INT4 zero-points: all of its KV heads and slots) to page dst on the
+ * stream, so that a sequence whose shared prefix ends inside a page can take
+ * its own copy of that page before appending past the prefix (then update its
+ * block-table entry and drop its reference to src).  One device-to-device
+ * copy per pool; no kernel.  KVQ_ERR_INVALID_ARG if src or dst is outside the
+ * pool or src == dst; KVQ_ERR_CUDA if a copy cannot be enqueued. */
+kvq_status kvq_copy_page(const kvq_cache* cache, int32_t src, int32_t dst, kvq_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -88,6 +88,95 @@ def test_allocator_rejects_bad_frees():
     a.close()
 
 
+def test_allocator_shared_pages_reference_counts():
+    """Shared prefix pages: allocation gives one reference, share adds, free
+    drops, and a page goes back on the free list with its last reference."""
+    a = kvq.PageAllocator(6, 3)
+    p = a.alloc(3)
+    assert [a.refcount(x) for x in p] == [1, 1, 1]
+    a.share([p[0], p[1], p[0]])                      # p0 now held 3 times, p1 twice
+    assert [a.refcount(x) for x in p] == [3, 2, 1]
+    a.free([p[0], p[1]])
+    assert [a.refcount(x) for x in p] == [2, 1, 1] and a.free_count == 3
+    a.free([p[1], p[0], p[0], p[2]])                 # p1, p0, p2 lose their last references
+    assert [a.refcount(x) for x in p] == [0, 0, 0] and a.free_count == 6
+    assert a.alloc(3) == [p[2], p[0], p[1]]          # pushed in the order they were released
+    a.close()
+
+
+def test_allocator_share_and_free_reject_without_changing_anything():
+    a = kvq.PageAllocator(5, 9)
+    p = a.alloc(2)
+    free_page = next(x for x in range(5) if x not in p)
+    for bad in ([99], [-1], [free_page], [p[0], free_page]):
+        with pytest.raises(kvq.KvqError) as e:
+            a.share(bad)
+        assert e.value.status == 1
+    with pytest.raises(kvq.KvqError):
+        a.free([p[0], p[0]])                          # two drops, one reference
+    a.share([p[0]])
+    with pytest.raises(kvq.KvqError):
+        a.free([p[0], p[0], p[0], p[1]])              # three drops, two references
+    assert [a.refcount(x) for x in p] == [2, 1] and a.free_count == 3
+    with pytest.raises(kvq.KvqError):
+        a.refcount(5)
+    a.close()
+
+
+def test_allocator_matches_a_plain_model_under_random_operations():
+    """Random alloc / share / free sequences against a plain model of the
+    header's rules: a stack of free ids (pop from the end, push released ids
+    in call order) and a count per page; failed calls change nothing."""
+    n, seed = 40, 77
+    a = kvq.PageAllocator(n, seed)
+    stack = oracle.free_list(n, seed).tolist()
+    refs = [0] * n
+    r = np.random.default_rng(5)
+    for _ in range(3000):
+        op = r.integers(3)
+        held = [i for i in range(n) if refs[i] > 0]
+        if op == 0:
+            k = int(r.integers(0, 4))
+            if k > len(stack):
+                with pytest.raises(kvq.KvqError):
+                    a.alloc(k)
+                continue
+            got = a.alloc(k)
+            want = [stack.pop() for _ in range(k)]
+            assert got == want
+            for x in want:
+                refs[x] = 1
+        else:
+            pool = held + [int(r.integers(n))] if held else [int(r.integers(n))]
+            ids = [int(r.choice(pool)) for _ in range(int(r.integers(1, 4)))]
+            counts = {x: ids.count(x) for x in ids}
+            ok = all(refs[x] > 0 for x in ids) and (op == 1 or all(counts[x] <= refs[x] for x in ids))
+            if not ok:
+                with pytest.raises(kvq.KvqError):
+                    (a.share if op == 1 else a.free)(ids)
+            elif op == 1:
+                a.share(ids)
+                for x in ids:
+                    refs[x] += 1
+            else:
+                a.free(ids)
+                for x in ids:
+                    refs[x] -= 1
+                    if refs[x] == 0:
+                        stack.append(x)
+        assert a.free_count == len(stack)
+        assert [a.refcount(i) for i in range(n)] == refs
+    a.close()
+
+
+def test_copy_page_argument_errors_before_any_device_access():
+    c = fake_cache(num_pages=4)
+    for src, dst in ((0, 0), (-1, 1), (0, 4), (4, 0)):
+        assert kvq.lib.kvq_copy_page(ctypes.byref(c), src, dst, None) == 1
+    assert kvq.lib.kvq_copy_page(None, 0, 1, None) == 1
+    assert kvq.lib.kvq_copy_page(ctypes.byref(fake_cache(head_dim=96)), 0, 1, None) == 7
+
+
 def fake_cache(scheme=1, head_dim=128, page_size=16, heads=8, align=256, group=32, num_pages=4):
     base = 1 << 20  # never dereferenced: argument checks run before any device access
     p = lambda i: base + i * (1 << 16) + (0 if align >= 16 else align)
@@ -142,6 +231,7 @@ def test_device_calls_report_cuda_error_without_a_gpu():
     assert call_decode(c) == 5
     assert call_append(fake_cache()) == 5
     assert kvq.lib.kvq_last_device_error(None) == 5
+    assert kvq.lib.kvq_copy_page(ctypes.byref(c), 0, 1, None) == 5
 
 
 def test_no_oracle_in_product_path():

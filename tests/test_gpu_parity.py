@@ -326,3 +326,60 @@ def test_append_quotient_sweep_bit_exact(scheme):
         want = getattr(o, name).view(np.uint8)
         bad = np.nonzero(got.view(np.uint8) != want)[0]
         assert bad.size == 0, f"{scheme} {name}: {bad.size} bytes differ, first at {bad[:5]}"
+
+
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4"])
+def test_shared_prefix_pages_with_copy_on_write(scheme):
+    """Sequence B reuses the pages of sequence A's first 100 tokens (six full
+    pages shared through the allocator's reference counts); the page where
+    the prefix ends is copied with kvq_copy_page before B appends its own
+    tokens past the prefix.  The pools equal an oracle cache in which B's
+    tokens were all appended into B's own slots, and both sequences decode
+    within tolerance."""
+    w = small(scheme, 32, 8, 128, 16)
+    P, H, D = w.page_size, w.kv_heads, w.head_dim
+    La, Lp, Lb = 117, 100, 150
+    num_pages = 24
+    alloc = kvq.PageAllocator(num_pages, 11)
+    g = kvq.PagedKVCache(scheme, num_pages, P, H, D, device=DEV)
+    o = oracle.OracleCache(scheme, num_pages, P, H, D)
+    ka, va = inp.kv_rows(w, 0, 0, 0, La)
+    kb, vb = inp.kv_rows(w, 0, 1, 0, Lb)
+    kb[:Lp], vb[:Lp] = ka[:Lp], va[:Lp]          # the shared prefix: the same tokens
+
+    pages_a = alloc.alloc((La + P - 1) // P)
+    n_full = Lp // P                              # 6 pages wholly inside the prefix
+    alloc.share(pages_a[:n_full + 1])             # B's table starts with A's first 7 pages
+    own = alloc.alloc(1)[0]                       # copy-on-write of the page the prefix ends in
+    pages_b = pages_a[:n_full] + [own] + alloc.alloc((Lb + P - 1) // P - n_full - 1)
+    alloc.free([pages_a[n_full]])                 # B drops its reference to A's page
+    bt = np.full((2, len(pages_b)), -1, np.int32)
+    bt[0, :len(pages_a)] = pages_a
+    bt[1] = pages_b
+    assert [alloc.refcount(x) for x in pages_a[:n_full + 1]] == [2] * n_full + [1]
+
+    sa = inp.slots(bt, 0, np.arange(La), P)
+    kvq.append(g, dev(sa), dev_bits(ka), dev_bits(va))
+    kvq.copy_page(g, pages_a[n_full], own)
+    sb = inp.slots(bt, 1, np.arange(Lp, Lb), P)
+    kvq.append(g, dev(sb), dev_bits(kb[Lp:]), dev_bits(vb[Lp:]))
+
+    assert o.append(sa, ka, va) == 0
+    assert o.append(inp.slots(bt, 1, np.arange(Lb), P), kb, vb) == 0
+    torch.cuda.synchronize()
+    assert kvq.last_device_error() == kvq.OK
+    names = ["k_codes", "v_codes", "k_scales", "v_scales"] + (["k_zeros", "v_zeros"] if scheme == "int4" else [])
+    for name in names:
+        got = g.codes_rowmajor(name[0]).reshape(-1) if "codes" in name else getattr(g, name).cpu().numpy()
+        assert np.array_equal(got.view(np.uint8), getattr(o, name).view(np.uint8)), name
+
+    import dataclasses
+    q = inp.queries(dataclasses.replace(w, batch=2), 0)
+    lens = np.array([La, Lb], np.int32)
+    out = torch.full((2, w.q_heads, D), float("nan"), dtype=torch.float32, device=DEV)
+    ws = kvq.alloc_workspace(g, 2, w.q_heads, bt.shape[1], device=DEV)
+    kvq.decode_attn(g, dev_bits(q), dev(bt), dev(lens), out, ws)
+    assert kvq.last_device_error() == kvq.OK
+    ref = o.decode_attn(q, bt, lens, w.q_heads, 0.0)
+    assert_attn_close(out.cpu().numpy().astype(np.float64), ref, f"{scheme} shared prefix")
+    alloc.close()
