@@ -66,6 +66,10 @@ SHAPES = [  # scheme, Hq, Hkv, D, P
     ("int8", 8, 8, 64, 16), ("int8", 8, 4, 64, 16), ("int8", 16, 4, 128, 32), ("int8", 32, 4, 128, 16),
     ("fp8", 4, 4, 128, 16), ("fp8", 16, 8, 64, 32), ("fp8", 32, 8, 128, 16), ("fp8", 8, 2, 128, 48),
     ("int4", 8, 8, 128, 32), ("int4", 16, 8, 64, 16), ("int4", 16, 4, 128, 16), ("int4", 64, 8, 128, 32),
+    # the remaining (head_dim, GQA ratio) instantiations of each scheme
+    ("int8", 16, 16, 128, 16), ("int8", 16, 8, 128, 16), ("int8", 16, 4, 64, 16), ("int8", 32, 4, 64, 16),
+    ("fp8", 8, 8, 64, 16), ("fp8", 16, 8, 128, 16), ("fp8", 32, 8, 64, 16), ("fp8", 64, 8, 64, 16),
+    ("int4", 8, 8, 64, 16), ("int4", 32, 16, 128, 16), ("int4", 32, 8, 64, 16), ("int4", 64, 8, 64, 16),
 ]
 
 
