@@ -72,6 +72,7 @@ def lib():
             L.orc_quant_int8_row.argtypes = [P, ctypes.c_int, P, P]
             L.orc_quant_fp8_row.argtypes = [P, ctypes.c_int, P, P]
             L.orc_quant_int4_row.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P]
+            L.orc_quant_int4sym_row.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P]
             L.orc_append.argtypes, L.orc_append.restype = [ctypes.POINTER(_Cache), P, P, P, c_i32], ctypes.c_int
             L.orc_decode_attn.argtypes = [ctypes.POINTER(_Cache), P, P, P, c_i32, c_i32, c_i32,
                                           ctypes.c_double, P]
@@ -140,6 +141,27 @@ def quant_int4_row(x: np.ndarray, group: int = 32):
     zp = np.empty(n // group, np.uint16)
     lib().orc_quant_int4_row(_p(x), n, group, _p(packed), _p(sc), _p(zp))
     return packed, sc, zp
+
+
+def quant_int4sym_row(x: np.ndarray, group: int = 32):
+    """Symmetric INT4 of one bf16 row (bits): packed two's-complement nibbles
+    and one fp32 scale per group (scale = group absmax / 7)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    n = x.size
+    packed = np.empty(n // 2, np.uint8)
+    sc = np.empty(n // group, np.float32)
+    lib().orc_quant_int4sym_row(_p(x), n, group, _p(packed), _p(sc))
+    return packed, sc
+
+
+def unpack_int4sym(packed: np.ndarray) -> np.ndarray:
+    """The signed codes of a packed symmetric INT4 row (even channel in the
+    low nibble, two's complement)."""
+    lo = (packed & 0xF).astype(np.int16)
+    hi = (packed >> 4).astype(np.int16)
+    q = np.empty(packed.size * 2, np.int16)
+    q[0::2], q[1::2] = lo, hi
+    return np.where(q >= 8, q - 16, q)
 
 
 # ---- paged cache image ---------------------------------------------------------------

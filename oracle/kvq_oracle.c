@@ -36,7 +36,9 @@
  * by the scale; FP8-E4M3 uses qmax = 448 (largest finite E4M3) and
  * round-to-nearest-even with saturation; INT4 is asymmetric over groups of 32
  * channels with an fp16 zero-point rounded down from the group minimum and an
- * fp16 scale rounded up from (max - zero) / 15; attention is exact fp64 over
+ * fp16 scale rounded up from (max - zero) / 15; symmetric INT4 (a row
+ * function only, for the scheme the library adds next) uses groups of 32,
+ * an fp32 scale max|x| / 7 and two's-complement nibbles; attention is exact fp64 over
  * the dequantized cache with softmax scale 1/sqrt(head_dim) and query head g
  * reading KV head g / (Hq / Hkv).
  *
@@ -236,6 +238,38 @@ void orc_quant_int4_row(const uint16_t* x, int n, int group, uint8_t* packed,
         zeros[gi] = zb;
     }
     for (int j = 0; j < n / 2; ++j) packed[j] = (uint8_t)(q[2 * j] | (q[2 * j + 1] << 4));
+}
+
+/* Symmetric INT4 of one row in groups of `group` channels: [P1]
+ * "Understanding Dynamic Quantization Techniques ..." with bits = 4, so the
+ * scale is the group's largest magnitude over 2^(4-1)-1 = 7 (one IEEE fp32
+ * division, kept in fp32), an all-zero group gets scale 1.0 and zero codes,
+ * and the code is the half-to-even rounding of the IEEE fp32 quotient x /
+ * scale, which lies in [-7, 7] by construction (clamped all the same).  Codes
+ * are stored as 4-bit two's complement, two per byte, the even channel in
+ * the low nibble.  (A scheme the pages name; the library's kernels do not
+ * implement it yet.) */
+void orc_quant_int4sym_row(const uint16_t* x, int n, int group, uint8_t* packed, float* scales) {
+    int ngroups = n / group;
+    int8_t q[1024];
+    for (int gi = 0; gi < ngroups; ++gi) {
+        const uint16_t* xg = x + gi * group;
+        float a = 0.0f;
+        for (int i = 0; i < group; ++i) {
+            float v = fabsf(orc_bf16_to_float(xg[i]));
+            if (v > a) a = v;
+        }
+        float s = (a == 0.0f) ? 1.0f : a / 7.0f;
+        for (int i = 0; i < group; ++i) {
+            float r = (a == 0.0f) ? 0.0f : rintf(orc_bf16_to_float(xg[i]) / s);
+            if (r < -7.0f) r = -7.0f;
+            if (r > 7.0f) r = 7.0f;
+            q[gi * group + i] = (int8_t)r;
+        }
+        scales[gi] = s;
+    }
+    for (int j = 0; j < n / 2; ++j)
+        packed[j] = (uint8_t)(((uint8_t)q[2 * j] & 0xF) | (((uint8_t)q[2 * j + 1] & 0xF) << 4));
 }
 
 /* ---- the paged cache image ------------------------------------------------- */

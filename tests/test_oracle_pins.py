@@ -226,6 +226,47 @@ def test_int4_bounds_and_range():
             assert np.all(np.abs(xf[g] - dq) <= sv / 2 * (1 + 1e-3) + 1e-7)
 
 
+# ------------------------------------------------------ symmetric INT4 ----
+def _golden_int4sym():
+    out = []
+    for line in open(os.path.join(GOLDEN, "int4sym_groups.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, xs, packed, sc = [p.strip() for p in line.split("|")]
+        out.append((name, [float(t) for t in xs.split()], [int(t, 16) for t in packed.split()], float(sc)))
+    return out
+
+
+@pytest.mark.parametrize("case", _golden_int4sym(), ids=lambda c: c[0])
+def test_int4sym_hand_examples(case):
+    name, xs, packed, sc = case
+    p, s = oracle.quant_int4sym_row(bf16(xs), 32)
+    assert p.tolist() == packed
+    assert float(s[0]) == sc
+
+
+def test_int4sym_bound_range_and_torch_rule():
+    """Codes in [-7, 7] with the group maximum at +-7, round trip within half
+    a scale, scale = fl(max|x| / 7), and the codes equal torch.round of the
+    fp32 quotient (half-to-even, as the pages' worked function rounds)."""
+    r = np.random.default_rng(21)
+    for _ in range(200):
+        x = bf16((r.standard_normal(128) * r.choice([1e-3, 1, 50]) + r.choice([0, 3])).astype(np.float32))
+        xf32 = inp.bf16_bits_to_float(x)
+        p, s = oracle.quant_int4sym_row(x, 32)
+        q = oracle.unpack_int4sym(p).astype(np.int64)
+        for gi in range(4):
+            g = slice(32 * gi, 32 * gi + 32)
+            a = np.float32(np.abs(xf32[g]).max())
+            assert s[gi] == (np.float32(1) if a == 0 else np.float32(a / np.float32(7)))
+            assert np.all(np.abs(q[g]) <= 7) and np.abs(q[g]).max() == 7
+            dq = q[g] * np.float64(s[gi])
+            assert np.all(np.abs(xf32[g].astype(np.float64) - dq) <= s[gi] / 2 * (1 + 1e-6))
+            t = torch.round(torch.from_numpy(xf32[g].copy()) / torch.tensor(s[gi], dtype=torch.float32))
+            assert np.array_equal(t.numpy().astype(np.int64), q[g])
+
+
 # ------------------------------------------------------------ attention ----
 def dense_dequant(cache: oracle.OracleCache, kv: int, rows: np.ndarray) -> np.ndarray:
     """Dequantize pool rows with this test's own reading of the layout and
