@@ -77,6 +77,20 @@ def algorithmic_bytes(w: inp.Workload, lens: np.ndarray, n_new: np.ndarray) -> d
             "kv_bytes": kv * L}
 
 
+def append_line(nb: dict, w: inp.Workload, k1_mean_ms: float, peak_gbs: float) -> dict:
+    """The quantize-append launch of a step on its own: tokens per second,
+    and its algorithmic bytes (bf16 K/V read, slots read, codes and scales
+    written) per second against the HBM peak."""
+    T = nb["append_tokens"] // w.layers      # tokens per launch
+    b = nb["append"] // w.layers             # algorithmic bytes per launch
+    t = k1_mean_ms * 1e-3
+    return {"kernel": "append_kernel (quantize-append)", "tokens_per_launch": T,
+            "mean_launch_us": round(k1_mean_ms * 1e3, 3), "tokens_per_s": round(T / t, 1),
+            "algorithmic_bytes_per_launch": b, "achieved_gbs": round(b / t / 1e9, 2),
+            "roofline_tokens_per_s": round(peak_gbs * 1e9 / (b / T), 1) if T else None,
+            "frac": round(b / t / 1e9 / peak_gbs, 4)}
+
+
 def measured_hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -272,6 +286,8 @@ class Bench:
         lens = self.seq_lens if lens is None else lens
         out = self.out if out is None else out
         for layer, c in enumerate(self.caches):
+            if events is not None:
+                events[layer][2].record()
             kvq.append(c, slots, k_new[layer], v_new[layer], stream=stream)
             if events is not None:
                 events[layer][0].record()
@@ -290,7 +306,8 @@ class Bench:
             raise RuntimeError(f"warm-up failed: {self.kvq.status_string(st)}")
         E = torch.cuda.Event
         step_ev = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(steps)]
-        k2_ev = [[(E(enable_timing=True), E(enable_timing=True)) for _ in self.caches] for _ in range(steps)]
+        # per layer: decode start (= append end), decode end, append start
+        k2_ev = [[tuple(E(enable_timing=True) for _ in range(3)) for _ in self.caches] for _ in range(steps)]
         barrier()
         torch.cuda.synchronize(self.dev)
         t0 = time.perf_counter()
@@ -304,8 +321,9 @@ class Bench:
         wall = time.perf_counter() - t0
         status = self.kvq.last_device_error()
         step_ms = [a.elapsed_time(b) for a, b in step_ev]
-        k2_ms = [a.elapsed_time(b) for row in k2_ev for a, b in row]
-        return step_ms, k2_ms, wall, status
+        k2_ms = [ev[0].elapsed_time(ev[1]) for row in k2_ev for ev in row]
+        k1_ms = [ev[2].elapsed_time(ev[0]) for row in k2_ev for ev in row]
+        return step_ms, k2_ms, k1_ms, wall, status
 
     def run_graph(self, steps: int, barrier):
         """The same step recorded once in a CUDA graph (all layers' append and
@@ -501,7 +519,7 @@ def main(argv=None):
     if not args.no_clocks:
         clocks.start()
         clocks.wait_first()
-    step_ms, k2_ms, wall, status = bench.run(args.steps, args.warmup, barrier)
+    step_ms, k2_ms, k1_ms, wall, status = bench.run(args.steps, args.warmup, barrier)
     eager_ms_per_step = max_over_ranks(sum(step_ms), world, dev) / args.steps
     graph_ms = None
     if not args.no_graph:
@@ -552,6 +570,7 @@ def main(argv=None):
                          "traffic": traffic_record(w.cid),
                          "mean_launch_us": round(k2_mean_ms * 1e3, 3),
                          "algorithmic_bytes_per_launch": nb["decode_partial"] // w.layers},
+            "append": append_line(nb, w, statistics.mean(k1_ms), peak),
             "e2e": {"value": round(job_throughput(nb["step"], world, e2e_per_step), 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_per_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": bench.launches_per_step * args.steps,
