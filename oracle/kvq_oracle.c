@@ -134,24 +134,36 @@ double orc_e4m3_value(uint8_t code) {
     return sign ? -v : v;
 }
 
-/* Round-to-nearest-even into E4M3 with saturation to +-448, by brute force:
- * among the 127 finite non-negative magnitudes, take the nearest to |y|; on a
- * tie take the one whose code is even (the even significand).  The sign of
- * the result is the sign of y, zero included. */
+/* The 127 finite non-negative E4M3 magnitudes, in code order (code c has
+ * magnitude e4m3_mag[c]; they increase strictly with c), filled once when the
+ * library is loaded from the definition above. */
+static double e4m3_mag[0x7f];
+
+__attribute__((constructor)) static void orc_init_e4m3_table(void) {
+    for (int c = 0; c < 0x7f; ++c) e4m3_mag[c] = orc_e4m3_value((uint8_t)c);
+}
+
+/* Round-to-nearest-even into E4M3 with saturation to +-448: the nearest of
+ * the 127 finite non-negative magnitudes to |y|, a tie going to the even code
+ * (the even significand).  The sign of the result is the sign of y, zero
+ * included.  The two magnitudes that bracket |y| are found by bisection over
+ * the increasing table; the nearest of the two is taken. */
 uint8_t orc_e4m3_encode(float yf) {
     double y = (double)yf;
     uint8_t sign = signbit(y) ? 0x80 : 0x00;
     double a = fabs(y);
     if (a >= 448.0) return sign | 0x7e;
-    int best = 0;
-    double best_d = INFINITY;
-    for (int c = 0; c <= 0x7e; ++c) {
-        double d = fabs(orc_e4m3_value((uint8_t)c) - a);
-        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
-            best = c;
-            best_d = d;
-        }
+    int lo = 0, hi = 0x7e; /* invariant: e4m3_mag[lo] <= a < e4m3_mag[hi] */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (e4m3_mag[mid] <= a) lo = mid;
+        else hi = mid;
     }
+    double dlo = a - e4m3_mag[lo], dhi = e4m3_mag[hi] - a;
+    int best;
+    if (dlo < dhi) best = lo;
+    else if (dhi < dlo) best = hi;
+    else best = (lo % 2 == 0) ? lo : hi;
     return sign | (uint8_t)best;
 }
 

@@ -132,6 +132,54 @@ def test_e4m3_encode_matches_torch_float8():
     assert np.array_equal(got, ref)
 
 
+def _fp8_rows_near_midpoints(r, n_rows=400, D=128):
+    """bf16 rows whose quotients x / scale fall on or within a few bf16 ulps of
+    E4M3 rounding midpoints, for scales of every mantissa (the row maximum a
+    is random, so scale = a / 448 is a generic fp32 value)."""
+    mags = np.array([oracle.e4m3_value(c) for c in range(0x7F)])
+    mids = (mags[:-1] + mags[1:]) / 2
+    rows = []
+    for _ in range(n_rows):
+        a = np.float32(r.uniform(0.5, 8.0))
+        a = inp.bf16_bits_to_float(bf16([a]))[0]
+        s = np.float32(a / np.float32(448.0))
+        m = r.choice(mids, D - 1) * r.choice([-1.0, 1.0], D - 1)
+        x = bf16(np.float32(m) * s)
+        x = (x.astype(np.int32) + r.integers(-2, 3, D - 1)).astype(np.uint16)  # a few ulps either side
+        x = np.where(np.abs(inp.bf16_bits_to_float(x)) < a, x, bf16([0.0])[0]).astype(np.uint16)
+        rows.append(np.concatenate([bf16([a]), x]))
+    return np.stack(rows)
+
+
+def test_fp8_row_matches_torch_restatement():
+    """The FP8 row rule restated with torch CPU ops in fp32: scale = max|x| /
+    448 (IEEE division), code = float8_e4m3fn cast (round-to-nearest-even) of
+    the IEEE quotient x / scale clamped to +-448; an all-zero row gets zero
+    codes and scale 1.0.  Random rows plus rows built to put the quotient on
+    or next to E4M3 midpoints, where dividing by the scale and multiplying by
+    its reciprocal round to different codes."""
+    r = np.random.default_rng(15)
+    rand = [bf16((r.standard_normal(128) * r.choice([1e-3, 1.0, 40.0])).astype(np.float32)) for _ in range(300)]
+    crafted = _fp8_rows_near_midpoints(r)
+    rows = np.concatenate([np.stack(rand), crafted, bf16(np.zeros((1, 128), np.float32))])
+    recip_differs = 0
+    for xb in rows:
+        t = torch.from_numpy(inp.bf16_bits_to_float(xb))
+        amax = t.abs().max()
+        if amax.item() == 0.0:
+            want_c, want_s = np.zeros(128, np.uint8), np.float32(1.0)
+        else:
+            scale = amax / 448.0
+            want_s = np.float32(scale.item())
+            want_c = (t / scale).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            wrong = (t * (1.0 / scale)).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            recip_differs += int((wrong != want_c).sum())
+        c, s = oracle.quant_fp8_row(xb)
+        assert np.float32(s) == want_s
+        assert np.array_equal(c, want_c)
+    assert recip_differs > 0, "the crafted rows must separate the division rule from the reciprocal rule"
+
+
 def test_fp8_row_bound():
     r = np.random.default_rng(14)
     for _ in range(100):
