@@ -157,6 +157,19 @@ kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* 
 
 namespace kvq {
 
+kvq_status decode_counter_region(const kvq_cache* cache, int B, int Hq, size_t* offset, size_t* bytes) {
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    const int G = gqa_ratio(cache, Hq);
+    if (G < 0) return KVQ_ERR_INVALID_ARG;
+    if (G == 0) return KVQ_ERR_UNSUPPORTED;
+    const int n_ctas = n_ctas_for(cache, G, B);
+    if (n_ctas <= 0) return KVQ_ERR_CUDA;
+    *offset = decode_counter_offset(n_ctas, G, cache->head_dim, B);
+    *bytes = (size_t)B * cache->num_kv_heads * sizeof(unsigned long long);
+    return KVQ_OK;
+}
+
 unsigned* device_error_word() {
     const int dev = current_device();
     if (dev < 0) return nullptr;

@@ -55,6 +55,8 @@
 // are what keeps enough bytes in flight.
 #pragma once
 
+#include <atomic>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -1274,33 +1276,42 @@ __global__ void __launch_bounds__(MERGE_THREADS) decode_merge_kernel(const Decod
                                        p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D, nullptr, nullptr, nullptr);
 }
 
-// Shared memory attribute per device, set once (host-only state).
+// Shared memory attribute per device, set once (host-only state).  Safe to
+// call from several host threads: the attribute call is idempotent, and the
+// flag only records that it succeeded.
 template <int SCHEME, int D, int G>
 cudaError_t configure_decode_t() {
     using C = DecodeCfg<SCHEME, D, G>;
-    static int configured[64];
+    static std::atomic<int> configured[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
-    if (!configured[dev]) {
+    if (!configured[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(decode_partial_kernel<SCHEME, D, G>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(MAX_SEQS));
         if (e != cudaSuccess) return e;
-        configured[dev] = 1;
+        configured[dev].store(1, std::memory_order_release);
     }
     return cudaSuccess;
 }
 
-// Resident CTAs per SM for this instantiation and batch size (the persistent
-// grid is this times the SM count).
+// Resident CTAs per SM for this instantiation (the persistent grid is this
+// times the SM count), taken at the largest shared-memory size any batch
+// needs, so that one value serves every call; queried once per device and
+// cached (a failed query is not cached).
 template <int SCHEME, int D, int G>
-int decode_ctas_per_sm_t(int B) {
+int decode_ctas_per_sm_t(int /*B*/) {
     using C = DecodeCfg<SCHEME, D, G>;
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = cached[dev].load(std::memory_order_acquire);
+    if (n > 0) return n;
     if (configure_decode_t<SCHEME, D, G>() != cudaSuccess) return 0;
-    int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partial_kernel<SCHEME, D, G>, C::THREADS,
-                                                      C::smem_bytes(B)) != cudaSuccess)
+                                                      C::smem_bytes(MAX_SEQS)) != cudaSuccess)
         return 0;
+    if (n > 0) cached[dev].store(n, std::memory_order_release);
     return n;
 }
 

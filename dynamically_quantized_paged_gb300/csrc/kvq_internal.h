@@ -101,6 +101,10 @@ cudaError_t launch_validate(const CacheView& c, const int32_t* block_table,
                             const int32_t* seq_lens, int B, int max_pages, unsigned* err,
                             cudaStream_t s);
 
+// Byte offset and length, inside a decode workspace for this problem, of the
+// per-segment arrival counters (host only; kvq_api.cu).
+kvq_status decode_counter_region(const kvq_cache* cache, int B, int Hq, size_t* offset, size_t* bytes);
+
 // Per-device error word (device address) and SM count.
 unsigned* device_error_word();
 int device_sm_count();

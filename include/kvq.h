@@ -221,13 +221,18 @@ kvq_status kvq_last_device_error(kvq_stream_t stream);
  * that memory until the process exits.  The call allocates nothing.  Its
  * first call on a device looks up the array's device address (set-up, once
  * per device, with that device current); make that first call before any
- * stream capture.  Every call shares the array and leaves its contents
- * behind; nothing in it needs to start at zero.  Calls whose kernels overlap
- * on the GPU (other streams, other host threads) race on the array: keep
- * them ordered.  Returns KVQ_ERR_WORKSPACE, launching nothing, if this
- * problem would need more scratch than the array holds (kvq_decode_workspace_bytes
- * reports the need).  Other arguments, rules and errors are those of
- * kvq_decode_attn. */
+ * stream capture: a first call made while `stream` is capturing returns
+ * KVQ_ERR_INVALID_ARG and enqueues nothing.  Every call shares the array and
+ * leaves its contents behind; the words that must start cleared (the split
+ * merge's arrival counters) are zeroed on `stream` by each call, with one
+ * memset node ahead of the decode launch.  Calls whose kernels overlap on the
+ * GPU (other streams, other host threads) race on the array: keep them
+ * ordered.  Returns KVQ_ERR_WORKSPACE, enqueuing nothing, if this problem
+ * would need more scratch than the array holds (kvq_decode_workspace_bytes
+ * reports the need).  The cached address (like the library's per-device
+ * error word) is not refreshed after cudaDeviceReset: do not use the library
+ * in a process after resetting the device.  Other arguments, rules and
+ * errors are those of kvq_decode_attn. */
 #define KVQ_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 
 kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const void* q, const int32_t* block_table,
