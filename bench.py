@@ -1,4 +1,4 @@
-"""Benchmark: one decode step of the paged quantized-KV path on GB300.
+"""Benchmark: decode steps of the paged quantized-KV path on GB300.
 
 A step is one pass of the whole hot path over one batch: quantize-append of
 the step's new tokens (kvq_append) and split-K fused-dequant decode attention
@@ -7,11 +7,28 @@ workload.  Pages come from the library's host allocator (scattered ids).
 Inputs are resident in HBM when the timed region starts; L2 is flushed (a
 256 MB write) before every timed step, outside the timed events.
 
-Default workload (N=1): the Llama-3-8B-shaped INT8 layer -- 32 sequences with
-lengths uniform in [512, 4096], 32 query / 8 KV heads, head_dim 128, page 16
--- decode step plus 1-token append.  --config selects another workload.
+Headline workload (N=1 default): the largest single-GPU configuration, the
+8-layer INT4 workload -- 16 sequences x 32768 cached tokens, 32 query / 8 KV
+heads, head_dim 128, page 32, asymmetric INT4 in groups of 32 -- decode step
+plus 1-token append per layer.  At N=1 the same JSON line carries one
+sub-record per other workload (--sub, default 2,3,5), each with its own
+decode roofline, append figures, end-to-end figure, clocks and CPU baseline.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl kvq|reference]
+Timing.  The headline `ms_per_step` is the mean over exactly --steps steps
+replayed from a CUDA graph after --warmup untimed steps, bracketed by a
+barrier and a device synchronize, max over ranks.  Per-launch kernel figures
+(the roofline and append blocks) come from a separate loop of eager steps,
+each launch bracketed by CUDA events on the launching stream, repeated for
+at least --kernel-seconds per workload so that the clock sampler sees the GPU
+under load; the clocks reported are those sampled during that loop.
+
+Multi-GPU (torchrun, N > 1): the batch's sequences are partitioned over the
+ranks (longest first onto the least-loaded rank); each rank allocates its own
+pages and block-table rows for its share and no data moves between ranks.
+`value` is all ranks' algorithmic bytes over the slowest rank's time (total
+work fixed as N grows: "scaling": "strong").
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--sub 2,3,5] [--impl kvq|reference]
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle (the
 only reference implementation there is) on the host cores, on a bounded
@@ -21,13 +38,13 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
 import sys
 import threading
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -41,6 +58,7 @@ METRIC = "paged quantized-KV decode attn GB/s (% of 8 TB/s HBM); append tokens/s
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+HEADLINE = 4
 
 
 # ---------------------------------------------------------------- accounting
@@ -52,14 +70,17 @@ def code_meta_bytes(w: inp.Workload):
 
 
 def step_plan(w: inp.Workload, lens: np.ndarray):
-    """Tokens appended per sequence in one step and the lengths after it."""
+    """Tokens appended per sequence in one step."""
     n_new = w.prefill_chunk if w.cid == 5 else w.append_tokens
-    n_new = np.minimum(lens, n_new).astype(np.int64)
-    return n_new
+    return np.minimum(lens, n_new).astype(np.int64)
 
 
 def algorithmic_bytes(w: inp.Workload, lens: np.ndarray, n_new: np.ndarray) -> dict:
-    """Bytes the method must move per step (per layer x layers): never padding."""
+    """Bytes the method must move per step (per layer x layers): never padding.
+    Decode: codes and scales of every cached token, the block-table entries of
+    the pages in use, the query rows, the lengths and the fp32 output rows.
+    Append: the bf16 K/V rows and slot of each new token read, its codes and
+    scales written."""
     cb, mb = code_meta_bytes(w)
     H, D, P = w.kv_heads, w.head_dim, w.page_size
     B, Hq = len(lens), w.q_heads
@@ -72,15 +93,30 @@ def algorithmic_bytes(w: inp.Workload, lens: np.ndarray, n_new: np.ndarray) -> d
     T = int(n_new.sum())
     append = T * (2 * H * D * 2 + 8 + 2 * H * (cb + mb))
     L = w.layers
-    return {"decode_partial": (kv + table + q + B * 4 + out) * L, "decode": decode * L,
-            "append": append * L, "step": (decode + append) * L, "append_tokens": T * L,
-            "kv_bytes": kv * L}
+    return {"decode": decode * L, "append": append * L, "step": (decode + append) * L,
+            "append_tokens": T * L, "kv_bytes": kv * L}
+
+
+def partition_sequences(lens, world: int) -> list:
+    """Shares of the batch's sequences for `world` ranks: longest first onto
+    the rank with the fewest tokens so far (ties: lower rank, then lower
+    sequence index).  Every sequence goes to exactly one rank; each share is
+    returned in increasing sequence order."""
+    lens = np.asarray(lens, np.int64)
+    order = sorted(range(len(lens)), key=lambda b: (-int(lens[b]), b))
+    load = [0] * world
+    shares = [[] for _ in range(world)]
+    for b in order:
+        r = min(range(world), key=lambda i: (load[i], i))
+        shares[r].append(b)
+        load[r] += int(lens[b])
+    return [np.array(sorted(s), np.int64) for s in shares]
 
 
 def append_line(nb: dict, w: inp.Workload, k1_mean_ms: float, peak_gbs: float) -> dict:
-    """The quantize-append launch of a step on its own: tokens per second,
-    and its algorithmic bytes (bf16 K/V read, slots read, codes and scales
-    written) per second against the HBM peak."""
+    """The quantize-append launch on its own: tokens per second, and its
+    algorithmic bytes (bf16 K/V read, slots read, codes and scales written)
+    per second against the HBM peak."""
     T = nb["append_tokens"] // w.layers      # tokens per launch
     b = nb["append"] // w.layers             # algorithmic bytes per launch
     t = k1_mean_ms * 1e-3
@@ -101,21 +137,27 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dynamically_quantized_paged_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("kvq_decode") or name in ("kvq_device.cuh", "kvq_internal.h", "kvq_tc.cuh"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()
+
+
 def traffic_record(cid: int):
-    """DRAM bytes per decode_partial launch from a committed ncu capture, if it
-    was taken on the current kernel source (else None)."""
+    """DRAM bytes per decode launch from a committed ncu capture, if it was
+    taken on the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f)
     except Exception:
         return None
-    import hashlib
-    h = hashlib.sha256()
-    for name in ("kvq_decode.cuh", "kvq_device.cuh", "kvq_internal.h"):
-        with open(os.path.join(ROOT, "dynamically_quantized_paged_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    if rec.get("kernel_source_sha256") != h.hexdigest():
+    if rec.get("kernel_source_sha256") != kernel_source_hash():
         return None
     entry = rec.get("workloads", {}).get(str(cid))
     return None if entry is None else entry.get("dram_bytes_per_launch")
@@ -133,13 +175,24 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def job_throughput(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
-    """Whole-job GB/s: every rank moves its own batch (weak scaling) in the
-    time of the slowest rank."""
-    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+def sum_over_ranks(x: int, world: int, device=None) -> int:
+    """The sum of x over all ranks (the job's total work)."""
+    if world <= 1:
+        return int(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([int(x)], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return int(t.item())
 
 
-# ---------------------------------------------------------------- clocks
+def job_throughput(total_bytes: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: all ranks' bytes of one step over the slowest rank's
+    step time."""
+    return total_bytes / (ms_per_step * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------- staging
 STAGE_ALIGN = 256  # byte alignment of each tensor in the host staging buffer
 
 
@@ -160,35 +213,37 @@ def stage_view(buf, t, off: int):
     return buf[off:off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
 
 
+# ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, enabled: bool = True):
         self.gpu = gpu_index
+        self.enabled = enabled
         self.proc = None
         self.lines = []
 
     def start(self):
+        if not self.enabled:
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 10.0:  # its start-up is done
+                time.sleep(0.05)
         except Exception:
             self.proc = None
+        return self
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
-
-    def wait_first(self, timeout_s: float = 10.0) -> None:
-        """Returns once the sampler has produced a line (its start-up is done)."""
-        t0 = time.time()
-        while self.proc is not None and not self.lines and time.time() - t0 < timeout_s:
-            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -201,7 +256,7 @@ class ClockSampler:
         self.thread.join(timeout=2)
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in self.lines[1:]:  # the first line is taken before the load starts
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -221,47 +276,65 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- the GPU arm
 class Bench:
-    def __init__(self, w: inp.Workload, device, rank: int):
+    """One workload's batch share, set up on one GPU: every layer's cache
+    filled by chunked appends (untimed), the step's new tokens and queries
+    resident, a workspace and an L2 flush buffer."""
+
+    def __init__(self, w: inp.Workload, device, seqs, alloc_seed: int):
         import torch
         import dynamically_quantized_paged_gb300 as kvq
         self.torch, self.kvq = torch, kvq
-        self.w, self.dev, self.rank = w, device, rank
-        self.lens = inp.seq_lens(w)
+        self.w, self.dev = w, device
+        self.seqs = np.asarray(seqs, np.int64)
+        self.lens = inp.seq_lens(w)[self.seqs]
         self.n_new = step_plan(w, self.lens)
-        B, P = w.batch, w.page_size
+        B, P = len(self.seqs), w.page_size
         need = inp.pages_needed(self.lens, P)
         self.max_pages = int(need.max())
         num_pages = int(need.sum()) + 16
         # page allocation through the library's host allocator (scattered ids)
-        self.alloc = kvq.PageAllocator(num_pages, seed=w.seed * 7919 + rank)
+        self.alloc = kvq.PageAllocator(num_pages, seed=alloc_seed)
         bt = np.full((B, self.max_pages), -1, np.int32)
-        for b in range(B):
-            bt[b, :need[b]] = self.alloc.alloc(int(need[b]))
+        for i in range(B):
+            bt[i, :need[i]] = self.alloc.alloc(int(need[i]))
         self.bt_host = bt
         dev = device
         self.bt = torch.from_numpy(bt).to(dev)
         self.seq_lens = torch.from_numpy(self.lens).to(dev)
         self.caches, self.q, self.k_new, self.v_new = [], [], [], []
-        new_slots = np.concatenate([inp.slots(bt, b, np.arange(self.lens[b] - self.n_new[b], self.lens[b]), P)
-                                    for b in range(B)])
+        new_slots = np.concatenate([inp.slots(bt, i, np.arange(self.lens[i] - self.n_new[i], self.lens[i]), P)
+                                    for i in range(B)])
         self.slots_new = torch.from_numpy(new_slots).to(dev)
-        for layer in range(w.layers):
-            c = kvq.PagedKVCache(w.scheme, num_pages, P, w.kv_heads, w.head_dim, device=dev, zero_init=False)
-            ks, vs = [], []
-            for b in range(B):
-                L, n = int(self.lens[b]), int(self.n_new[b])
-                for s0 in range(0, L - n, w.prefill_chunk):     # prefill (untimed)
-                    s1 = min(L - n, s0 + w.prefill_chunk)
-                    k, v = self._rows(layer, b, s0, s1)
-                    sl = inp.slots(bt, b, np.arange(s0, s1), P)
-                    kvq.append(c, torch.from_numpy(sl).to(dev), k, v)
-                k, v = self._rows(layer, b, L - n, L)
-                ks.append(k)
-                vs.append(v)
-            self.k_new.append(torch.cat(ks))
-            self.v_new.append(torch.cat(vs))
-            self.caches.append(c)
-            self.q.append(torch.from_numpy(inp.queries(w, layer).view(np.int16)).to(dev))
+        workers = min(16, os.cpu_count() or 1)
+        with ThreadPoolExecutor(max_workers=workers) as ex:
+            for layer in range(w.layers):
+                c = kvq.PagedKVCache(w.scheme, num_pages, P, w.kv_heads, w.head_dim, device=dev, zero_init=False)
+                ks, vs = [], []
+                # the rows are generated on host threads, a bounded window ahead
+                pending = {}
+                nxt = 0
+
+                def submit(i):
+                    return ex.submit(inp.kv_rows, w, layer, int(self.seqs[i]), 0, int(self.lens[i]))
+
+                for i in range(B):
+                    while nxt < B and nxt < i + 2 * workers:
+                        pending[nxt] = submit(nxt)
+                        nxt += 1
+                    k, v = pending.pop(i).result()
+                    kd = torch.from_numpy(k.view(np.int16)).to(dev)
+                    vd = torch.from_numpy(v.view(np.int16)).to(dev)
+                    L, n = int(self.lens[i]), int(self.n_new[i])
+                    for s0 in range(0, L - n, w.prefill_chunk):     # prefill (untimed)
+                        s1 = min(L - n, s0 + w.prefill_chunk)
+                        sl = inp.slots(bt, i, np.arange(s0, s1), P)
+                        kvq.append(c, torch.from_numpy(sl).to(dev), kd[s0:s1], vd[s0:s1])
+                    ks.append(kd[L - n:L].clone())
+                    vs.append(vd[L - n:L].clone())
+                self.k_new.append(torch.cat(ks))
+                self.v_new.append(torch.cat(vs))
+                self.caches.append(c)
+                self.q.append(torch.from_numpy(np.ascontiguousarray(inp.queries(w, layer)[self.seqs]).view(np.int16)).to(dev))
         self.out = torch.empty((B, w.q_heads, w.head_dim), dtype=torch.float32, device=dev)
         self.ws = kvq.alloc_workspace(self.caches[0], B, w.q_heads, self.max_pages, device=dev)
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -270,11 +343,6 @@ class Bench:
         if st != kvq.OK:
             raise RuntimeError(f"set-up failed: {kvq.status_string(st)}")
         self.launches_per_step = 2 * w.layers  # quantize-append + fused decode per layer
-
-    def _rows(self, layer, b, s0, s1):
-        k, v = inp.kv_rows(self.w, layer, b, s0, s1)
-        t = self.torch
-        return (t.from_numpy(k.view(np.int16)).to(self.dev), t.from_numpy(v.view(np.int16)).to(self.dev))
 
     def step(self, events=None, q=None, k_new=None, v_new=None, slots=None, bt=None, lens=None, out=None,
              stream=None):
@@ -295,7 +363,8 @@ class Bench:
             if events is not None:
                 events[layer][1].record()
 
-    def run(self, steps: int, warmup: int, barrier):
+    def run_eager(self, steps: int, warmup: int, barrier):
+        """--steps eager steps after --warmup: per-step events."""
         torch = self.torch
         for _ in range(warmup):
             self.flush.zero_()
@@ -305,27 +374,19 @@ class Bench:
         if st != self.kvq.OK:
             raise RuntimeError(f"warm-up failed: {self.kvq.status_string(st)}")
         E = torch.cuda.Event
-        step_ev = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(steps)]
-        # per layer: decode start (= append end), decode end, append start
-        k2_ev = [[tuple(E(enable_timing=True) for _ in range(3)) for _ in self.caches] for _ in range(steps)]
+        ev = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(steps)]
         barrier()
         torch.cuda.synchronize(self.dev)
-        t0 = time.perf_counter()
         for i in range(steps):
             self.flush.zero_()
-            step_ev[i][0].record()
-            self.step(events=k2_ev[i])
-            step_ev[i][1].record()
+            ev[i][0].record()
+            self.step()
+            ev[i][1].record()
         torch.cuda.synchronize(self.dev)
         barrier()
-        wall = time.perf_counter() - t0
-        status = self.kvq.last_device_error()
-        step_ms = [a.elapsed_time(b) for a, b in step_ev]
-        k2_ms = [ev[0].elapsed_time(ev[1]) for row in k2_ev for ev in row]
-        k1_ms = [ev[2].elapsed_time(ev[0]) for row in k2_ev for ev in row]
-        return step_ms, k2_ms, k1_ms, wall, status
+        return [a.elapsed_time(b) for a, b in ev], self.kvq.last_device_error()
 
-    def run_graph(self, steps: int, barrier):
+    def run_graph(self, steps: int, warmup: int, barrier):
         """The same step recorded once in a CUDA graph (all layers' append and
         decode launches) and replayed: what a serving loop that replays its
         decode step pays, without per-launch host overhead.  The L2 flush
@@ -339,7 +400,7 @@ class Bench:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             self.step(stream=stream)
-        for _ in range(3):
+        for _ in range(warmup):
             self.flush.zero_()
             graph.replay()
         torch.cuda.synchronize(self.dev)
@@ -347,6 +408,7 @@ class Bench:
         evs = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(steps)]
         barrier()
         torch.cuda.synchronize(self.dev)
+        t0 = time.perf_counter()
         for i in range(steps):
             self.flush.zero_()
             evs[i][0].record()
@@ -354,7 +416,34 @@ class Bench:
             evs[i][1].record()
         torch.cuda.synchronize(self.dev)
         barrier()
-        return [a.elapsed_time(b) for a, b in evs], self.kvq.last_device_error()
+        wall = time.perf_counter() - t0
+        self.graph = graph
+        return [a.elapsed_time(b) for a, b in evs], wall, self.kvq.last_device_error()
+
+    def kernel_loop(self, seconds: float):
+        """Eager steps with every append and decode launch bracketed by CUDA
+        events on the launching stream, repeated until `seconds` of wall time
+        have passed.  Returns (decode ms per launch, append ms per launch,
+        steps run, wall seconds)."""
+        torch = self.torch
+        E = torch.cuda.Event
+        batch = 64
+        evs = [[tuple(E(enable_timing=True) for _ in range(3)) for _ in self.caches] for _ in range(batch)]
+        k2, k1, n = [], [], 0
+        t0 = time.perf_counter()
+        while True:
+            for i in range(batch):
+                self.flush.zero_()
+                self.step(events=evs[i])
+            torch.cuda.synchronize(self.dev)
+            for row in evs:
+                for ev in row:
+                    k2.append(ev[0].elapsed_time(ev[1]))
+                    k1.append(ev[2].elapsed_time(ev[0]))
+            n += batch
+            if time.perf_counter() - t0 >= seconds:
+                break
+        return k2, k1, n, time.perf_counter() - t0
 
     def run_e2e(self, steps: int, warmup: int):
         """The same step through the public API with HOST buffers: a pinned host
@@ -397,6 +486,13 @@ class Bench:
         torch.cuda.synchronize(self.dev)
         return [a.elapsed_time(b) for a, b in evs], h2d, d2h
 
+    def close(self):
+        self.graph = None
+        self.caches, self.q, self.k_new, self.v_new = [], [], [], []
+        self.ws = self.flush = self.out = None
+        self.alloc.close()
+        self.torch.cuda.empty_cache()
+
 
 def describe(w: inp.Workload) -> str:
     L = w.lengths
@@ -410,6 +506,83 @@ def describe(w: inp.Workload) -> str:
         "decode step + 1-token append"
     return (f"{w.name}: {w.layers} layer(s), B={w.batch}, {lens}, Hq={w.q_heads}/Hkv={w.kv_heads}, "
             f"d={w.head_dim}, page {w.page_size}, {w.scheme} KV codes, {step}")
+
+
+def roofline_block(w, nb, k2_ms, peak, peak_kind):
+    mean = statistics.mean(k2_ms)
+    b = nb["decode"] // w.layers
+    achieved = b / (mean * 1e-3) / 1e9
+    return {"kernel": "decode kernel (split-K fused-dequant decode, merge fused)",
+            "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+            "traffic": traffic_record(w.cid), "mean_launch_us": round(mean * 1e3, 3),
+            "median_launch_us": round(statistics.median(k2_ms) * 1e3, 3), "launches_timed": len(k2_ms),
+            "algorithmic_bytes_per_launch": b, "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
+
+
+def measure_workload(w, dev, local_rank, args, world, rank, barrier, headline: bool):
+    """Everything the line reports for one workload (this rank's share)."""
+    seqs = partition_sequences(inp.seq_lens(w), world)[rank] if world > 1 else np.arange(w.batch)
+    bench = Bench(w, dev, seqs, alloc_seed=w.seed * 7919 + rank)
+    nb = algorithmic_bytes(w, bench.lens, bench.n_new)
+    total_step = sum_over_ranks(nb["step"], world, dev)
+    total_decode = sum_over_ranks(nb["decode"], world, dev)
+    total_seqs = sum_over_ranks(len(seqs), world, dev)
+    total_append = sum_over_ranks(nb["append_tokens"], world, dev)
+    steps = args.steps if headline else max(10, args.steps // 2)
+    clocks = ClockSampler(local_rank, enabled=not args.no_clocks).start()
+    eager_ms, status = bench.run_eager(steps, args.warmup, barrier)
+    graph_ms, wall, gstatus = (None, None, status) if args.no_graph else bench.run_graph(steps, args.warmup, barrier)
+    k2_ms, k1_ms, loop_steps, loop_wall = bench.kernel_loop(args.kernel_seconds)
+    clock_info = clocks.stop()
+    if status == bench.kvq.OK:
+        status = gstatus
+    timed = graph_ms if graph_ms is not None else eager_ms
+    ms_per_step = max_over_ranks(sum(timed), world, dev) / steps
+    eager_per_step = max_over_ranks(sum(eager_ms), world, dev) / steps
+    e2e_ms, h2d, d2h = bench.run_e2e(max(3, steps // 2), 3)
+    e2e_per_step = max_over_ranks(statistics.mean(e2e_ms), world, dev)
+    st2 = bench.kvq.last_device_error()
+    if status == bench.kvq.OK:
+        status = st2
+    peak, peak_kind = measured_hbm_peak()
+    rec = {
+        "value": round(job_throughput(total_step, ms_per_step), 2),
+        "ms_per_step": round(ms_per_step, 5),
+        "ms_per_step_eager": round(eager_per_step, 5),
+        "launch": "cuda_graph_replay" if graph_ms is not None else "eager",
+        "steps": steps,
+        "config": {"workload": describe(w), "batch": w.batch, "layers": w.layers,
+                   "cached_tokens": int(inp.seq_lens(w).sum()), "kv_codes": w.scheme,
+                   "l2": "flushed before every timed step (256 MB write, outside the timed events)",
+                   "parallelism": (f"sequences partitioned over {world} GPUs, no collective" if world > 1
+                                   else "1 GPU")},
+        "hbm_frac_of_8tbs": round(job_throughput(total_step, ms_per_step) / NOMINAL_HBM_GBS / max(world, 1), 4),
+        "decode_kv_gbs_step": round(job_throughput(total_decode, ms_per_step), 2),
+        "decode_tokens_per_s": round(total_seqs / (ms_per_step * 1e-3), 1),
+        "append_tokens_per_s_step": round(total_append / (ms_per_step * 1e-3), 1),
+        "algorithmic_bytes_per_step": total_step,
+        "roofline": roofline_block(w, nb, k2_ms, peak, peak_kind),
+        "append": append_line(nb, w, statistics.mean(k1_ms), peak),
+        "kernel_loop": {"steps": loop_steps, "wall_s": round(loop_wall, 3),
+                        "what": "eager steps, each launch bracketed by CUDA events; the clocks below are "
+                                "sampled across the timed steps and this loop"},
+        "e2e": {"value": round(job_throughput(total_step, e2e_per_step), 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_per_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": bench.launches_per_step * steps,
+        "clocks": clock_info,
+        "wall_s_timed_region": round(wall, 4) if wall is not None else None,
+        "step_ms_min_median_max": [round(min(timed), 5), round(statistics.median(timed), 5), round(max(timed), 5)],
+        "device_status": bench.kvq.status_string(status),
+    }
+    bench.close()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, cores, desc, _ = oracle_sample_run(w, rank, args.cpu_budget)
+        rec["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                               "sample": desc}
+    return rec
 
 
 # ---------------------------------------------------------------- oracle arms
@@ -481,10 +654,14 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=sorted(inp.WORKLOADS))
+    ap.add_argument("--config", type=int, default=HEADLINE, choices=sorted(inp.WORKLOADS))
+    ap.add_argument("--sub", default="2,3,5",
+                    help="other workloads measured as sub-records of the line at N=1 ('' for none)")
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--kernel-seconds", type=float, default=1.0,
+                    help="wall seconds of the per-launch timing loop of each workload")
     ap.add_argument("--cpu-budget", type=float, default=2.0,
-                    help="wall seconds of oracle work for the cpu_baseline sample")
+                    help="wall seconds of oracle work for each cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi during the timed region")
     ap.add_argument("--no-graph", action="store_true",
@@ -513,77 +690,32 @@ def main(argv=None):
         if world > 1:
             dist.barrier()
 
-    bench = Bench(w, dev, rank)
-    nb = algorithmic_bytes(w, bench.lens, bench.n_new)
-    clocks = ClockSampler(local_rank)
-    if not args.no_clocks:
-        clocks.start()
-        clocks.wait_first()
-    step_ms, k2_ms, k1_ms, wall, status = bench.run(args.steps, args.warmup, barrier)
-    eager_ms_per_step = max_over_ranks(sum(step_ms), world, dev) / args.steps
-    graph_ms = None
-    if not args.no_graph:
-        graph_ms, gstatus = bench.run_graph(args.steps, barrier)
-        if status == bench.kvq.OK:
-            status = gstatus
-    clock_info = clocks.stop()
-    timed_ms = graph_ms if graph_ms is not None else step_ms
-    total_ms = max_over_ranks(sum(timed_ms), world, dev)
-    ms_per_step = total_ms / args.steps
-    e2e_ms, h2d, d2h = bench.run_e2e(max(3, args.steps // 2), 3)
-    e2e_per_step = max_over_ranks(statistics.mean(e2e_ms), world, dev)
-
+    head = measure_workload(w, dev, local_rank, args, world, rank, barrier, headline=True)
+    subs = {}
+    if world == 1:
+        for s in [int(x) for x in args.sub.split(",") if x.strip()]:
+            if s != args.config:
+                subs[str(s)] = measure_workload(inp.WORKLOADS[s], dev, local_rank, args, world, rank, barrier,
+                                                headline=False)
     if rank == 0:
-        peak, peak_kind = measured_hbm_peak()
-        k2_mean_ms = statistics.mean(k2_ms)
-        achieved = nb["decode_partial"] / w.layers / (k2_mean_ms * 1e-3) / 1e9
-        value = job_throughput(nb["step"], world, ms_per_step)
-        decode_gbs = nb["decode"] / (ms_per_step * 1e-3) / 1e9
         line = {
             "metric": METRIC,
-            "value": round(value, 2),
+            "value": head.pop("value"),
             "unit": "GB/s",
             "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup,
-            "ms_per_step": round(ms_per_step, 5),
-            "ms_per_step_eager": round(eager_ms_per_step, 5),
-            "launch": "cuda_graph_replay" if graph_ms is not None else "eager",
+            "ms_per_step": head.pop("ms_per_step"),
             "higher_is_better": True,
-            "scaling": "weak",
+            "scaling": "strong",
             "vs_baseline": None,
             "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": describe(w), "batch": w.batch, "layers": w.layers,
-                       "cached_tokens": int(bench.lens.sum()), "kv_codes": w.scheme,
-                       "l2": "flushed before every timed step (256 MB write, outside the timed events)",
-                       "parallelism": f"replicas x{world} (independent batches, no collective)"},
-            "hbm_frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
-            "decode_kv_gbs_step": round(decode_gbs, 2),
-            "decode_tokens_per_s": round(world * w.batch / (ms_per_step * 1e-3), 1),
-            "append_tokens_per_s_step": round(world * nb["append_tokens"] / (ms_per_step * 1e-3), 1),
-            "algorithmic_bytes_per_step": nb["step"],
-            "roofline": {"kernel": "decode_partial_kernel (split-K fused-dequant decode, merge fused)",
-                         "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                         if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "traffic": traffic_record(w.cid),
-                         "mean_launch_us": round(k2_mean_ms * 1e3, 3),
-                         "algorithmic_bytes_per_launch": nb["decode_partial"] // w.layers},
-            "append": append_line(nb, w, statistics.mean(k1_ms), peak),
-            "e2e": {"value": round(job_throughput(nb["step"], world, e2e_per_step), 2), "unit": "GB/s",
-                    "ms_per_step": round(e2e_per_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": bench.launches_per_step * args.steps,
-            "clocks": clock_info,
-            "wall_s_timed_region": round(wall, 4),
-            "step_ms_min_median_max": [round(min(timed_ms), 5), round(statistics.median(timed_ms), 5),
-                                       round(max(timed_ms), 5)],
-            "device_status": bench.kvq.status_string(status),
         }
-        if not args.no_cpu_baseline and world >= 1:
-            gbs, cores, desc, _ = oracle_sample_run(w, rank, args.cpu_budget)
-            line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                    "sample": desc}
+        head.pop("steps")
+        line.update(head)
+        if subs:
+            line["workloads"] = subs
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -597,7 +729,8 @@ def run_reference(args, w, rank, world):
     gbs, cores, desc, times = oracle_sample_run(w, 0, args.cpu_budget, steps=args.steps, warmup=args.warmup)
     ms = statistics.mean(times) * 1e3
     line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "strong",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": describe(w), "batch": w.batch, "layers": w.layers, "kv_codes": w.scheme},
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "kind": "oracle", "cores": cores,
