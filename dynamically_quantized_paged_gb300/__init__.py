@@ -141,12 +141,9 @@ class PagedKVCache:
 
     def codes_rowmajor(self, which: str):
         """Host copy of the K or V codes (which = "k" or "v") as
-        uint8 [num_pages][num_kv_heads][page_size][code bytes per token]; the
-        INT8 V pool, stored 4 tokens of a channel per word, is reordered."""
+        uint8 [num_pages][num_kv_heads][page_size][code bytes per token]."""
         t = (self.k_codes if which == "k" else self.v_codes).cpu().numpy()
         cb = self.head_dim // 2 if self.scheme == "int4" else self.head_dim
-        if self.scheme == "int8" and which == "v":
-            t = t.reshape(self.num_pages, self.num_kv_heads, self.page_size // 4, cb, 4).transpose(0, 1, 2, 4, 3)
         return t.reshape(self.num_pages, self.num_kv_heads, self.page_size, cb)
 
     @property

@@ -121,8 +121,7 @@ kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* 
     if (dev < 0) return KVQ_ERR_CUDA;
     const int n_ctas = n_ctas_for(cache, G, B);
     if (n_ctas <= 0) return KVQ_ERR_CUDA;
-    const int warps = kvq::decode_warps(G);
-    const size_t need = kvq::decode_workspace_bytes(n_ctas, warps, G, cache->head_dim, B, cache->num_kv_heads);
+    const size_t need = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, B, cache->num_kv_heads);
     if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     unsigned* err = kvq::device_error_word();
     if (!err) return KVQ_ERR_CUDA;
@@ -145,11 +144,6 @@ kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* 
     p.gen = next_generation();
     p.seg_ctr = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) +
                                                       kvq::decode_counter_offset(n_ctas, G, cache->head_dim, B));
-    p.wp_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                      kvq::decode_warp_partial_offset(n_ctas, G, cache->head_dim, B,
-                                                                      cache->num_kv_heads));
-    p.wp_m = p.wp_o + (size_t)2 * n_ctas * warps * G * cache->head_dim;
-    p.wp_l = p.wp_m + (size_t)2 * n_ctas * warps * G;
     return KVQ_OK;
 }
 
@@ -312,7 +306,7 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_seqs,
     if (G == 0) return KVQ_ERR_UNSUPPORTED;
     const int n_ctas = n_ctas_for(cache, G, num_seqs);
     if (n_ctas <= 0) return KVQ_ERR_CUDA;
-    *bytes = kvq::decode_workspace_bytes(n_ctas, kvq::decode_warps(G), G, cache->head_dim, num_seqs,
+    *bytes = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, num_seqs,
                                          cache->num_kv_heads);
     return KVQ_OK;
 }

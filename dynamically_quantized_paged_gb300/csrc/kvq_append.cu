@@ -143,16 +143,8 @@ __global__ void __launch_bounds__(APPEND_THREADS, 4) append_kernel(AppendParams 
                     }
                 }
                 if (valid) {
-                    if (SCHEME == KVQ_INT8_SYM_TOKEN && kv) {
-                        // V codes: 4 consecutive tokens of a channel side by side
-                        // (the row-major offset of a 4-token block is unchanged)
-                        uint8_t* dst = p.v_codes + (prow - off) * D + (off / 4) * (4 * D) + (li * 8) * 4 + (off % 4);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) dst[4 * i] = (uint8_t)((i < 4 ? lo : hi) >> (8 * (i & 3)));
-                    } else {
-                        uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * D + li * 8;
-                        *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
-                    }
+                    uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * D + li * 8;
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
                     if (li == 0) static_cast<float*>(kv ? p.v_scales : p.k_scales)[prow] = scale;
                 }
             } else {  // INT4 asymmetric, groups of 32 channels = 4 lanes

@@ -1,15 +1,15 @@
-// kvq_decode_int4.cu -- instantiations of the split-K decode kernel for the
+// kvq_decode_int4.cu -- instantiations of the tensor-core decode kernel for the
 // int4 scheme (separate translation unit so the schemes compile in parallel).
-#include "kvq_decode.cuh"
+#include "kvq_tc.cuh"
 
 namespace kvq {
 
 cudaError_t launch_decode_partial_int4(const DecodeParams& p, int G, cudaStream_t s) {
-    return launch_decode_partial_scheme<KVQ_INT4_ASYM_G32>(p, G, s);
+    return tc::launch_scheme<KVQ_INT4_ASYM_G32>(p, G, s);
 }
 
-int decode_ctas_per_sm_int4(int head_dim, int G, int B) {
-    return decode_ctas_per_sm_scheme<KVQ_INT4_ASYM_G32>(head_dim, G, B);
+int decode_ctas_per_sm_int4(int head_dim, int G, int /*B*/) {
+    return tc::ctas_per_sm_scheme<KVQ_INT4_ASYM_G32>(head_dim, G);
 }
 
 }  // namespace kvq

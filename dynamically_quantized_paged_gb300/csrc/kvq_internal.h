@@ -18,10 +18,8 @@ constexpr unsigned ERR_TIMEOUT = 2u;
 constexpr int UNIT = 16;
 // Threads of the two-launch form's merge kernel (one CTA per segment).
 constexpr int MERGE_THREADS = 128;
-// Warps of a decode CTA (one CTA per SM) for GQA ratio G.
-constexpr int decode_warps(int G) { return G >= 8 ? 8 : 12; }
 constexpr int MAX_SEQS = 4096;     // per decode call (the plan lives in shared memory)
-constexpr int MIN_SLICE_UNITS = 8; // smallest per-warp share of the work, in units
+constexpr int MIN_SLICE_UNITS = 8; // smallest per-CTA share of the work, in units (one tile)
 
 struct CacheView {
     int scheme, num_pages, page_size, num_kv_heads, head_dim, group;
@@ -57,9 +55,6 @@ struct DecodeParams {
     float* ws_o;  // [2 * n_ctas][G][D]
     float* ws_m;  // [2 * n_ctas][G]
     float* ws_l;  // [2 * n_ctas][G]
-    float* wp_o;  // per-warp partials: [2 * n_ctas * warps][G][D]
-    float* wp_m;  // [2 * n_ctas * warps][G]
-    float* wp_l;  // [2 * n_ctas * warps][G]
     int B, Hq, max_pages;
     int n_ctas;
     float q_scale;  // softmax scale * log2(e), folded into q
@@ -69,11 +64,10 @@ struct DecodeParams {
     unsigned long long* seg_ctr;        // [B * Hkv] arrival counters: (gen << 32) | arrivals
 };
 
-// Workspace layout for n_ctas persistent CTAs of `warps` warps (two partial
-// slots per CTA and per warp): CTA partials o [2 n_ctas][G][D], m [2 n_ctas][G],
-// l [2 n_ctas][G] (fp32); the published plan: int64 U, int64 S, int32
-// prefix[B + 1]; one uint64 arrival counter per (sequence, KV head) segment;
-// then (16-byte aligned) the warp partials o [2 n_ctas warps][G][D], m, l.
+// Workspace layout for n_ctas persistent CTAs (two partial slots per CTA):
+// partials o [2 n_ctas][G][D], m [2 n_ctas][G], l [2 n_ctas][G] (fp32); the
+// published plan: int64 U, int64 S, int32 prefix[B + 1]; then (8-byte
+// aligned) one uint64 arrival counter per (sequence, KV head) segment.
 inline size_t decode_plan_offset(int n_ctas, int G, int D) {
     const size_t slots = 2 * (size_t)n_ctas;
     return slots * G * D * sizeof(float) + 2 * slots * G * sizeof(float);
@@ -82,14 +76,9 @@ inline size_t decode_counter_offset(int n_ctas, int G, int D, int B) {
     const size_t end_plan = decode_plan_offset(n_ctas, G, D) + 16 + ((size_t)B + 1) * sizeof(int32_t);
     return (end_plan + 7) / 8 * 8;
 }
-inline size_t decode_warp_partial_offset(int n_ctas, int G, int D, int B, int Hkv) {
+inline size_t decode_workspace_bytes(int n_ctas, int G, int D, int B, int Hkv) {
     const size_t end = decode_counter_offset(n_ctas, G, D, B) + (size_t)B * Hkv * sizeof(unsigned long long);
     return (end + 15) / 16 * 16;
-}
-inline size_t decode_workspace_bytes(int n_ctas, int warps, int G, int D, int B, int Hkv) {
-    const size_t slots = 2 * (size_t)n_ctas * warps;
-    return decode_warp_partial_offset(n_ctas, G, D, B, Hkv) + slots * G * D * sizeof(float) +
-           2 * slots * G * sizeof(float);
 }
 
 cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaStream_t s);

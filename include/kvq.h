@@ -79,10 +79,6 @@ typedef enum kvq_scheme {
  * caller-owned device memory, sized by kvq_cache_bytes.  Layout:
  *   codes   [num_pages][num_kv_heads][page_size][head_dim]    int8 / e4m3
  *           [num_pages][num_kv_heads][page_size][head_dim/2]  INT4 (packed)
- *           INT8 V codes only: [num_pages][num_kv_heads][page_size/4][head_dim][4],
- *           the codes of 4 consecutive tokens of one channel side by side
- *           (the operand of one 4-way byte dot product in the value sum);
- *           a 16-token run still occupies the same 16 * head_dim bytes.
  *   scales  [num_pages][num_kv_heads][page_size]              fp32
  *           [num_pages][num_kv_heads][page_size][head_dim/32] fp16 (INT4)
  *   zeros   INT4 only, same shape as its scales; NULL otherwise.
