@@ -20,11 +20,14 @@
 // accumulation; the CUDA cores only widen codes, run the online softmax and
 // fold the per-token scales in.
 //
-// One CTA per SM (persistent grid), 10 warps:
-//  * warp 8, the producer: streams each tile's pages with 16-byte cp.async
-//    into a ring of R raw stages (K codes, V codes, scales, INT4 zero-points,
-//    the piece's query rows); completion is tracked by the stage's mbarrier
-//    (cp.async.mbarrier.arrive), so the producer never waits for its copies;
+// One CTA per SM (persistent grid), 12 warps:
+//  * warps 8-10, the producers: stream each tile's pages with 16-byte
+//    cp.async into a ring of R raw stages (K codes, V codes, scales, INT4
+//    zero-points, the piece's query rows), the tile's 16-token units dealt
+//    round-robin over the three warps; completion is tracked by the stage's
+//    mbarrier (cp.async.mbarrier.arrive), so no producer waits for its
+//    copies, and the page ids of the next tile are loaded while the copies
+//    of this one are issued;
 //  * warps 0-3, the token group (thread = token of the tile): widens its
 //    token's K codes into tensor memory (the A operand of the scores, lane =
 //    token), builds the query operand at the start of each piece, and after
@@ -35,7 +38,7 @@
 //    memory (the A operand of the values MMA, stored channel-contiguous per
 //    token: "MN-major"), then, thread = channel, folds each tile's values
 //    product into its running fp32 output (rescaled by the softmax's alpha);
-//  * warp 9, lane 0, the MMA issuer: scores of tile i, then values of tile
+//  * warp 11, lane 0, the MMA issuer: scores of tile i, then values of tile
 //    i - 1, each completed into an mbarrier by tcgen05.commit.
 // Every operand buffer is double-buffered by tile parity, so the token group
 // widens tile i + 1 while the scores of tile i run, and the channel group
@@ -257,9 +260,10 @@ struct Cfg {
     static constexpr int TM_COLS = TM_USED <= 32 ? 32 : TM_USED <= 64 ? 64 : TM_USED <= 128 ? 128
                                  : TM_USED <= 256 ? 256 : 512;
     static_assert(TM_USED <= 512, "tensor memory");
-    // threads
-    static constexpr int THREADS = 320;
-    static constexpr int PR_WARP = 8, MM_WARP = 9;
+    // threads: token group 0-3, channel group 4-7, NPW producer warps, the MMA warp
+    static constexpr int NPW = 3;
+    static constexpr int PR_WARP0 = 8, MM_WARP = PR_WARP0 + NPW;
+    static constexpr int THREADS = 32 * (MM_WARP + 1);
     // one raw stage (bytes)
     static constexpr int RK = 0;
     static constexpr int RV = RK + T * CB;
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
 
     if (tid == 0) {
         for (int s = 0; s < R; ++s) {
-            mbar_init(full(s), 32 + 1);  // 32 producer lanes' copies + the producer's metadata
+            mbar_init(full(s), C::NPW * (32 + 1));  // per producer warp: 32 lanes' copies + its lane 0
             mbar_init(empty(s), 8);      // 4 token warps + 4 channel warps
         }
         for (int b = 0; b < 2; ++b) {
@@ -460,43 +464,49 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
     const int Hkv = p.c.num_kv_heads;
     const int P = p.c.page_size;
 
-    if (warp == C::PR_WARP) {
-        // ------------------------------------------------------------ producer
+    if (warp >= C::PR_WARP0 && warp < C::PR_WARP0 + C::NPW) {
+        // ------------------------------------------------------------ producers
+        // NPW warps fill each stage together: warp pw copies units pw, pw +
+        // NPW, ... of the tile (a single warp's 16-byte copies cannot keep up
+        // with the consumers); the last warp also copies a piece's query rows.
+        const int pw = warp - C::PR_WARP0;
         const uint64_t pol_kv = l2_evict_first_policy();  // pages are read once
         const uint64_t pol_q = l2_evict_normal_policy();
         TileIter it;
         it.begin(plan, prefix, p);
-        for (int i = 0; it.valid; it.template next<TU>(p), ++i) {
+        // page id of this lane's unit of tile t2 (lane < units of the tile),
+        // loaded one tile ahead of its copies
+        auto page_of = [&](const TileIter& t2) -> int {
+            if (!t2.valid || lane >= t2.template nunits<TU>()) return -1;
+            const int lp = ((t2.u0 + lane) * UNIT) / P;
+            return __ldg(p.block_table + (int64_t)t2.pc.b * p.max_pages + lp);
+        };
+        int my_page = page_of(it);
+        for (int i = 0; it.valid; ++i) {
             const int s = i % R;
             if (i >= R && !mbar_wait(empty(s), ((i / R) - 1) & 1, p.err)) {
                 *sm.abort_flag() = 1;
                 break;
             }
             if (*sm.abort_flag()) break;
+            TileIter nx = it;
+            nx.template next<TU>(p);
+            const int next_page = page_of(nx);
             uint8_t* st = smem + C::OFF_RAW0 + s * C::STAGE;
             const Piece& pc = it.pc;
             const int nu = it.template nunits<TU>();
-            if (it.first()) {  // the piece's query rows travel with its first tile
+            if (it.first() && pw == C::NPW - 1) {  // the piece's query rows travel with its first tile
                 const uint8_t* qsrc =
                     reinterpret_cast<const uint8_t*>(p.q + ((int64_t)pc.b * p.Hq + (int64_t)pc.h * G) * D);
                 constexpr int NQ = G * D * 2 / 16;
                 for (int c = lane; c < NQ; c += 32) cp_async16(st + C::RQ + 16 * c, qsrc + 16 * c, pol_q);
             }
-            // page ids of the tile's units, one lane each
-            int my_page = -1;
-            if (lane < nu) {
-                const int u = it.u0 + lane;
-                const int lp = (u * UNIT) / P;
-                my_page = __ldg(p.block_table + (int64_t)pc.b * p.max_pages + lp);
-            }
-            uint32_t bad = 0;
-            for (int uu = 0; uu < nu; ++uu) {
+            // units whose page id lies outside the pool are not copied (every
+            // warp sees the whole mask; warp 0 publishes it)
+            const uint32_t bad = __ballot_sync(0xffffffffu, lane < nu && (my_page < 0 || my_page >= p.c.num_pages));
+            for (int uu = pw; uu < nu; uu += C::NPW) {
                 const int page = __shfl_sync(0xffffffffu, my_page, uu);
-                if (page < 0 || page >= p.c.num_pages) {
-                    bad |= 1u << uu;
-                    if (lane == 0) flag_error(p.err, ERR_BAD_TABLE);
-                    continue;
-                }
+                if ((bad >> uu) & 1u) continue;
                 const int u = it.u0 + uu;
                 const int off = u * UNIT - ((u * UNIT) / P) * P;
                 const int64_t row = ((int64_t)page * Hkv + pc.h) * P + off;
@@ -524,10 +534,15 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                     cp_async16(st + dst + uu * UNIT * C::MB + 16 * part,
                                static_cast<const uint8_t*>(src) + row * C::MB + 16 * part, pol_kv);
             }
-            if (lane == 0) sm.stage_bad()[s] = bad;
+            if (pw == 0 && lane == 0) {
+                sm.stage_bad()[s] = bad;
+                if (bad) flag_error(p.err, ERR_BAD_TABLE);
+            }
             __syncwarp();
             cp_async_arrive_noinc(full(s));
             if (lane == 0) mbar_arrive(full(s));
+            my_page = next_page;
+            it = nx;
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == C::MM_WARP) {
