@@ -21,20 +21,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// L2 policy for data read exactly once (the KV pages): evict first.
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-// L2 policy for data several CTAs read (the query rows): normal eviction.
-__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
 // Programmatic dependent launch.  A kernel launched with programmatic stream
 // serialization may start before the kernel ahead of it in the stream has
 // finished; grid_dependency_wait() returns once that kernel has completed and
@@ -43,13 +29,13 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
-// 16-byte asynchronous copy global -> shared (bypassing L1), with an L2
-// cache-policy hint; completion is tracked per warp-thread with commit /
-// wait groups (no spin loops).
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-                 "l"(policy)
-                 : "memory");
+// 16-byte asynchronous copy global -> shared (bypassing L1).  No L2
+// cache-policy operand: on sm_103a the cache-hinted form of this copy raised
+// "illegal instruction" in a minimal streaming kernel whose unhinted twin ran
+// clean, so no copy in this library carries one.  Completion is tracked per
+// thread (commit / wait groups, or an mbarrier arrival).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>

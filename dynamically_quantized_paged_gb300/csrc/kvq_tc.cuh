@@ -81,14 +81,30 @@ __device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive(uint32_t a) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
 }
+// Non-blocking test of the phase with the given parity.
 __device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.b32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
         : "r"(a), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Potentially blocking test: the thread may be suspended until the phase
+// completes or about SUSPEND_NS have passed (rather than for a system-defined
+// time), which bounds the polling of a long wait.
+constexpr uint32_t SUSPEND_NS = 1000000;
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(a), "r"(parity), "r"(SUSPEND_NS)
         : "memory");
     return done != 0;
 }
@@ -97,7 +113,7 @@ __device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, unsigned* err) {
     const uint64_t t0 = globaltimer();
-    while (!mbar_test(a, parity)) {
+    while (!mbar_try(a, parity)) {
         if (globaltimer() - t0 > WAIT_LIMIT_NS) {
             flag_error(err, ERR_TIMEOUT);
             return false;
@@ -470,8 +486,6 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
         // NPW, ... of the tile (a single warp's 16-byte copies cannot keep up
         // with the consumers); the last warp also copies a piece's query rows.
         const int pw = warp - C::PR_WARP0;
-        const uint64_t pol_kv = l2_evict_first_policy();  // pages are read once
-        const uint64_t pol_q = l2_evict_normal_policy();
         TileIter it;
         it.begin(plan, prefix, p);
         // page id of this lane's unit of tile t2 (lane < units of the tile),
@@ -499,7 +513,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                 const uint8_t* qsrc =
                     reinterpret_cast<const uint8_t*>(p.q + ((int64_t)pc.b * p.Hq + (int64_t)pc.h * G) * D);
                 constexpr int NQ = G * D * 2 / 16;
-                for (int c = lane; c < NQ; c += 32) cp_async16(st + C::RQ + 16 * c, qsrc + 16 * c, pol_q);
+                for (int c = lane; c < NQ; c += 32) cp_async16(st + C::RQ + 16 * c, qsrc + 16 * c);
             }
             // units whose page id lies outside the pool are not copied (every
             // warp sees the whole mask; warp 0 publishes it)
@@ -518,8 +532,8 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                     const int c = k * 32 + lane;
                     if (NC % 32 == 0 || c < NC) {
                         const int L = uu * NC + c;  // chunk index within the tile (row-major)
-                        cp_async16(st + C::RK + 16 * swz(L), kc + 16 * c, pol_kv);
-                        cp_async16(st + C::RV + 16 * swz(L), vc + 16 * c, pol_kv);
+                        cp_async16(st + C::RK + 16 * swz(L), kc + 16 * c);
+                        cp_async16(st + C::RV + 16 * swz(L), vc + 16 * c);
                     }
                 }
                 constexpr int NS16 = UNIT * C::MB / 16;  // 16-byte chunks of one scale (or zero) run
@@ -532,7 +546,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                 else if (C::INT4 && which == 3) { src = p.c.v_zeros; dst = C::RVZ; }
                 if (src)
                     cp_async16(st + dst + uu * UNIT * C::MB + 16 * part,
-                               static_cast<const uint8_t*>(src) + row * C::MB + 16 * part, pol_kv);
+                               static_cast<const uint8_t*>(src) + row * C::MB + 16 * part);
             }
             if (pw == 0 && lane == 0) {
                 sm.stage_bad()[s] = bad;
