@@ -31,8 +31,8 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-INT8, FP8, INT4 = 1, 2, 3
-SCHEME_IDS = {"int8": INT8, "fp8": FP8, "int4": INT4}
+INT8, FP8, INT4, INT4SYM = 1, 2, 3, 4
+SCHEME_IDS = {"int8": INT8, "fp8": FP8, "int4": INT4, "int4sym": INT4SYM}
 
 
 def build(force: bool = False) -> str:
@@ -168,9 +168,10 @@ def unpack_int4sym(packed: np.ndarray) -> np.ndarray:
 class OracleCache:
     """Host image of one layer's paged quantized cache (numpy arrays).
 
-    Layout: codes [page][kv_head][page_size][head_dim] (INT4: head_dim/2 bytes,
-    two codes per byte), scales [page][kv_head][page_size] fp32 (INT4: fp16
-    bits [..][head_dim/group], plus zeros of the same shape)."""
+    Layout: codes [page][kv_head][page_size][head_dim] (INT4 and symmetric
+    INT4: head_dim/2 bytes, two codes per byte), scales [page][kv_head]
+    [page_size] fp32 (INT4: fp16 bits [..][head_dim/group], plus zeros of the
+    same shape; symmetric INT4: fp32 [..][head_dim/group], no zeros)."""
 
     def __init__(self, scheme: str, num_pages: int, page_size: int, num_kv_heads: int,
                  head_dim: int, group: int = 32):
@@ -178,12 +179,17 @@ class OracleCache:
         self.sid = SCHEME_IDS[scheme]
         self.num_pages, self.page_size = num_pages, page_size
         self.num_kv_heads, self.head_dim = num_kv_heads, head_dim
-        self.group = group if scheme == "int4" else 0
+        self.group = group if scheme in ("int4", "int4sym") else 0
         rows = num_pages * num_kv_heads * page_size
-        cb = head_dim // 2 if scheme == "int4" else head_dim
+        cb = head_dim // 2 if scheme in ("int4", "int4sym") else head_dim
         self.k_codes = np.zeros(rows * cb, np.uint8)
         self.v_codes = np.zeros(rows * cb, np.uint8)
-        if scheme == "int4":
+        if scheme == "int4sym":
+            ng = head_dim // group
+            self.k_scales = np.zeros(rows * ng, np.float32)
+            self.v_scales = np.zeros(rows * ng, np.float32)
+            self.k_zeros = self.v_zeros = None
+        elif scheme == "int4":
             ng = head_dim // group
             self.k_scales = np.zeros(rows * ng, np.uint16)
             self.v_scales = np.zeros(rows * ng, np.uint16)
@@ -252,4 +258,6 @@ def scale_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int, sch
     """Scale (and zero-point) overhead per token over all layers."""
     if scheme == "int4":
         return 2 * num_layers * num_kv_heads * (head_dim // group) * (2 + 2)
+    if scheme == "int4sym":
+        return 2 * num_layers * num_kv_heads * (head_dim // group) * 4
     return 2 * num_layers * num_kv_heads * 4

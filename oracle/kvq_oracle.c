@@ -36,9 +36,9 @@
  * by the scale; FP8-E4M3 uses qmax = 448 (largest finite E4M3) and
  * round-to-nearest-even with saturation; INT4 is asymmetric over groups of 32
  * channels with an fp16 zero-point rounded down from the group minimum and an
- * fp16 scale rounded up from (max - zero) / 15; symmetric INT4 (a row
- * function only, for the scheme the library adds next) uses groups of 32,
- * an fp32 scale max|x| / 7 and two's-complement nibbles; attention is exact fp64 over
+ * fp16 scale rounded up from (max - zero) / 15; symmetric INT4 uses groups
+ * of 32, an fp32 scale max|x| / 7 and two's-complement nibbles; attention is
+ * exact fp64 over
  * the dequantized cache with softmax scale 1/sqrt(head_dim) and query head g
  * reading KV head g / (Hq / Hkv).
  *
@@ -55,7 +55,7 @@
 #endif
 
 /* ---- scheme ids (the oracle's own copy of the numbering) ----------------- */
-enum { ORC_INT8 = 1, ORC_FP8 = 2, ORC_INT4 = 3 };
+enum { ORC_INT8 = 1, ORC_FP8 = 2, ORC_INT4 = 3, ORC_INT4SYM = 4 };
 
 /* ---- number formats, from their definitions ------------------------------ */
 
@@ -259,8 +259,7 @@ void orc_quant_int4_row(const uint16_t* x, int n, int group, uint8_t* packed,
  * and the code is the half-to-even rounding of the IEEE fp32 quotient x /
  * scale, which lies in [-7, 7] by construction (clamped all the same).  Codes
  * are stored as 4-bit two's complement, two per byte, the even channel in
- * the low nibble.  (A scheme the pages name; the library's kernels do not
- * implement it yet.) */
+ * the low nibble.  Dequantization: code * scale. */
 void orc_quant_int4sym_row(const uint16_t* x, int n, int group, uint8_t* packed, float* scales) {
     int ngroups = n / group;
     int8_t q[1024];
@@ -293,6 +292,8 @@ void orc_quant_int4sym_row(const uint16_t* x, int n, int group, uint8_t* packed,
  *   INT4:           codes  [page][kv_head][page_size][head_dim/2] 2 codes/B
  *                   scales, zeros [page][kv_head][page_size][head_dim/group]
  *                                                                 fp16 bits
+ *   symmetric INT4: codes as INT4 (two's-complement nibbles)
+ *                   scales [page][kv_head][page_size][head_dim/group] fp32
  * A token at physical slot `slot` lives in page slot / page_size at offset
  * slot % page_size. */
 typedef struct {
@@ -301,7 +302,7 @@ typedef struct {
 } orc_cache;
 
 static int64_t row_code_bytes(const orc_cache* c) {
-    return c->scheme == ORC_INT4 ? c->head_dim / 2 : c->head_dim;
+    return (c->scheme == ORC_INT4 || c->scheme == ORC_INT4SYM) ? c->head_dim / 2 : c->head_dim;
 }
 
 /* Quantize-append: token t's K and V rows ([T][Hkv][D] bf16) are quantized
@@ -329,6 +330,10 @@ int orc_append(const orc_cache* c, const int64_t* slot_mapping, const uint16_t* 
                 } else if (c->scheme == ORC_FP8) {
                     float* sc = (float*)(kv == 0 ? c->k_scales : c->v_scales) + row;
                     orc_quant_fp8_row(x, D, codes, sc);
+                } else if (c->scheme == ORC_INT4SYM) {
+                    int ng = D / c->group;
+                    float* sc = (float*)(kv == 0 ? c->k_scales : c->v_scales) + row * ng;
+                    orc_quant_int4sym_row(x, D, c->group, codes, sc);
                 } else {
                     int ng = D / c->group;
                     uint16_t* sc = (uint16_t*)(kv == 0 ? c->k_scales : c->v_scales) + row * ng;
@@ -352,6 +357,14 @@ static void dequant_row(const orc_cache* c, int kv, int64_t row, double* out) {
     } else if (c->scheme == ORC_FP8) {
         double s = ((const float*)(kv == 0 ? c->k_scales : c->v_scales))[row];
         for (int j = 0; j < D; ++j) out[j] = orc_e4m3_value(codes[j]) * s;
+    } else if (c->scheme == ORC_INT4SYM) {
+        int ng = D / c->group;
+        const float* sc = (const float*)(kv == 0 ? c->k_scales : c->v_scales) + row * ng;
+        for (int j = 0; j < D; ++j) {
+            int nib = (j & 1) ? (codes[j / 2] >> 4) : (codes[j / 2] & 0xf);
+            int code = nib >= 8 ? nib - 16 : nib; /* 4-bit two's complement */
+            out[j] = (double)code * (double)sc[j / c->group];
+        }
     } else {
         int ng = D / c->group;
         const uint16_t* sc = (const uint16_t*)(kv == 0 ? c->k_scales : c->v_scales) + row * ng;

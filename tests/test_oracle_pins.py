@@ -329,9 +329,16 @@ def dense_dequant(cache: oracle.OracleCache, kv: int, rows: np.ndarray) -> np.nd
         c = codes.reshape(-1, D)[rows]
         v = torch.from_numpy(np.ascontiguousarray(c)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
         return v * scales[rows][:, None].astype(np.float64)
-    zeros = cache.k_zeros if kv == 0 else cache.v_zeros
     ng = D // cache.group
     pk = codes.reshape(-1, D // 2)[rows]
+    if cache.scheme == "int4sym":
+        # two's-complement nibbles: int8 arithmetic shift of the nibble placed high
+        lo = (pk << 4).view(np.int8) >> 4
+        hi = pk.view(np.int8) >> 4
+        c = np.stack([lo, hi], axis=-1).reshape(len(rows), D).astype(np.float64)
+        s = scales.reshape(-1, ng)[rows].astype(np.float64)
+        return c * np.repeat(s, cache.group, axis=1)
+    zeros = cache.k_zeros if kv == 0 else cache.v_zeros
     c = np.stack([pk & 15, pk >> 4], axis=-1).reshape(len(rows), D).astype(np.float64)
     s = scales.reshape(-1, ng)[rows].view(np.float16).astype(np.float64)
     z = zeros.reshape(-1, ng)[rows].view(np.float16).astype(np.float64)
@@ -371,7 +378,7 @@ def _build(scheme, lens, Hq, H, D, P, seed, spare=3):
     return w, cache, bt, q
 
 
-@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4"])
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4", "int4sym"])
 def test_decode_matches_brute_force(scheme):
     lens = np.array([1, 17, 40, 0, 33], np.int32)
     w, cache, bt, q = _build(scheme, lens, Hq=8, H=2, D=64, P=16, seed=21)
@@ -425,6 +432,24 @@ def test_decode_closed_forms():
     mean_v = dense_dequant(cache, 1, rows).mean(axis=0)
     np.testing.assert_allclose(got[0, 0], mean_v, rtol=0, atol=1e-13)
     np.testing.assert_allclose(got[0, 1], mean_v, rtol=0, atol=1e-13)
+
+
+def test_int4sym_append_places_rows_of_the_row_function():
+    """The pool holds, at each token's slot and KV head, exactly the codes and
+    scales of the symmetric INT4 row function applied to that row."""
+    lens = np.array([5, 19], np.int32)
+    w, cache, bt, q = _build("int4sym", lens, Hq=4, H=2, D=64, P=16, seed=31)
+    for b, L in enumerate(lens):
+        k, v = inp.kv_rows(w, 0, b, 0, L)
+        for t in range(L):
+            for h in range(2):
+                row = (int(bt[b, t // 16]) * 2 + h) * 16 + t % 16
+                for kv, src in ((0, k), (1, v)):
+                    p, sc = oracle.quant_int4sym_row(src[t, h], 32)
+                    codes = cache.k_codes if kv == 0 else cache.v_codes
+                    scales = cache.k_scales if kv == 0 else cache.v_scales
+                    assert np.array_equal(codes.reshape(-1, 32)[row], p)
+                    assert np.array_equal(scales.reshape(-1, 2)[row], sc)
 
 
 def test_append_skips_negative_slots_and_rejects_out_of_pool():
