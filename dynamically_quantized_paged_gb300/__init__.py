@@ -17,8 +17,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
-INT8, FP8, INT4 = 1, 2, 3
-SCHEMES = {"int8": INT8, "fp8": FP8, "int4": INT4}
+INT8, FP8, INT4, INT4SYM = 1, 2, 3, 4
+SCHEMES = {"int8": INT8, "fp8": FP8, "int4": INT4, "int4sym": INT4SYM}
 
 OK = 0
 STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_SCHEME_MISMATCH",
@@ -124,7 +124,7 @@ class PagedKVCache:
         self.sid = SCHEMES[scheme]
         self.num_pages, self.page_size = num_pages, page_size
         self.num_kv_heads, self.head_dim = num_kv_heads, head_dim
-        self.group = 32 if scheme == "int4" else 0
+        self.group = 32 if scheme in ("int4", "int4sym") else 0
         cb, sb, zb = cache_bytes(scheme, num_pages, page_size, num_kv_heads, head_dim)
         alloc = torch.zeros if zero_init else torch.empty
         self.k_codes = alloc(cb, dtype=torch.uint8, device=device)
@@ -143,7 +143,7 @@ class PagedKVCache:
         """Host copy of the K or V codes (which = "k" or "v") as
         uint8 [num_pages][num_kv_heads][page_size][code bytes per token]."""
         t = (self.k_codes if which == "k" else self.v_codes).cpu().numpy()
-        cb = self.head_dim // 2 if self.scheme == "int4" else self.head_dim
+        cb = self.head_dim // 2 if self.scheme in ("int4", "int4sym") else self.head_dim
         return t.reshape(self.num_pages, self.num_kv_heads, self.page_size, cb)
 
     @property

@@ -35,12 +35,13 @@ int current_device() {
 
 kvq_status check_cache(const kvq_cache* c) {
     if (!c) return KVQ_ERR_INVALID_ARG;
-    if (c->scheme < KVQ_INT8_SYM_TOKEN || c->scheme > KVQ_INT4_ASYM_G32) return KVQ_ERR_INVALID_ARG;
+    if (c->scheme < KVQ_INT8_SYM_TOKEN || c->scheme > KVQ_INT4_SYM_G32) return KVQ_ERR_INVALID_ARG;
     if (c->num_pages < 1 || c->page_size < 1 || c->num_kv_heads < 1 || c->head_dim < 1)
         return KVQ_ERR_INVALID_ARG;
     if (c->page_size % kvq::UNIT != 0) return KVQ_ERR_UNSUPPORTED;
     if (c->head_dim != 64 && c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
-    if (c->scheme == KVQ_INT4_ASYM_G32 && c->group != 32) return KVQ_ERR_UNSUPPORTED;
+    if ((c->scheme == KVQ_INT4_ASYM_G32 || c->scheme == KVQ_INT4_SYM_G32) && c->group != 32)
+        return KVQ_ERR_UNSUPPORTED;
     const void* need[4] = {c->k_codes, c->v_codes, c->k_scales, c->v_scales};
     for (const void* p : need)
         if (!p || !aligned(p, 16)) return KVQ_ERR_INVALID_ARG;
@@ -236,13 +237,13 @@ const char* kvq_status_string(kvq_status s) {
 kvq_status kvq_cache_bytes(int32_t scheme, int32_t num_pages, int32_t page_size,
                            int32_t num_kv_heads, int32_t head_dim, size_t* code_bytes,
                            size_t* scale_bytes, size_t* zero_bytes) {
-    if (scheme < KVQ_INT8_SYM_TOKEN || scheme > KVQ_INT4_ASYM_G32) return KVQ_ERR_INVALID_ARG;
+    if (scheme < KVQ_INT8_SYM_TOKEN || scheme > KVQ_INT4_SYM_G32) return KVQ_ERR_INVALID_ARG;
     if (num_pages < 1 || page_size < 1 || num_kv_heads < 1 || head_dim < 1) return KVQ_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
     const size_t rows = (size_t)num_pages * num_kv_heads * page_size;
-    const bool int4 = scheme == KVQ_INT4_ASYM_G32;
-    if (code_bytes) *code_bytes = rows * (int4 ? head_dim / 2 : head_dim);
-    if (scale_bytes) *scale_bytes = rows * (int4 ? (head_dim / 32) * 2 : 4);
+    const bool int4 = scheme == KVQ_INT4_ASYM_G32, int4s = scheme == KVQ_INT4_SYM_G32;
+    if (code_bytes) *code_bytes = rows * (int4 || int4s ? head_dim / 2 : head_dim);
+    if (scale_bytes) *scale_bytes = rows * (int4 ? (head_dim / 32) * 2 : int4s ? (head_dim / 32) * 4 : 4);
     if (zero_bytes) *zero_bytes = int4 ? rows * (head_dim / 32) * 2 : 0;
     return KVQ_OK;
 }
@@ -380,9 +381,9 @@ kvq_status kvq_copy_page(const kvq_cache* cache, int32_t src, int32_t dst, kvq_s
     // every pool is page-major: a page's rows ([Hkv][page_size], any interleave
     // inside) are one contiguous block of the same size in each
     const size_t rows = (size_t)cache->num_kv_heads * cache->page_size;
-    const bool int4 = cache->scheme == KVQ_INT4_ASYM_G32;
-    const size_t code_b = rows * (int4 ? cache->head_dim / 2 : cache->head_dim);
-    const size_t meta_b = rows * (int4 ? (cache->head_dim / 32) * 2 : 4);
+    const bool int4 = cache->scheme == KVQ_INT4_ASYM_G32, int4s = cache->scheme == KVQ_INT4_SYM_G32;
+    const size_t code_b = rows * (int4 || int4s ? cache->head_dim / 2 : cache->head_dim);
+    const size_t meta_b = rows * (int4 ? (cache->head_dim / 32) * 2 : int4s ? (cache->head_dim / 32) * 4 : 4);
     struct Pool { void* base; size_t bytes; } pools[6] = {
         {cache->k_codes, code_b}, {cache->v_codes, code_b}, {cache->k_scales, meta_b},
         {cache->v_scales, meta_b}, {int4 ? cache->k_zeros : nullptr, meta_b},

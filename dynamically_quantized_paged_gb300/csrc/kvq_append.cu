@@ -23,30 +23,55 @@ namespace {
 constexpr int APPEND_THREADS = 256;
 constexpr int APPEND_UNROLL = 4;  // rows per lane group whose loads are issued together
 
-// RNE(fl(x / s)) as an integer, for |x / s| <= 128.  With r = RN(1/s),
+// RNE(fl(x_i / s)) as integers, for |x_i / s| <= 128.  With r = RN(1/s),
 // y = RN(x r) lies within 1.5 * 2^-23 * |x / s| (< 2^-15 here) of fl(x / s),
 // so unless y is within 2^-14 of a half-integer both round to the same
-// integer; near one, the quotient is computed exactly.
-__device__ __forceinline__ int rne_quotient(float x, float s, float r) {
-    const float y = __fmul_rn(x, r);
-    const float c = rintf(y);
-    if (fabsf(__fsub_rn(y, c)) < 0.5f - 0x1p-14f) return (int)c;
-    return __float2int_rn(__fdiv_rn(x, s));
+// integer.  Near one, the quotient is computed exactly; that branch is taken
+// by the whole warp or not at all (it is rare), so that the division is not
+// evaluated for every element.
+template <int N>
+__device__ __forceinline__ void rne_quotients(const float* x, float s, float r, int* q) {
+    bool slow = false;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float y = __fmul_rn(x[i], r);
+        const float c = rintf(y);
+        q[i] = (int)c;
+        slow |= !(fabsf(__fsub_rn(y, c)) < 0.5f - 0x1p-14f);
+    }
+    if (__any_sync(0xffffffffu, slow)) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const float y = __fmul_rn(x[i], r);
+            if (!(fabsf(__fsub_rn(y, rintf(y))) < 0.5f - 0x1p-14f)) q[i] = __float2int_rn(__fdiv_rn(x[i], s));
+        }
+    }
 }
 
-// fl(x / s) where only its E4M3 rounding matters: y = RN(x r) is within 3
+// fl(x_i / s) where only its E4M3 rounding matters: y = RN(x r) is within 3
 // fp32 ulps of fl(x / s); E4M3 rounding (3 mantissa bits) can only differ
 // if y is within a few ulps of a midpoint between E4M3 values (fp32 mantissa
 // bits 19..0 = 0x80000) or in the E4M3 subnormal range; there the exact
-// quotient is used.
-__device__ __forceinline__ float e4m3_quotient(float x, float s, float r) {
-    const float y = __fmul_rn(x, r);
+// quotient is used (a warp-uniform branch, as above).
+__device__ __forceinline__ bool e4m3_needs_exact(float y) {
     const uint32_t bits = __float_as_uint(y);
     const int e = (int)((bits >> 23) & 0xFFu);
     const int low = (int)(bits & 0xFFFFFu);
-    const bool near_mid = abs(low - 0x80000) <= 8;
-    const bool tiny = e < 127 - 6 && y != 0.0f;
-    return (near_mid || tiny) ? __fdiv_rn(x, s) : y;
+    return abs(low - 0x80000) <= 8 || (e < 127 - 6 && y != 0.0f);
+}
+template <int N>
+__device__ __forceinline__ void e4m3_quotients(const float* x, float s, float r, float* y) {
+    bool slow = false;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        y[i] = __fmul_rn(x[i], r);
+        slow |= e4m3_needs_exact(y[i]);
+    }
+    if (__any_sync(0xffffffffu, slow)) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (e4m3_needs_exact(y[i])) y[i] = __fdiv_rn(x[i], s);
+    }
 }
 
 template <int SCHEME, int D>
@@ -64,7 +89,10 @@ __global__ void __launch_bounds__(APPEND_THREADS, 4) append_kernel(AppendParams 
     const int64_t nwarps = ((int64_t)gridDim.x * APPEND_THREADS) >> 5;
     const int64_t stride = nwarps * RPW;
 
-    for (int64_t r0 = warp_id * RPW + lane / LPR; r0 < rows; r0 += stride * APPEND_UNROLL) {
+    // the trip count is the same for every lane of the warp (rows past the
+    // end are carried as invalid), so the warp collectives below see all lanes
+    for (int64_t rb = warp_id * RPW; rb < rows; rb += stride * APPEND_UNROLL) {
+        const int64_t r0 = rb + lane / LPR;
         // issue every load of APPEND_UNROLL rows before using any of them
         int64_t slot[APPEND_UNROLL];
         uint4 raw[APPEND_UNROLL];
@@ -118,34 +146,51 @@ __global__ void __launch_bounds__(APPEND_THREADS, 4) append_kernel(AppendParams 
                 const bool zero_row = (a == 0.0f);
                 const float scale = zero_row ? 1.0f : __fdiv_rn(a, QMAX);
                 const float rcp = __frcp_rn(scale);
+                // (a zero row's x are all +-0: codes 0 with scale 1)
                 uint32_t lo = 0, hi = 0;
-                if (!zero_row) {
-                    if constexpr (SCHEME == KVQ_INT8_SYM_TOKEN) {
-                        uint32_t b[8];
+                if constexpr (SCHEME == KVQ_INT8_SYM_TOKEN) {
+                    int q[8];
+                    rne_quotients<8>(x, scale, rcp, q);
+                    uint32_t b[8];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            int q = rne_quotient(x[i], scale, rcp);
-                            q = max(-127, min(127, q));
-                            b[i] = (uint32_t)(q & 0xFF);
-                        }
-                        lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-                        hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
-                    } else {
-                        uint32_t pr[4];
+                    for (int i = 0; i < 8; ++i) b[i] = (uint32_t)(max(-127, min(127, q[i])) & 0xFF);
+                    lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+                    hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+                } else {
+                    float y[8];
+                    e4m3_quotients<8>(x, scale, rcp, y);
+                    uint32_t pr[4];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float2 y = make_float2(e4m3_quotient(x[2 * i], scale, rcp),
-                                                         e4m3_quotient(x[2 * i + 1], scale, rcp));
-                            pr[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
-                        }
-                        lo = pr[0] | (pr[1] << 16);
-                        hi = pr[2] | (pr[3] << 16);
-                    }
+                    for (int i = 0; i < 4; ++i)
+                        pr[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(y[2 * i], y[2 * i + 1]), __NV_SATFINITE,
+                                                                    __NV_E4M3);
+                    lo = zero_row ? 0u : (pr[0] | (pr[1] << 16));  // a zero row (even of -0) codes +0
+                    hi = zero_row ? 0u : (pr[2] | (pr[3] << 16));
                 }
                 if (valid) {
                     uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * D + li * 8;
                     *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
                     if (li == 0) static_cast<float*>(kv ? p.v_scales : p.k_scales)[prow] = scale;
+                }
+            } else if constexpr (SCHEME == KVQ_INT4_SYM_G32) {  // symmetric INT4, groups of 32 channels = 4 lanes
+                float a = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
+#pragma unroll
+                for (int off = 2; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+                // scale = a / 7 in fp32 (1 for an all-zero group, whose x are
+                // +-0 and so round to code 0 as well); |x / scale| <= 7
+                const float sc = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 7.0f);
+                const float rcp = __frcp_rn(sc);
+                int q[8];
+                rne_quotients<8>(x, sc, rcp, q);
+                uint32_t packed = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) packed |= ((uint32_t)max(-7, min(7, q[i])) & 0xFu) << (4 * i);
+                if (valid) {
+                    uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * (D / 2) + li * 4;
+                    *reinterpret_cast<uint32_t*>(dst) = packed;
+                    if ((li & 3) == 0) static_cast<float*>(kv ? p.v_scales : p.k_scales)[prow * (D / 32) + li / 4] = sc;
                 }
             } else {  // INT4 asymmetric, groups of 32 channels = 4 lanes
                 float mn = x[0], mx = x[0];
@@ -165,13 +210,14 @@ __global__ void __launch_bounds__(APPEND_THREADS, 4) append_kernel(AppendParams 
                 if (__half2float(sh) == 0.0f) sh = __float2half(1.0f);
                 const float sf = __half2float(sh);
                 const float rcp = __frcp_rn(sf);
+                float d[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) d[i] = __fsub_rn(x[i], zf);
+                int q[8];
+                rne_quotients<8>(d, sf, rcp, q);
                 uint32_t packed = 0;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    int q = rne_quotient(__fsub_rn(x[i], zf), sf, rcp);
-                    q = max(0, min(15, q));
-                    packed |= (uint32_t)q << (4 * i);
-                }
+                for (int i = 0; i < 8; ++i) packed |= (uint32_t)max(0, min(15, q[i])) << (4 * i);
                 if (valid) {
                     uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * (D / 2) + li * 4;
                     *reinterpret_cast<uint32_t*>(dst) = packed;
@@ -229,10 +275,12 @@ cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaS
     if (head_dim == 128) {
         if (scheme == KVQ_INT8_SYM_TOKEN) return launch_append_t<KVQ_INT8_SYM_TOKEN, 128>(p, s);
         if (scheme == KVQ_FP8E4M3_TOKEN) return launch_append_t<KVQ_FP8E4M3_TOKEN, 128>(p, s);
+        if (scheme == KVQ_INT4_SYM_G32) return launch_append_t<KVQ_INT4_SYM_G32, 128>(p, s);
         return launch_append_t<KVQ_INT4_ASYM_G32, 128>(p, s);
     }
     if (scheme == KVQ_INT8_SYM_TOKEN) return launch_append_t<KVQ_INT8_SYM_TOKEN, 64>(p, s);
     if (scheme == KVQ_FP8E4M3_TOKEN) return launch_append_t<KVQ_FP8E4M3_TOKEN, 64>(p, s);
+    if (scheme == KVQ_INT4_SYM_G32) return launch_append_t<KVQ_INT4_SYM_G32, 64>(p, s);
     return launch_append_t<KVQ_INT4_ASYM_G32, 64>(p, s);
 }
 

@@ -253,13 +253,18 @@ template <int SCHEME, int D, int G>
 struct Cfg {
     static constexpr bool INT8 = SCHEME == KVQ_INT8_SYM_TOKEN;
     static constexpr bool FP8 = SCHEME == KVQ_FP8E4M3_TOKEN;
-    static constexpr bool INT4 = SCHEME == KVQ_INT4_ASYM_G32;
+    // both INT4 schemes share the 4-bit layout and the group arithmetic; the
+    // symmetric one has fp32 scales, no stored zero-point (zero = -8 scale
+    // once its two's-complement codes are read as offset binary, code ^ 8)
+    static constexpr bool INT4 = SCHEME == KVQ_INT4_ASYM_G32 || SCHEME == KVQ_INT4_SYM_G32;
+    static constexpr bool SYM4 = SCHEME == KVQ_INT4_SYM_G32;
+    static constexpr uint32_t NIBX = SYM4 ? 0x88888888u : 0u;  // XOR taking codes to offset binary
     static constexpr int T = 128;                  // tokens per tile
     static constexpr int TU = T / UNIT;            // 16-token units per tile
     static constexpr int CB = INT4 ? D / 2 : D;    // code bytes per token row
     static constexpr int NCH = CB / 16;            // 16-byte chunks per token row
     static constexpr int NGR = D / 32;             // INT4 groups per row
-    static constexpr int MB = INT4 ? NGR * 2 : 4;  // bytes per token in one scale (or zero) array
+    static constexpr int MB = INT4 ? NGR * (SYM4 ? 4 : 2) : 4;  // bytes per token in one scale (or zero) array
     // scores MMA columns: INT8 hi | lo per head; FP8 one per head; INT4 hi | lo per (group, head)
     static constexpr int NS_USED = INT8 ? 2 * G : (INT4 ? 2 * NGR * G : G);
     static constexpr int NS = NS_USED <= 16 ? 16 : NS_USED;
@@ -286,8 +291,8 @@ struct Cfg {
     static constexpr int RKS = RV + T * CB;
     static constexpr int RVS = RKS + T * MB;
     static constexpr int RKZ = RVS + T * MB;
-    static constexpr int RVZ = RKZ + (INT4 ? T * MB : 0);
-    static constexpr int RQ = RVZ + (INT4 ? T * MB : 0);
+    static constexpr int RVZ = RKZ + (INT4 && !SYM4 ? T * MB : 0);
+    static constexpr int RQ = RVZ + (INT4 && !SYM4 ? T * MB : 0);
     static constexpr int STAGE = RQ + G * D * 2;
     // operand buffers: V^T (128 channel rows x T tokens, fp16, MN-major:
     // (c, t) at (c/8)*VS_SBO + (t/8)*128 + (t%8)*16 + (c%8)*2), the query
@@ -542,8 +547,8 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                 int dst = 0;
                 if (which == 0) { src = p.c.k_scales; dst = C::RKS; }
                 else if (which == 1) { src = p.c.v_scales; dst = C::RVS; }
-                else if (C::INT4 && which == 2) { src = p.c.k_zeros; dst = C::RKZ; }
-                else if (C::INT4 && which == 3) { src = p.c.v_zeros; dst = C::RVZ; }
+                else if (C::INT4 && !C::SYM4 && which == 2) { src = p.c.k_zeros; dst = C::RKZ; }
+                else if (C::INT4 && !C::SYM4 && which == 3) { src = p.c.v_zeros; dst = C::RVZ; }
                 if (src)
                     cp_async16(st + dst + uu * UNIT * C::MB + 16 * part,
                                static_cast<const uint8_t*>(src) + row * C::MB + 16 * part);
@@ -725,7 +730,15 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                 }
             }
             // this token's scales
-            if constexpr (C::INT4) {
+            if constexpr (C::SYM4) {
+#pragma unroll
+                for (int r = 0; r < C::NGR; ++r) {
+                    ks_n[r] = reinterpret_cast<const float*>(st + C::RKS)[t * C::NGR + r];
+                    vs_n[r] = reinterpret_cast<const float*>(st + C::RVS)[t * C::NGR + r];
+                    kz_n[r] = -8.0f * ks_n[r];  // exact
+                    vz_n[r] = -8.0f * vs_n[r];
+                }
+            } else if constexpr (C::INT4) {
 #pragma unroll
                 for (int r = 0; r < C::NGR; ++r) {
                     ks_n[r] = __half2float(reinterpret_cast<const __half*>(st + C::RKS)[t * C::NGR + r]);
@@ -746,7 +759,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
 #pragma unroll
                 for (int cc = 0; cc < CPS; ++cc) {
                     const uint4 raw = *reinterpret_cast<const uint4*>(st + C::RK + 16 * swz(t * C::NCH + c0 + cc));
-                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                    const uint32_t w4[4] = {raw.x ^ C::NIBX, raw.y ^ C::NIBX, raw.z ^ C::NIBX, raw.w ^ C::NIBX};
                     if constexpr (C::INT8) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k) s8x4_to_h2x2(w4[k], r[cc * 8 + 2 * k], r[cc * 8 + 2 * k + 1]);
@@ -983,7 +996,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c) {
                 const uint4 raw = *reinterpret_cast<const uint4*>(st + C::RV + 16 * swz(ct * C::NCH + c));
-                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                const uint32_t w4[4] = {raw.x ^ C::NIBX, raw.y ^ C::NIBX, raw.z ^ C::NIBX, raw.w ^ C::NIBX};
                 if constexpr (C::INT4) {
                     // 32 channels (one group): 4 blocks of 8
 #pragma unroll

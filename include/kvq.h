@@ -69,7 +69,12 @@ typedef enum kvq_scheme {
      * group minimum, scale = fp16 round-up of (max - zero) / 15 (1.0 if that
      * is 0), code = round-half-even((x - zero) / scale) in [0, 15], two codes
      * per byte, even channel in the low nibble. */
-    KVQ_INT4_ASYM_G32 = 3
+    KVQ_INT4_ASYM_G32 = 3,
+    /* per (token, KV head, 32-channel group): scale = max|x| / 7 (fp32; 1.0
+     * for an all-zero group), code = round-half-even(x / scale) in [-7, 7],
+     * stored as 4-bit two's complement, two codes per byte, even channel in
+     * the low nibble; no zero-point ([P1] with bits = 4). */
+    KVQ_INT4_SYM_G32 = 4
 } kvq_scheme;
 
 /* One layer of the paged quantized cache ([P1] section "Integrating Dynamic
@@ -78,10 +83,11 @@ typedef enum kvq_scheme {
  * Optimization": 16 tokens per block by default).  All six pools are
  * caller-owned device memory, sized by kvq_cache_bytes.  Layout:
  *   codes   [num_pages][num_kv_heads][page_size][head_dim]    int8 / e4m3
- *           [num_pages][num_kv_heads][page_size][head_dim/2]  INT4 (packed)
+ *           [num_pages][num_kv_heads][page_size][head_dim/2]  both INT4 (packed)
  *   scales  [num_pages][num_kv_heads][page_size]              fp32
- *           [num_pages][num_kv_heads][page_size][head_dim/32] fp16 (INT4)
- *   zeros   INT4 only, same shape as its scales; NULL otherwise.
+ *           [num_pages][num_kv_heads][page_size][head_dim/32] fp16 (INT4 asym)
+ *           [num_pages][num_kv_heads][page_size][head_dim/32] fp32 (INT4 sym)
+ *   zeros   asymmetric INT4 only, same shape as its scales; NULL otherwise.
  * The token stored at physical slot s lives in page s / page_size at
  * offset s % page_size.  Supported: head_dim 64 or 128, page_size a positive
  * multiple of 16, num_kv_heads >= 1.  Several layers share one block table
@@ -92,7 +98,7 @@ typedef struct kvq_cache {
     int32_t page_size;    /* tokens per page */
     int32_t num_kv_heads;
     int32_t head_dim;
-    int32_t group;        /* channels per INT4 group: must be 32; ignored otherwise */
+    int32_t group;        /* channels per INT4 group (both INT4 schemes): must be 32; ignored otherwise */
     void* k_codes;
     void* v_codes;
     void* k_scales;

@@ -45,7 +45,7 @@ import torch
 class Workload:
     cid: int
     name: str
-    scheme: str              # "int8" | "fp8" | "int4"
+    scheme: str              # "int8" | "fp8" | "int4" | "int4sym"
     layers: int
     batch: int
     q_heads: int

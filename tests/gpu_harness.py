@@ -92,8 +92,8 @@ class Case:
         """Bit-exact comparison of codes, scales (and zeros).  full=True compares
         the whole pools (unwritten rows are zero on both sides)."""
         w = self.w
-        cb = w.head_dim // 2 if w.scheme == "int4" else w.head_dim
-        mb = (w.head_dim // 32) * 2 if w.scheme == "int4" else 4
+        cb = w.head_dim // 2 if w.scheme in ("int4", "int4sym") else w.head_dim
+        mb = {"int4": (w.head_dim // 32) * 2, "int4sym": (w.head_dim // 32) * 4}.get(w.scheme, 4)
         names = ["k_codes", "v_codes", "k_scales", "v_scales"] + (["k_zeros", "v_zeros"] if w.scheme == "int4" else [])
         rows = None if full else self.used_rows()
         for name in names:

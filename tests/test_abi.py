@@ -40,7 +40,7 @@ def test_status_strings():
     assert kvq.status_string(99) == "unknown status"
 
 
-@pytest.mark.parametrize("scheme,bits", [("int8", 8), ("fp8", 8), ("int4", 4)])
+@pytest.mark.parametrize("scheme,bits", [("int8", 8), ("fp8", 8), ("int4", 4), ("int4sym", 4)])
 def test_cache_bytes_match_printed_bytes_per_token(scheme, bits):
     # 80 layers, 8 KV heads, head_dim 128: K+V codes per token
     code, scale, zero = kvq.cache_bytes(scheme, 3, 16, 8, 128)

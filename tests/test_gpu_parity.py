@@ -65,6 +65,20 @@ def test_workload4_int4_eight_layers():
         torch.cuda.empty_cache()
 
 
+def test_int4sym_eight_layer_shapes():
+    """The 8-layer INT4 workload's shapes (16 x 32768 tokens, Hq 32 / Hkv 8,
+    d 128, page 32) under symmetric INT4, one layer: whole pools bit-exact,
+    attention on three sequences."""
+    import dataclasses
+    w = dataclasses.replace(inp.WORKLOADS[4], scheme="int4sym", layers=1)
+    lens = inp.seq_lens(w)
+    case = Case(w, lens)
+    case.compare_cache(full=True)
+    got = case.decode()
+    sample = [0, 7, 15]
+    assert_attn_close(got[sample], case.oracle_decode(seqs=sample), "symmetric INT4, 8-layer shapes")
+
+
 # ------------------------------------------------------------- edge cases
 SHAPES = [  # scheme, Hq, Hkv, D, P
     ("int8", 8, 8, 64, 16), ("int8", 8, 4, 64, 16), ("int8", 16, 4, 128, 32), ("int8", 32, 4, 128, 16),
@@ -74,6 +88,9 @@ SHAPES = [  # scheme, Hq, Hkv, D, P
     ("int8", 16, 16, 128, 16), ("int8", 16, 8, 128, 16), ("int8", 16, 4, 64, 16), ("int8", 32, 4, 64, 16),
     ("fp8", 8, 8, 64, 16), ("fp8", 16, 8, 128, 16), ("fp8", 32, 8, 64, 16), ("fp8", 64, 8, 64, 16),
     ("int4", 8, 8, 64, 16), ("int4", 32, 16, 128, 16), ("int4", 32, 8, 64, 16), ("int4", 64, 8, 64, 16),
+    # symmetric INT4: every (head_dim, GQA ratio) instantiation
+    ("int4sym", 8, 8, 128, 16), ("int4sym", 8, 8, 64, 32), ("int4sym", 16, 8, 128, 16), ("int4sym", 16, 8, 64, 16),
+    ("int4sym", 16, 4, 128, 32), ("int4sym", 32, 8, 64, 16), ("int4sym", 64, 8, 128, 16), ("int4sym", 32, 4, 64, 16),
 ]
 
 
@@ -144,6 +161,13 @@ def _tie_rows(scheme, D):
         f[:, 0] = 448.0
         f[:, 1:] = np.resize(np.concatenate([mids, -mids]), D - 1)
         f[3] = 0.0
+    elif scheme == "int4sym":  # group absmax 7 -> scale 1: x.5 ties
+        f[:] = np.resize((np.arange(2 * D) % 14 - 7) + 0.5, (4, D))
+        f[:, ::32] = 7.0
+        f[1, ::32] = -7.0                                      # negative absmax
+        f[2, :32] = 0.0                                        # an all-zero group
+        f[2, 32:64] = np.float32(2.0 ** -30) * (np.arange(32) % 7 - 3)  # a tiny group
+        f[3] = 0.0                                             # an all-zero row
     else:                      # INT4: constant groups, tiny minima, exact ties
         f[0] = 0.5
         f[1] = np.tile(np.concatenate([[-1.5, 6.0, 0.0, 0.25, 0.75, 1.25], np.full(26, 2.0)]), D // 32)
@@ -152,7 +176,7 @@ def _tie_rows(scheme, D):
     return inp.to_bf16_bits(f)
 
 
-@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4"])
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4", "int4sym"])
 def test_tie_breaking_and_zero_rows_bit_exact(scheme):
     D, H = 128, 2
     w = small(scheme, 4, H, D, 16)
@@ -308,7 +332,7 @@ def quotient_sweep_rows(D=128):
     return np.concatenate(rows)
 
 
-@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4"])
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4", "int4sym"])
 def test_append_quotient_sweep_bit_exact(scheme):
     """The append divides by the scale with a fast reciprocal product and
     falls back to the exact IEEE quotient only near a rounding midpoint.
@@ -336,7 +360,7 @@ def test_append_quotient_sweep_bit_exact(scheme):
         assert bad.size == 0, f"{scheme} {name}: {bad.size} bytes differ, first at {bad[:5]}"
 
 
-@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4"])
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4", "int4sym"])
 def test_shared_prefix_pages_with_copy_on_write(scheme):
     """Sequence B reuses the pages of sequence A's first 100 tokens (six full
     pages shared through the allocator's reference counts); the page where
