@@ -5,7 +5,9 @@ the step's new tokens (kvq_append) and split-K fused-dequant decode attention
 with its merge (kvq_decode_attn: one launch), for every layer of the
 workload.  Pages come from the library's host allocator (scattered ids).
 Inputs are resident in HBM when the timed region starts; L2 is flushed (a
-256 MB write) before every timed step, outside the timed events.
+256 MB write, then a 256 MB read that evicts the write's dirty lines, so their
+write-back does not run under the timed kernels) before every timed step,
+outside the timed events.
 
 Headline workload (N=1 default): the largest single-GPU configuration, the
 8-layer INT4 workload -- 16 sequences x 32768 cached tokens, 32 query / 8 KV
@@ -338,11 +340,19 @@ class Bench:
         self.out = torch.empty((B, w.q_heads, w.head_dim), dtype=torch.float32, device=dev)
         self.ws = kvq.alloc_workspace(self.caches[0], B, w.q_heads, self.max_pages, device=dev)
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.flush_read = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
         torch.cuda.synchronize(dev)
         st = kvq.last_device_error()
         if st != kvq.OK:
             raise RuntimeError(f"set-up failed: {kvq.status_string(st)}")
         self.launches_per_step = 2 * w.layers  # quantize-append + fused decode per layer
+
+    def flush_l2(self):
+        """Evict the step's data from L2: write a buffer larger than L2, then
+        read another one, so that the dirty lines of the write are written
+        back during the flush rather than while the timed kernels run."""
+        self.flush.zero_()
+        self.flush_sink = self.flush_read.sum()
 
     def step(self, events=None, q=None, k_new=None, v_new=None, slots=None, bt=None, lens=None, out=None,
              stream=None):
@@ -367,7 +377,7 @@ class Bench:
         """--steps eager steps after --warmup: per-step events."""
         torch = self.torch
         for _ in range(warmup):
-            self.flush.zero_()
+            self.flush_l2()
             self.step()
         torch.cuda.synchronize(self.dev)
         st = self.kvq.last_device_error()
@@ -378,7 +388,7 @@ class Bench:
         barrier()
         torch.cuda.synchronize(self.dev)
         for i in range(steps):
-            self.flush.zero_()
+            self.flush_l2()
             ev[i][0].record()
             self.step()
             ev[i][1].record()
@@ -401,7 +411,7 @@ class Bench:
         with torch.cuda.graph(graph, stream=stream):
             self.step(stream=stream)
         for _ in range(warmup):
-            self.flush.zero_()
+            self.flush_l2()
             graph.replay()
         torch.cuda.synchronize(self.dev)
         E = torch.cuda.Event
@@ -410,7 +420,7 @@ class Bench:
         torch.cuda.synchronize(self.dev)
         t0 = time.perf_counter()
         for i in range(steps):
-            self.flush.zero_()
+            self.flush_l2()
             evs[i][0].record()
             graph.replay()
             evs[i][1].record()
@@ -433,7 +443,7 @@ class Bench:
         t0 = time.perf_counter()
         while True:
             for i in range(batch):
-                self.flush.zero_()
+                self.flush_l2()
                 self.step(events=evs[i])
             torch.cuda.synchronize(self.dev)
             for row in evs:
@@ -473,13 +483,13 @@ class Bench:
             h_out.copy_(self.out, non_blocking=True)
 
         for _ in range(warmup):
-            self.flush.zero_()
+            self.flush_l2()
             one()
         torch.cuda.synchronize(self.dev)
         E = torch.cuda.Event
         evs = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(steps)]
         for i in range(steps):
-            self.flush.zero_()
+            self.flush_l2()
             evs[i][0].record()
             one()
             evs[i][1].record()
@@ -489,7 +499,7 @@ class Bench:
     def close(self):
         self.graph = None
         self.caches, self.q, self.k_new, self.v_new = [], [], [], []
-        self.ws = self.flush = self.out = None
+        self.ws = self.flush = self.flush_read = self.out = None
         self.alloc.close()
         self.torch.cuda.empty_cache()
 
@@ -556,7 +566,7 @@ def measure_workload(w, dev, local_rank, args, world, rank, barrier, headline: b
         "steps": steps,
         "config": {"workload": describe(w), "batch": w.batch, "layers": w.layers,
                    "cached_tokens": int(inp.seq_lens(w).sum()), "kv_codes": w.scheme,
-                   "l2": "flushed before every timed step (256 MB write, outside the timed events)",
+                   "l2": "flushed before every timed step (256 MB write, then a 256 MB read, outside the timed events)",
                    "parallelism": (f"sequences partitioned over {world} GPUs, no collective" if world > 1
                                    else "1 GPU")},
         "hbm_frac_of_8tbs": round(job_throughput(total_step, ms_per_step) / NOMINAL_HBM_GBS / max(world, 1), 4),
@@ -664,6 +674,9 @@ def main(argv=None):
                     help="wall seconds of oracle work for each cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi during the timed region")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling runs only: override the workload's layer count (the per-launch work is "
+                         "per layer; the JSON line names the layers it ran)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the eager launches only (default: the step is also replayed from a CUDA graph "
                          "and that time is the headline value)")
@@ -675,6 +688,9 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     w = inp.WORKLOADS[args.config]
+    if args.layers > 0:
+        import dataclasses
+        w = dataclasses.replace(w, layers=args.layers)
 
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
