@@ -44,6 +44,10 @@ struct AppendParams {
     int64_t num_slots;  // num_pages * page_size
     int num_tokens, num_kv_heads, page_size;
     unsigned* err;
+    // n / num_kv_heads and n / page_size for 0 <= n < 2^31 as
+    // (n * mul) >> shift (filled in by launch_append)
+    uint64_t heads_mul, page_mul;
+    int heads_shift, page_shift;
 };
 
 struct DecodeParams {

@@ -193,6 +193,41 @@ def test_tie_breaking_and_zero_rows_bit_exact(scheme):
     assert_attn_close(case.decode(), case.oracle_decode(), scheme)
 
 
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4", "int4sym"])
+def test_tiny_magnitude_rows_bit_exact(scheme):
+    """Rows (and 32-channel groups) whose largest magnitude is tiny, down to
+    the smallest bf16 subnormal: the reciprocal of such a scale overflows, so
+    the append must take the exact quotient; codes and scales equal the
+    oracle's."""
+    D, H, P = 128, 1, 16
+    r = np.random.default_rng(41)
+    bits = []
+    for top in (0x0001, 0x0003, 0x0010, 0x007F, 0x0080, 0x0100, 0x0800, 0x0C00):  # subnormals .. ~1e-36
+        for _ in range(4):
+            row = r.integers(0, top + 1, size=D).astype(np.uint16)
+            row[r.integers(0, D)] = top
+            row[r.random(D) < 0.5] |= 0x8000
+            bits.append(row)
+    rows = np.stack(bits)
+    T = rows.shape[0]
+    k = rows.reshape(T, H, D)
+    v = np.ascontiguousarray(k[::-1])
+    slots = np.arange(T, dtype=np.int64)
+    npg = (T + P - 1) // P
+    g = kvq.PagedKVCache(scheme, npg, P, H, D, device=DEV)
+    o = oracle.OracleCache(scheme, npg, P, H, D)
+    kvq.append(g, dev(slots), dev_bits(k), dev_bits(v))
+    assert o.append(slots, k, v) == 0
+    torch.cuda.synchronize()
+    assert kvq.last_device_error() == kvq.OK
+    names = ["k_codes", "v_codes", "k_scales", "v_scales"] + (["k_zeros", "v_zeros"] if scheme == "int4" else [])
+    for name in names:
+        got = g.codes_rowmajor(name[0]).reshape(-1) if "codes" in name else getattr(g, name).cpu().numpy()
+        want = getattr(o, name).view(np.uint8)
+        bad = np.nonzero(got.view(np.uint8) != want)[0]
+        assert bad.size == 0, f"{scheme} {name}: {bad.size} bytes differ, first at {bad[:5]}"
+
+
 # ------------------------------------------------------------- device-side errors
 def test_bad_page_id_is_flagged_not_faulted():
     w = small("int8", 8, 4, 64, 16)
