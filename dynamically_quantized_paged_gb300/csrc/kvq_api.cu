@@ -122,7 +122,8 @@ kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* 
     if (dev < 0) return KVQ_ERR_CUDA;
     const int n_ctas = n_ctas_for(cache, G, B);
     if (n_ctas <= 0) return KVQ_ERR_CUDA;
-    const size_t need = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, B, cache->num_kv_heads);
+    const int warps = kvq::decode_alu_warps(cache->scheme, G);
+    const size_t need = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, B, cache->num_kv_heads, warps);
     if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     unsigned* err = kvq::device_error_word();
     if (!err) return KVQ_ERR_CUDA;
@@ -135,6 +136,15 @@ kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* 
     p.ws_o = static_cast<float*>(workspace);
     p.ws_m = p.ws_o + (size_t)2 * n_ctas * G * cache->head_dim;
     p.ws_l = p.ws_m + (size_t)2 * n_ctas * G;
+    if (warps > 0) {
+        p.wp_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                          kvq::decode_warp_partial_offset(n_ctas, G, cache->head_dim, B,
+                                                                          cache->num_kv_heads));
+        p.wp_m = p.wp_o + (size_t)2 * n_ctas * warps * G * cache->head_dim;
+        p.wp_l = p.wp_m + (size_t)2 * n_ctas * warps * G;
+    } else {
+        p.wp_o = p.wp_m = p.wp_l = nullptr;
+    }
     p.B = B;
     p.Hq = Hq;
     p.max_pages = max_pages;
@@ -307,8 +317,8 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_seqs,
     if (G == 0) return KVQ_ERR_UNSUPPORTED;
     const int n_ctas = n_ctas_for(cache, G, num_seqs);
     if (n_ctas <= 0) return KVQ_ERR_CUDA;
-    *bytes = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, num_seqs,
-                                         cache->num_kv_heads);
+    *bytes = kvq::decode_workspace_bytes(n_ctas, G, cache->head_dim, num_seqs, cache->num_kv_heads,
+                                         kvq::decode_alu_warps(cache->scheme, G));
     return KVQ_OK;
 }
 

@@ -28,16 +28,20 @@ namespace kvq {
 // ---- the split plan ------------------------------------------------------------
 // units_b = ceil(min(seq_len_b, max_pages * page_size) / UNIT); segments
 // (b, h) laid out in (b, h) order; prefix[b] = sum of units_b' for b' < b;
-// U = Hkv * prefix[B]; CTA slice S = max(ceil(U / n_ctas), MIN_SLICE_UNITS).
+// U = Hkv * prefix[B]; with WPC workers per CTA, worker slice
+// Sw = max(ceil(U / (n_ctas * WPC)), MIN_SLICE_UNITS) and CTA slice
+// S = WPC * Sw (the tensor-core kernel: one worker per CTA; the CUDA-core
+// kernel: every warp is a worker).
 struct Plan {
     int B, Hkv;
     int64_t U;
-    int64_t S;   // units per CTA
+    int64_t Sw;  // units per worker
+    int64_t S;   // units per CTA: its workers' slices laid end to end
 };
 
 // All NT threads of the block build the plan: per-sequence unit counts,
 // then their exclusive prefix sums in shared memory (prefix[0..B]).
-template <int NT>
+template <int NT, int WPC = 1>
 __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefix, int64_t* misc) {
     static_assert(NT % 32 == 0 && NT <= 1024, "whole warps");
     constexpr int NW = NT / 32;
@@ -97,8 +101,10 @@ __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefi
     pl.B = B;
     pl.Hkv = p.c.num_kv_heads;
     pl.U = (int64_t)pl.Hkv * misc[0];
-    const int64_t S = (pl.U + p.n_ctas - 1) / p.n_ctas;
-    pl.S = S < MIN_SLICE_UNITS ? MIN_SLICE_UNITS : S;
+    const int64_t workers = (int64_t)p.n_ctas * WPC;
+    const int64_t Sw = (pl.U + workers - 1) / workers;
+    pl.Sw = Sw < MIN_SLICE_UNITS ? MIN_SLICE_UNITS : Sw;
+    pl.S = pl.Sw * WPC;
     return pl;
 }
 

@@ -59,6 +59,9 @@ struct DecodeParams {
     float* ws_o;  // [2 * n_ctas][G][D]
     float* ws_m;  // [2 * n_ctas][G]
     float* ws_l;  // [2 * n_ctas][G]
+    float* wp_o;  // CUDA-core kernel only: per-warp partials [2 * n_ctas * warps][G][D]
+    float* wp_m;  // [2 * n_ctas * warps][G]
+    float* wp_l;  // [2 * n_ctas * warps][G]
     int B, Hq, max_pages;
     int n_ctas;
     float q_scale;  // softmax scale * log2(e), folded into q
@@ -68,10 +71,21 @@ struct DecodeParams {
     unsigned long long* seg_ctr;        // [B * Hkv] arrival counters: (gen << 32) | arrivals
 };
 
+// The CUDA-core kernel (kvq_alu.cuh) serves GQA ratios up to 4 of the INT8,
+// FP8 and asymmetric INT4 schemes, the tensor-core kernel (kvq_tc.cuh) the
+// rest; decode_alu_warps gives the former's warps per CTA, 0 for the latter.
+inline int decode_alu_warps(int scheme, int G) {
+    const bool alu = G <= 4 && (scheme == KVQ_INT8_SYM_TOKEN || scheme == KVQ_FP8E4M3_TOKEN ||
+                                scheme == KVQ_INT4_ASYM_G32);
+    return alu ? 12 : 0;
+}
+
 // Workspace layout for n_ctas persistent CTAs (two partial slots per CTA):
 // partials o [2 n_ctas][G][D], m [2 n_ctas][G], l [2 n_ctas][G] (fp32); the
 // published plan: int64 U, int64 S, int32 prefix[B + 1]; then (8-byte
-// aligned) one uint64 arrival counter per (sequence, KV head) segment.
+// aligned) one uint64 arrival counter per (sequence, KV head) segment; then,
+// for the CUDA-core kernel of `warps` warps per CTA (16-byte aligned), the
+// warp partials o [2 n_ctas warps][G][D], m and l [2 n_ctas warps][G].
 inline size_t decode_plan_offset(int n_ctas, int G, int D) {
     const size_t slots = 2 * (size_t)n_ctas;
     return slots * G * D * sizeof(float) + 2 * slots * G * sizeof(float);
@@ -80,9 +94,14 @@ inline size_t decode_counter_offset(int n_ctas, int G, int D, int B) {
     const size_t end_plan = decode_plan_offset(n_ctas, G, D) + 16 + ((size_t)B + 1) * sizeof(int32_t);
     return (end_plan + 7) / 8 * 8;
 }
-inline size_t decode_workspace_bytes(int n_ctas, int G, int D, int B, int Hkv) {
+inline size_t decode_warp_partial_offset(int n_ctas, int G, int D, int B, int Hkv) {
     const size_t end = decode_counter_offset(n_ctas, G, D, B) + (size_t)B * Hkv * sizeof(unsigned long long);
     return (end + 15) / 16 * 16;
+}
+inline size_t decode_workspace_bytes(int n_ctas, int G, int D, int B, int Hkv, int warps) {
+    const size_t slots = 2 * (size_t)n_ctas * warps;
+    return decode_warp_partial_offset(n_ctas, G, D, B, Hkv) + slots * G * D * sizeof(float) +
+           2 * slots * G * sizeof(float);
 }
 
 cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaStream_t s);
