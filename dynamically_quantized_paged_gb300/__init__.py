@@ -21,6 +21,7 @@ INT8, FP8, INT4, INT4SYM = 1, 2, 3, 4
 SCHEMES = {"int8": INT8, "fp8": FP8, "int4": INT4, "int4sym": INT4SYM}
 
 OK = 0
+OUT_F32, OUT_BF16 = 0, 1  # kvq_out_dtype
 STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_SCHEME_MISMATCH",
                 3: "KVQ_ERR_OUT_OF_PAGES", 4: "KVQ_ERR_BAD_TABLE", 5: "KVQ_ERR_CUDA",
                 6: "KVQ_ERR_DEVICE_TIMEOUT", 7: "KVQ_ERR_UNSUPPORTED", 8: "KVQ_ERR_WORKSPACE"}
@@ -30,7 +31,7 @@ EXPORTS = ["kvq_status_string", "kvq_cache_bytes", "kvq_append", "kvq_decode_wor
            "kvq_decode_attn", "kvq_decode_partial", "kvq_decode_merge", "kvq_validate_tables",
            "kvq_last_device_error", "kvq_allocator_create", "kvq_allocator_destroy",
            "kvq_alloc_pages", "kvq_free_pages", "kvq_allocator_free_count", "kvq_decode_attn_noalloc",
-           "kvq_share_pages", "kvq_page_refcount", "kvq_copy_page"]
+           "kvq_share_pages", "kvq_page_refcount", "kvq_copy_page", "kvq_decode_attn_out"]
 
 
 class KvqError(RuntimeError):
@@ -62,6 +63,7 @@ def _load() -> ctypes.CDLL:
     L.kvq_decode_workspace_bytes.argtypes = [cachep, i32, i32, i32, sz]
     dec = [cachep, P, P, P, P, i32, i32, i32, ctypes.c_float, P, ctypes.c_size_t, P]
     L.kvq_decode_attn.argtypes = dec
+    L.kvq_decode_attn_out.argtypes = [cachep, P, P, P, P, i32, i32, i32, i32, ctypes.c_float, P, ctypes.c_size_t, P]
     L.kvq_decode_partial.argtypes = dec
     L.kvq_decode_merge.argtypes = dec
     L.kvq_validate_tables.argtypes = [cachep, P, P, i32, i32, P]
@@ -185,16 +187,22 @@ def alloc_workspace(cache: PagedKVCache, num_seqs: int, num_q_heads: int, max_pa
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def _decode_call(fn, name, cache, q, block_table, seq_lens, out, workspace, softmax_scale, stream):
+def _decode_call(fn, name, cache, q, block_table, seq_lens, out, workspace, softmax_scale, stream, bf16_ok=False):
     B = seq_lens.numel()
     if q.dim() != 3 or q.shape[0] != B or q.shape[2] != cache.head_dim or tuple(out.shape) != tuple(q.shape) \
             or block_table.dim() != 2 or block_table.shape[0] != B:
         raise ValueError(f"{name}: shapes q{tuple(q.shape)} out{tuple(out.shape)} "
                          f"block_table{tuple(block_table.shape)} seq_lens[{B}] do not agree")
-    if q.element_size() != 2 or out.dtype != torch.float32 or seq_lens.element_size() != 4 \
-            or block_table.element_size() != 4:
-        raise ValueError(f"{name}: q must be bf16 bits, out fp32, tables int32")
+    out_ok = out.dtype == torch.float32 or (bf16_ok and out.dtype == torch.bfloat16)
+    if q.element_size() != 2 or not out_ok or seq_lens.element_size() != 4 or block_table.element_size() != 4:
+        raise ValueError(f"{name}: q must be bf16 bits, out fp32{' or bf16' if bf16_ok else ''}, tables int32")
     Hq = q.shape[1]
+    if bf16_ok:  # kvq_decode_attn_out: the output dtype rides along
+        dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+        _check(fn(ctypes.byref(cache.struct), _ptr(q), _ptr(block_table), _ptr(seq_lens), _ptr(out), dt, B, Hq,
+                  block_table.shape[1], float(softmax_scale), _ptr(workspace), workspace.numel(),
+                  _stream(stream)), name)
+        return
     _check(fn(ctypes.byref(cache.struct), _ptr(q), _ptr(block_table), _ptr(seq_lens), _ptr(out), B, Hq,
               block_table.shape[1], float(softmax_scale), _ptr(workspace), workspace.numel(),
               _stream(stream)), name)
@@ -203,10 +211,15 @@ def _decode_call(fn, name, cache, q, block_table, seq_lens, out, workspace, soft
 def decode_attn(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
                 seq_lens: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
                 softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
-    """kvq_decode_attn: out[B, Hq, d] (fp32) = paged GQA decode attention of
-    q[B, Hq, d] (bf16) over the quantized cache."""
-    _decode_call(lib.kvq_decode_attn, "kvq_decode_attn", cache, q, block_table, seq_lens, out,
-                 workspace, softmax_scale, stream)
+    """kvq_decode_attn: out[B, Hq, d] = paged GQA decode attention of
+    q[B, Hq, d] (bf16) over the quantized cache; out fp32, or bf16 (through
+    kvq_decode_attn_out: the fp32 result rounded to nearest even)."""
+    if out.dtype == torch.bfloat16:
+        _decode_call(lib.kvq_decode_attn_out, "kvq_decode_attn_out", cache, q, block_table, seq_lens, out,
+                     workspace, softmax_scale, stream, bf16_ok=True)
+    else:
+        _decode_call(lib.kvq_decode_attn, "kvq_decode_attn", cache, q, block_table, seq_lens, out,
+                     workspace, softmax_scale, stream)
     return out
 
 

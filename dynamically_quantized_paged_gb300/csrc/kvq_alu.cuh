@@ -183,8 +183,8 @@ decode_partial_kernel(const DecodeParams p) {
     if (p.fuse_merge) {  // empty sequences get zero rows (no CTA's slice touches them)
         for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
             if (prefix[b + 1] != prefix[b]) continue;
-            float* row = p.out + (int64_t)b * p.Hq * D;
-            for (int i = threadIdx.x; i < p.Hq * D; i += blockDim.x) row[i] = 0.0f;
+            const OutRow row = out_row(p, (int64_t)b * p.Hq * D);
+            for (int i = threadIdx.x; i < p.Hq * D; i += blockDim.x) store_out(row, i, 0.0f);
         }
     }
     uint8_t* ring = smem + C::OFF_STAGES + warp * STAGES_ * C::STAGE;
@@ -779,7 +779,7 @@ decode_partial_kernel(const DecodeParams p) {
             }
         }
         if (pc.whole) {
-            float* row = p.out + ((int64_t)pc.b * p.Hq + (int64_t)pc.h * G) * D;
+            const OutRow row = out_row(p, ((int64_t)pc.b * p.Hq + (int64_t)pc.h * G) * D);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float lg = __shfl_sync(0xffffffffu, l_run, g * C::DUP);  // lane g*DUP holds head g
@@ -787,8 +787,8 @@ decode_partial_kernel(const DecodeParams p) {
                 if (v_tok == 0) {
 #pragma unroll
                     for (int jj = 0; jj < C::VCH; jj += 4)
-                        *reinterpret_cast<float4*>(row + g * D + v_c0 + jj) =
-                            make_float4(o[g][jj] * inv, o[g][jj + 1] * inv, o[g][jj + 2] * inv, o[g][jj + 3] * inv);
+                        store_out4(row, g * D + v_c0 + jj,
+                                   make_float4(o[g][jj] * inv, o[g][jj + 1] * inv, o[g][jj + 2] * inv, o[g][jj + 3] * inv));
                 }
             }
         } else {
@@ -847,7 +847,7 @@ decode_partial_kernel(const DecodeParams p) {
         const int elem = it % NE;
         merge_element<D, G>(p.wp_o, p.wp_m, p.wp_l, e.a, plan.Sw, e.k0, e.n, elem / (D / 4), (elem % (D / 4)) * 4,
                             lane, it < np * NE,
-                            e.slot < 0 ? p.out + ((int64_t)e.b * p.Hq + (int64_t)e.h * G) * D : nullptr,
+                            e.slot < 0 ? out_row(p, ((int64_t)e.b * p.Hq + (int64_t)e.h * G) * D) : no_row(),
                             e.slot < 0 ? nullptr : p.ws_o + (int64_t)e.slot * G * D,
                             e.slot < 0 ? nullptr : p.ws_m + (int64_t)e.slot * G,
                             e.slot < 0 ? nullptr : p.ws_l + (int64_t)e.slot * G);
@@ -877,7 +877,7 @@ decode_partial_kernel(const DecodeParams p) {
             const int64_t k0 = e.a / plan.S, n = (e.a + e.units - 1) / plan.S - k0 + 1;
             merge_element<D, G>(p.ws_o, p.ws_m, p.ws_l, e.a, plan.S, k0, e.slot == -2 ? 0 : (int)n,
                                 elem / (D / 4), (elem % (D / 4)) * 4, lane, it < np * NE && e.slot != -2,
-                                p.out + ((int64_t)e.b * p.Hq + (int64_t)e.h * G) * D, nullptr, nullptr, nullptr);
+                                out_row(p, ((int64_t)e.b * p.Hq + (int64_t)e.h * G) * D), nullptr, nullptr, nullptr);
         }
     }
 }

@@ -101,7 +101,7 @@ int n_ctas_for(const kvq_cache* c, int G, int B) {
 
 // Shared argument checks of the three decode entry points; fills p.
 kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* block_table,
-                          const int32_t* seq_lens, float* out, int32_t B, int32_t Hq,
+                          const int32_t* seq_lens, void* out, int32_t B, int32_t Hq,
                           int32_t max_pages, float softmax_scale, void* workspace,
                           size_t workspace_bytes, kvq::DecodeParams& p, int& G) {
     kvq_status st = check_cache(cache);
@@ -152,6 +152,7 @@ kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* 
     p.q_scale = scale * 1.4426950408889634f;  // log2(e): the kernel works in base 2
     p.err = err;
     p.fuse_merge = 0;
+    p.out_bf16 = 0;
     p.gen = next_generation();
     p.seg_ctr = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) +
                                                       kvq::decode_counter_offset(n_ctas, G, cache->head_dim, B));
@@ -362,6 +363,23 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const int32_t*
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     p.fuse_merge = 1;  // one launch: splits are merged by the CTA that finishes them last
     if (kvq::launch_decode_partial(p, G, s) != cudaSuccess) return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_attn_out(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                               const int32_t* seq_lens, void* out, int32_t out_dtype, int32_t num_seqs,
+                               int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
+                               void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+    if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
+    kvq::DecodeParams p;
+    int G = 0;
+    kvq_status st = prepare_decode(cache, q, block_table, seq_lens, out, num_seqs, num_q_heads,
+                                   max_pages_per_seq, softmax_scale, workspace, workspace_bytes, p, G);
+    if (st != KVQ_OK || num_seqs == 0) return st;
+    p.fuse_merge = 1;
+    p.out_bf16 = out_dtype == KVQ_OUT_BF16;
+    if (kvq::launch_decode_partial(p, G, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KVQ_ERR_CUDA;
     return KVQ_OK;
 }
 

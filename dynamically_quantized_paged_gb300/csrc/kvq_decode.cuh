@@ -25,6 +25,34 @@
 
 namespace kvq {
 
+// ---- final output rows ------------------------------------------------------------
+// A final output row (head g's D values at row + g * D): fp32, or bf16 rounded
+// to nearest even from the same fp32 value.  base == nullptr: no final row.
+struct OutRow {
+    void* base;
+    int bf16;
+};
+__device__ __forceinline__ OutRow out_row(const DecodeParams& p, int64_t elem) {
+    return OutRow{p.out_bf16 ? static_cast<void*>(static_cast<__nv_bfloat16*>(p.out) + elem)
+                             : static_cast<void*>(static_cast<float*>(p.out) + elem),
+                  p.out_bf16};
+}
+__device__ __forceinline__ OutRow no_row() { return OutRow{nullptr, 0}; }
+__device__ __forceinline__ void store_out(const OutRow& r, int64_t i, float v) {
+    if (r.bf16) static_cast<__nv_bfloat16*>(r.base)[i] = __float2bfloat16_rn(v);
+    else static_cast<float*>(r.base)[i] = v;
+}
+// four consecutive values at i (a multiple of 4)
+__device__ __forceinline__ void store_out4(const OutRow& r, int64_t i, float4 v) {
+    if (r.bf16) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(r.base) + i) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(r.base) + i) = v;
+    }
+}
+
 // ---- the split plan ------------------------------------------------------------
 // units_b = ceil(min(seq_len_b, max_pages * page_size) / UNIT); segments
 // (b, h) laid out in (b, h) order; prefix[b] = sum of units_b' for b' < b;
@@ -196,7 +224,7 @@ struct PieceWalk {
 // the same launch.  Every thread of the CTA (NT threads) calls this.
 template <int D, int G, int NT>
 __device__ __forceinline__ void merge_workers(const float* so, const float* sm, const float* sl, int64_t a,
-                                              int64_t S, int64_t k0, int64_t k1, int tid, float* row,
+                                              int64_t S, int64_t k0, int64_t k1, int tid, OutRow row,
                                               float* dst_o, float* dst_m, float* dst_l) {
     constexpr int NE = G * D / 4;                    // float4 elements of the output rows
     constexpr int EPT = (NE + NT - 1) / NT;          // per thread
@@ -266,10 +294,9 @@ __device__ __forceinline__ void merge_workers(const float* so, const float* sm, 
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
         if (eg[k] < 0) continue;
-        if (row) {
+        if (row.base) {
             const float inv = (L[k] > 0.0f) ? 1.0f / L[k] : 0.0f;
-            *reinterpret_cast<float4*>(row + eg[k] * D + ej[k]) =
-                make_float4(O[k].x * inv, O[k].y * inv, O[k].z * inv, O[k].w * inv);
+            store_out4(row, eg[k] * D + ej[k], make_float4(O[k].x * inv, O[k].y * inv, O[k].z * inv, O[k].w * inv));
         } else {
             *reinterpret_cast<float4*>(dst_o + eg[k] * D + ej[k]) = O[k];
             if (ej[k] == 0) {
@@ -289,7 +316,7 @@ __device__ __forceinline__ void merge_workers(const float* so, const float* sm, 
 template <int D, int G>
 __device__ __forceinline__ void merge_element(const float* so, const float* sm, const float* sl, int64_t a,
                                               int64_t S, int64_t k0, int n, int g, int j, int lane, bool active,
-                                              float* row, float* dst_o, float* dst_m, float* dst_l) {
+                                              OutRow row, float* dst_o, float* dst_m, float* dst_l) {
     constexpr int LPH = D / 4 < 32 ? D / 4 : 32;
     constexpr int UNR = 8;
     const int64_t k_start = a / S;
@@ -332,9 +359,9 @@ __device__ __forceinline__ void merge_element(const float* so, const float* sm, 
         }
     }
     if (!active) return;
-    if (row) {
+    if (row.base) {
         const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
-        *reinterpret_cast<float4*>(row + g * D + j) = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+        store_out4(row, g * D + j, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
     } else {
         *reinterpret_cast<float4*>(dst_o + g * D + j) = O;
         if (j == 0) {
@@ -413,14 +440,14 @@ __global__ void __launch_bounds__(MERGE_THREADS) decode_merge_kernel(const Decod
     const int32_t* prefix = reinterpret_cast<const int32_t*>(wsplan + 2);
     const int units = prefix[b + 1] - prefix[b];
     if (units == 0) {
-        float* out = p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D;
-        for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = 0.0f;
+        const OutRow out = out_row(p, ((int64_t)b * p.Hq + (int64_t)h * G) * D);
+        for (int i = threadIdx.x; i < G * D; i += blockDim.x) store_out(out, i, 0.0f);
         return;
     }
     const int64_t a = (int64_t)p.c.num_kv_heads * prefix[b] + (int64_t)h * units;
     if (a / S == (a + units - 1) / S) return;  // finished inside one CTA's slice
     merge_workers<D, G, MERGE_THREADS>(p.ws_o, p.ws_m, p.ws_l, a, S, a / S, (a + units - 1) / S, threadIdx.x,
-                                       p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D, nullptr, nullptr, nullptr);
+                                       out_row(p, ((int64_t)b * p.Hq + (int64_t)h * G) * D), nullptr, nullptr, nullptr);
 }
 
 template <int D, int G>

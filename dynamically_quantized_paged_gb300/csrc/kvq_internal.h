@@ -55,7 +55,7 @@ struct DecodeParams {
     const uint16_t* q;  // bf16 bits [B][Hq][D]
     const int32_t* block_table;
     const int32_t* seq_lens;
-    float* out;
+    void* out;          // [B][Hq][D]: fp32, or bf16 when out_bf16
     float* ws_o;  // [2 * n_ctas][G][D]
     float* ws_m;  // [2 * n_ctas][G]
     float* ws_l;  // [2 * n_ctas][G]
@@ -67,6 +67,7 @@ struct DecodeParams {
     float q_scale;  // softmax scale * log2(e), folded into q
     unsigned* err;
     int fuse_merge;                     // 1: the last CTA of a split segment merges it in place
+    int out_bf16;                       // 1: the output rows are bf16 (round to nearest even), else fp32
     uint32_t gen;                       // call generation tagging the arrival counters
     unsigned long long* seg_ctr;        // [B * Hkv] arrival counters: (gen << 32) | arrivals
 };

@@ -473,8 +473,8 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
     if (p.fuse_merge) {  // empty sequences get zero rows (no CTA's slice touches them)
         for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
             if (prefix[b + 1] != prefix[b]) continue;
-            float* row = p.out + (int64_t)b * p.Hq * D;
-            for (int i = tid; i < p.Hq * D; i += C::THREADS) row[i] = 0.0f;
+            const OutRow row = out_row(p, (int64_t)b * p.Hq * D);
+            for (int i = tid; i < p.Hq * D; i += C::THREADS) store_out(row, i, 0.0f);
         }
     }
     fence_proxy_async_smem();
@@ -1069,13 +1069,13 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                 const float* pi = sm.pinfo(pb);
                 const Piece& pc = it.pc;
                 if (pc.whole) {
-                    float* row = p.out + ((int64_t)pc.b * p.Hq + (int64_t)pc.h * G) * D;
+                    const OutRow row = out_row(p, ((int64_t)pc.b * p.Hq + (int64_t)pc.h * G) * D);
                     if (ct < D) {
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
                             const float L = pi[g];
                             const float z = C::INT4 ? pi[2 * G + g * C::NGR + grp] : 0.0f;
-                            row[g * D + ch] = (L > 0.0f) ? (o[g] + z) / L : 0.0f;
+                            store_out(row, g * D + ch, (L > 0.0f) ? (o[g] + z) / L : 0.0f);
                         }
                     }
                 } else {
@@ -1157,7 +1157,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
             const int it = i0 + lane;
             merge_element<D, G>(p.ws_o, p.ws_m, p.ws_l, a, plan.S, k0, (int)n, (it % NE) / (D / 4),
                                 ((it % NE) % (D / 4)) * 4, lane, it < NE,
-                                p.out + ((int64_t)b * p.Hq + (int64_t)h * G) * D, nullptr, nullptr, nullptr);
+                                out_row(p, ((int64_t)b * p.Hq + (int64_t)h * G) * D), nullptr, nullptr, nullptr);
         }
     }
 }

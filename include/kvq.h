@@ -182,6 +182,24 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const int32_t*
                            int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
                            void* workspace, size_t workspace_bytes, kvq_stream_t stream);
 
+/* Output element types of kvq_decode_attn_out. */
+typedef enum kvq_out_dtype {
+    KVQ_OUT_F32 = 0,  /* fp32, as kvq_decode_attn */
+    KVQ_OUT_BF16 = 1  /* bf16: the fp32 result rounded to nearest even */
+} kvq_out_dtype;
+
+/* kvq_decode_attn with the output element type chosen by out_dtype:
+ *   out  device, [num_seqs][num_q_heads][head_dim] of fp32 (KVQ_OUT_F32) or
+ *        bf16 (KVQ_OUT_BF16); 16-byte aligned.
+ * Every output element is the value kvq_decode_attn computes, rounded to
+ * nearest even when bf16 (the split partials stay fp32).  Other arguments,
+ * rules and errors as kvq_decode_attn; an unknown out_dtype gives
+ * KVQ_ERR_INVALID_ARG. */
+kvq_status kvq_decode_attn_out(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                               const int32_t* seq_lens, void* out, int32_t out_dtype, int32_t num_seqs,
+                               int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
+                               void* workspace, size_t workspace_bytes, kvq_stream_t stream);
+
 /* The first launch of the two-launch form of kvq_decode_attn: every
  * (sequence, KV head) whose tokens one CTA covers entirely gets its final
  * output row; the rest leave split partials (max, sum, unnormalized output)

@@ -242,3 +242,11 @@ def test_no_oracle_in_product_path():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "liboracle" not in text and "kvq_oracle" not in text, f
+
+
+def test_decode_attn_out_rejects_an_unknown_output_dtype():
+    """The output dtype is checked before anything else: no device needed."""
+    import ctypes
+    st = kvq.lib.kvq_decode_attn_out(None, None, None, None, None, 7, 1, 8, 1, ctypes.c_float(0.0), None, 0, None)
+    assert st == 1  # KVQ_ERR_INVALID_ARG
+

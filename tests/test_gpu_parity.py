@@ -79,6 +79,26 @@ def test_int4sym_eight_layer_shapes():
     assert_attn_close(got[sample], case.oracle_decode(seqs=sample), "symmetric INT4, 8-layer shapes")
 
 
+@pytest.mark.parametrize("shape", [("int8", 32, 8, 128, 16), ("int4", 32, 8, 128, 32), ("fp8", 64, 8, 128, 16),
+                                   ("int4sym", 16, 8, 64, 16)], ids=lambda s: "-".join(map(str, s)))
+def test_bf16_output_is_the_rounded_fp32_output(shape):
+    """kvq_decode_attn_out with bf16 output writes, element for element, the
+    fp32 output of kvq_decode_attn rounded to nearest even: final rows of
+    whole segments, merged split segments (a 40000-token sequence) and the
+    zero rows of empty sequences, on both decode kernels."""
+    scheme, Hq, Hkv, D, P = shape
+    w = small(scheme, Hq, Hkv, D, P)
+    lens = np.array([1, 0, 300, 5000, 17, 40000], np.int32)
+    case = Case(w, lens, oracle_seqs=[])
+    ref32 = case.decode()
+    out = torch.full((len(lens), Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = kvq.alloc_workspace(case.g, len(lens), Hq, case.bt.shape[1], device=DEV)
+    kvq.decode_attn(case.g, dev_bits(case.q), dev(case.bt), dev(case.lens), out, ws)
+    assert kvq.last_device_error() == kvq.OK
+    want = torch.from_numpy(ref32.astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(out.cpu().view(torch.int16), want.view(torch.int16))
+
+
 # ------------------------------------------------------------- edge cases
 SHAPES = [  # scheme, Hq, Hkv, D, P
     ("int8", 8, 8, 64, 16), ("int8", 8, 4, 64, 16), ("int8", 16, 4, 128, 32), ("int8", 32, 4, 128, 16),
