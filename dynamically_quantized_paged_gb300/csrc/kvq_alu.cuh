@@ -40,12 +40,16 @@
 //  * online softmax in base 2 directly on those lanes (max over the unit by
 //    shuffles); the weights p * value scale go to shared memory;
 //  * values: each lane owns 4 (or 8) channels x G heads of fp32 accumulators.
-//    INT8: the unit's weights of each head become 16-bit fixed point
-//    relative to their maximum; the lane transposes the codes of 4
-//    consecutive tokens into one word per channel (byte permutes), dp4a
-//    accumulates the unit in int32 (high byte, times 256, then low byte), and
-//    one FMA per accumulator adds the unit.  FP8, INT4: scalar FMAs on exactly
-//    converted codes (INT4 adds the zero-points once per token).
+//    INT8, INT4: the unit's weights of each head (INT4: of each head and
+//    32-channel group, since the value scale is per group) become 16-bit
+//    fixed point relative to their maximum, packed by the score lanes into
+//    words of 4 token bytes; the value lane transposes the codes of the same
+//    4 tokens into one word per channel (byte permutes; INT4 masks the two
+//    nibbles apart), dp4a accumulates the unit in int32 (high byte, times
+//    256, then low byte), and one FMA per accumulator adds the unit.  INT4's
+//    zero-point term, sum over tokens of p * zero, is kept per (group, head)
+//    on the score lanes and added once when the piece ends.  FP8: scalar
+//    FMAs on exactly converted codes.
 // The query rows of a piece travel in the stage of the warp's first unit of
 // that piece.
 #pragma once
@@ -96,21 +100,35 @@ struct DecodeCfg {
     static constexpr int QW = CPL / 2;  // fp16 pairs of query per head per lane
     static constexpr bool TWO_ACC = G <= 2;  // a second accumulator set for more ILP when registers allow
     // values: VCH channels per lane, VL lanes per token, VT token groups.
-    // INT8 values go through dp4a: weights as 16-bit fixed point (hi and lo
-    // bytes) against the codes of 4 consecutive tokens of one channel.
-    static constexpr bool VDP = INT8;
+    // INT8 and INT4 values go through dp4a: weights as 16-bit fixed point (hi
+    // and lo bytes) against the codes of one channel in a block of 4 tokens.
+    static constexpr bool VDP = INT8 || INT4;
     static constexpr int VCH = (VDP || (G >= 8 && D == 128)) ? 4 : 8;
     static constexpr int VL = D / VCH;
     static constexpr int VT = 32 / VL;
     static constexpr int V_UNROLL = (G >= 8) ? 4 : UNIT / VT;  // token loop unrolling (register pressure)
     static constexpr int NBLK = UNIT / 4 / VT;                 // dp4a path: 4-token blocks per lane
+    // dp4a path: a block is the 4 tokens whose weights LPB score lanes (same
+    // channels and head, consecutive token slots) hold over their PASSES
+    // passes, so each lane packs its bytes into one store: byte i of block b
+    // is token (i % PASSES) * TPP + b * LPB + i / PASSES.
+    static constexpr int LPB = 4 / PASSES;
+    // INT4 weights carry the value scale of their 32-channel group, so there
+    // is one weight per (token, group, head); a score lane computes GPL groups
+    static constexpr int NGW = INT4 ? NGR : 1;
+    static constexpr int GPL = NGW > DUP ? NGW / DUP : 1;
     // shared memory layout (bytes)
     static constexpr int OFF_STAGES = 0;
     static constexpr int OFF_W = OFF_STAGES + WARPS * STAGES * STAGE;
-    // per warp: weights (fp32 Wt[UNIT][G], or on the dp4a path the bytes
-    // WB[UNIT/4][hi, lo][G][4 tokens]), then the weights' fixed-point step
-    // WQ[G] (dp4a path), then alpha[G]
-    static constexpr int W_BYTES = (UNIT * G * 4 + 2 * G * 4 + 15) / 16 * 16;
+    // per warp: weights (fp32 Wt[UNIT][G], or on the dp4a path the words
+    // WB[UNIT/4][hi, lo][NGW][G] of 4 token bytes), then the weights'
+    // fixed-point step WQ[NGW][G] (dp4a path), alpha[G], and (INT4) the
+    // zero-point sums ZS[NGR][G] of a finished piece
+    static constexpr int WB_BYTES = VDP ? UNIT * 2 * NGW * G : UNIT * G * 4;
+    static constexpr int W_OFF_WQ = WB_BYTES;
+    static constexpr int W_OFF_AL = W_OFF_WQ + NGW * G * 4;
+    static constexpr int W_OFF_ZS = W_OFF_AL + G * 4;
+    static constexpr int W_BYTES = (W_OFF_ZS + (INT4 ? NGR * G * 4 : 0) + 15) / 16 * 16;
     static constexpr int OFF_MISC = OFF_W + WARPS * W_BYTES;
     static constexpr int OFF_PLAN = OFF_MISC + 16;
     static size_t smem_bytes(int B) { return OFF_PLAN + (size_t)(B + 1) * 4; }
@@ -118,6 +136,9 @@ struct DecodeCfg {
     static_assert(STAGE % 16 == 0 && Q_BYTES % 16 == 0 && (UNIT * MB) % 16 == 0, "16-byte copies");
     static_assert(OFF_W % 16 == 0, "alignment");
     static_assert(4 * (UNIT * MB / 16) <= 32, "one lane per 16 bytes of scales and zeros");
+    static_assert(!VDP || PASSES == 4 || PASSES == 2, "a lane's weight bytes fill a word or a half word");
+    static_assert(!VDP || (NGW % GPL == 0 && NGW / GPL <= DUP), "every group has a writer lane");
+    static_assert(!VDP || VCH == 4, "one dp4a word per channel");
 };
 
 // Transpose-reduction across the KL lanes that share a token: N values per
@@ -296,9 +317,10 @@ decode_partial_kernel(const DecodeParams p) {
     const int tid = threadIdx.x;
     uint8_t* wbase = smem + C::OFF_W + warp * C::W_BYTES;
     float* Wt = reinterpret_cast<float*>(wbase);                   // [UNIT][G]
-    uint8_t* WB = wbase;                                           // dp4a path: weight bytes
-    float* WQ = reinterpret_cast<float*>(wbase + UNIT * G * 4);    // [G]
-    float* AL = WQ + G;                                            // [G]
+    uint32_t* WB = reinterpret_cast<uint32_t*>(wbase);             // dp4a path: weight words
+    float* WQ = reinterpret_cast<float*>(wbase + C::W_OFF_WQ);     // [NGW][G]
+    float* AL = reinterpret_cast<float*>(wbase + C::W_OFF_AL);     // [G]
+    float* ZS = reinterpret_cast<float*>(wbase + C::W_OFF_ZS);     // INT4: [NGR][G]
     // score-lane coordinates
     const int k_tok = lane / C::KL;
     const int k_c0 = (C::SHEAD ? (lane % C::KL) % C::DUP : lane % C::KL) * C::CPL;
@@ -325,10 +347,11 @@ decode_partial_kernel(const DecodeParams p) {
         float my_sq = 0.0f;     // INT8: fixed-point step of this lane's head times the softmax scale
         float m_run = -INFINITY, l_run = 0.0f;
         float o[G][C::VCH];
-        float zacc[G];
+        float zr[C::GPL];  // INT4: this lane's running sum of p * value zero-point, per group
+#pragma unroll
+        for (int j = 0; j < C::GPL; ++j) zr[j] = 0.0f;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            zacc[g] = 0.0f;
             sq[g] = 0.0f;
             qisum[g] = 0.0f;
 #pragma unroll
@@ -569,37 +592,74 @@ decode_partial_kernel(const DecodeParams p) {
                 const float alpha = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - m_new);
                 float psum = 0.0f;
                 if constexpr (C::VDP) {
-                    // weights W = p * value scale, then 16-bit fixed point per
-                    // (unit, head): W ~ wq * (256 hi + lo), wq = max W / 65535
-                    float wv[C::PASSES];
-                    float wmax = 0.0f;
+                    // weights W = p * value scale (INT4: the scale of each of the
+                    // lane's GPL groups), then 16-bit fixed point per (unit, group,
+                    // head): W ~ wq * (256 hi + lo), wq = max W / 65535
+                    // the weight groups this score lane writes (INT4: GPL groups
+                    // from w_r0; INT8: the one group, on the lane that writes its head)
+                    const int w_r0 = ((lane % C::DUP) * C::GPL) % C::NGW;
+                    const bool w_writer = (lane % C::DUP) * C::GPL < C::NGW;
+                    float wv[C::GPL][C::PASSES];
+                    float wmax[C::GPL], zs[C::GPL];
+#pragma unroll
+                    for (int j = 0; j < C::GPL; ++j) wmax[j] = zs[j] = 0.0f;
 #pragma unroll
                     for (int pass = 0; pass < C::PASSES; ++pass) {
                         const int t = pass * C::TPP + k_tok;
+                        const bool valid = t < n_valid;
                         const float pr = (sc[pass] == -INFINITY) ? 0.0f : fast_exp2(sc[pass] - m_new);
                         psum += pr;
-                        wv[pass] = (t < n_valid) ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
-                        wmax = fmaxf(wmax, wv[pass]);
+                        if constexpr (C::INT8) {
+                            wv[0][pass] = valid ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < C::GPL; ++j) {
+                                const int gi = t * C::NGR + w_r0 + j;
+                                const float vs = __half2float(reinterpret_cast<const __half*>(stg + C::VS)[gi]);
+                                const float vz = __half2float(reinterpret_cast<const __half*>(stg + C::VZ)[gi]);
+                                wv[j][pass] = valid ? pr * vs : 0.0f;
+                                zs[j] += valid ? pr * vz : 0.0f;
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < C::GPL; ++j) wmax[j] = fmaxf(wmax[j], wv[j][pass]);
                     }
 #pragma unroll
-                    for (int off = C::KL; off < 32; off <<= 1)
-                        wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
-                    // Below 1e-30 the unit's weights are negligible next to the
-                    // running sum (>= 1 after the first token) and are dropped.
-                    const bool live = wmax > 1e-30f;
-                    const float inv = live ? __fdividef(65535.0f, wmax) : 0.0f;
-                    if (k_writer) {
+                    for (int j = 0; j < C::GPL; ++j) {
+                        float wm = wmax[j];
 #pragma unroll
-                        for (int pass = 0; pass < C::PASSES; ++pass) {
-                            const int t = pass * C::TPP + k_tok;
-                            // round to nearest in the low mantissa bits of 2^23 + W * inv;
-                            // W * inv <= 65535 (1 + 2^-22) never rounds up to 65536
-                            const uint32_t bits = __float_as_uint(fmaf(wv[pass], inv, 8388608.0f));
-                            uint8_t* dst = WB + (((t >> 2) * 2) * G + k_head) * 4 + (t & 3);
-                            dst[0] = (uint8_t)(bits >> 8);  // hi byte
-                            dst[G * 4] = (uint8_t)bits;     // lo byte
+                        for (int off = C::KL; off < 32; off <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
+                        // Below 1e-30 the unit's weights are negligible next to the
+                        // running sum (>= 1 after the first token) and are dropped.
+                        const bool live = wm > 1e-30f;
+                        const float inv = live ? __fdividef(65535.0f, wm) : 0.0f;
+                        // round to nearest in the low mantissa bits of 2^23 + W * inv;
+                        // W * inv <= 65535 (1 + 2^-22) never rounds up to 65536
+                        uint32_t bits[C::PASSES];
+#pragma unroll
+                        for (int pass = 0; pass < C::PASSES; ++pass)
+                            bits[pass] = __float_as_uint(fmaf(wv[j][pass], inv, 8388608.0f));
+                        // this lane's bytes of its block: low bytes -> lo word, next bytes -> hi word
+                        uint32_t lo = __byte_perm(bits[0], bits[1], 0x0040);
+                        uint32_t hi = __byte_perm(bits[0], bits[1], 0x0051);
+                        if constexpr (C::PASSES == 4) {
+                            lo = __byte_perm(lo, __byte_perm(bits[2], bits[3], 0x0040), 0x5410);
+                            hi = __byte_perm(hi, __byte_perm(bits[2], bits[3], 0x0051), 0x5410);
                         }
-                        if (k_tok == 0) WQ[k_head] = live ? wmax * (1.0f / 65535.0f) : 0.0f;
+                        if (w_writer) {
+                            const int blk = k_tok / C::LPB;
+                            const int wi = ((blk * 2) * C::NGW + w_r0 + j) * G + k_head;  // hi word; lo is one half-block on
+                            if constexpr (C::PASSES == 4) {
+                                WB[wi] = hi;
+                                WB[wi + C::NGW * G] = lo;
+                            } else {
+                                uint16_t* wb16 = reinterpret_cast<uint16_t*>(WB);
+                                wb16[2 * wi + k_tok % 2] = (uint16_t)hi;
+                                wb16[2 * (wi + C::NGW * G) + k_tok % 2] = (uint16_t)lo;
+                            }
+                            if (k_tok == 0) WQ[(w_r0 + j) * G + k_head] = live ? wm * (1.0f / 65535.0f) : 0.0f;
+                        }
+                        if constexpr (C::INT4) zr[j] = fmaf(zr[j], alpha, zs[j]);
                     }
                 } else {
 #pragma unroll
@@ -607,11 +667,8 @@ decode_partial_kernel(const DecodeParams p) {
                         const int t = pass * C::TPP + k_tok;
                         const float pr = (sc[pass] == -INFINITY) ? 0.0f : fast_exp2(sc[pass] - m_new);
                         psum += pr;
-                        if (k_writer) {
-                            float wv = pr;
-                            if constexpr (!C::INT4) wv = (t < n_valid) ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
-                            Wt[t * G + k_head] = wv;
-                        }
+                        if (k_writer)
+                            Wt[t * G + k_head] = (t < n_valid) ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
                     }
                 }
                 l_run = l_run * alpha + psum;
@@ -624,31 +681,50 @@ decode_partial_kernel(const DecodeParams p) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         const float a = AL[g];
-                        zacc[g] *= a;
 #pragma unroll
                         for (int jj = 0; jj < C::VCH; ++jj) o[g][jj] *= a;
                     }
                 }
                 if constexpr (C::VDP) {
-                    // codes of 4 consecutive tokens x this lane's 4 channels,
-                    // transposed to one word per channel (token bytes in order)
+                    // codes of one 4-token block x this lane's 4 channels,
+                    // transposed to one word per channel (token bytes in block
+                    // order).  INT4 keeps each odd channel's code in the high
+                    // nibble (16 x code), a factor taken out with the step.
                     uint32_t x[C::NBLK][4];
 #pragma unroll
                     for (int k = 0; k < C::NBLK; ++k) {
-                        const uint8_t* src = stg + C::VC + (4 * (v_tok + k * C::VT)) * D + v_c0;
-                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(src);
-                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(src + D);
-                        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(src + 2 * D);
-                        const uint32_t w3 = *reinterpret_cast<const uint32_t*>(src + 3 * D);
-                        const uint32_t a01 = __byte_perm(w0, w1, 0x5140), b01 = __byte_perm(w0, w1, 0x7362);
-                        const uint32_t a23 = __byte_perm(w2, w3, 0x5140), b23 = __byte_perm(w2, w3, 0x7362);
-                        x[k][0] = __byte_perm(a01, a23, 0x5410);
-                        x[k][1] = __byte_perm(a01, a23, 0x7632);
-                        x[k][2] = __byte_perm(b01, b23, 0x5410);
-                        x[k][3] = __byte_perm(b01, b23, 0x7632);
+                        const int b = v_tok + k * C::VT;
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int t = (i % C::PASSES) * C::TPP + b * C::LPB + i / C::PASSES;
+                            if constexpr (C::INT4)
+                                w[i] = *reinterpret_cast<const uint16_t*>(stg + C::VC + t * (D / 2) + v_c0 / 2);
+                            else
+                                w[i] = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * D + v_c0);
+                        }
+                        const uint32_t a01 = __byte_perm(w[0], w[1], 0x5140);
+                        const uint32_t a23 = __byte_perm(w[2], w[3], 0x5140);
+                        if constexpr (C::INT4) {
+                            const uint32_t y0 = __byte_perm(a01, a23, 0x5410);  // channels v_c0, v_c0 + 1
+                            const uint32_t y1 = __byte_perm(a01, a23, 0x7632);  // channels v_c0 + 2, v_c0 + 3
+                            x[k][0] = y0 & 0x0F0F0F0Fu;
+                            x[k][1] = y0 & 0xF0F0F0F0u;
+                            x[k][2] = y1 & 0x0F0F0F0Fu;
+                            x[k][3] = y1 & 0xF0F0F0F0u;
+                        } else {
+                            const uint32_t b01 = __byte_perm(w[0], w[1], 0x7362);
+                            const uint32_t b23 = __byte_perm(w[2], w[3], 0x7362);
+                            x[k][0] = __byte_perm(a01, a23, 0x5410);
+                            x[k][1] = __byte_perm(a01, a23, 0x7632);
+                            x[k][2] = __byte_perm(b01, b23, 0x5410);
+                            x[k][3] = __byte_perm(b01, b23, 0x7632);
+                        }
                     }
-                    // sum over the unit of (256 hi + lo) * code in int32 (|sum| < 2^28),
-                    // then one FMA per accumulator with the step wq
+                    // sum over the unit of (256 hi + lo) * code in int32 (INT8:
+                    // |sum| < 2^28; INT4: < 16 * 255 * 240 * 257 < 2^28), then one
+                    // FMA per accumulator with the step wq
+                    const int rv = C::INT4 ? v_c0 / 32 : 0;  // the lane's weight group
                     constexpr int GC = G < 4 ? G : 4;
 #pragma unroll
                     for (int g0 = 0; g0 < G; g0 += GC) {
@@ -668,7 +744,7 @@ decode_partial_kernel(const DecodeParams p) {
 #pragma unroll
                             for (int k = 0; k < C::NBLK; ++k) {
                                 const int blk = v_tok + k * C::VT;
-                                const uint8_t* wsrc = WB + ((blk * 2 + half) * G + g0) * 4;
+                                const uint32_t* wsrc = WB + ((blk * 2 + half) * C::NGW + rv) * G + g0;
                                 uint32_t wq4[GC];
                                 if constexpr (GC == 4) {
                                     const uint4 r = *reinterpret_cast<const uint4*>(wsrc);
@@ -677,19 +753,24 @@ decode_partial_kernel(const DecodeParams p) {
                                     const uint2 r = *reinterpret_cast<const uint2*>(wsrc);
                                     wq4[0] = r.x; wq4[1] = r.y;
                                 } else {
-                                    wq4[0] = *reinterpret_cast<const uint32_t*>(wsrc);
+                                    wq4[0] = *wsrc;
                                 }
 #pragma unroll
                                 for (int gg = 0; gg < GC; ++gg)
 #pragma unroll
-                                    for (int j = 0; j < 4; ++j) acc[gg][j] = dp4a_us(wq4[gg], (int)x[k][j], acc[gg][j]);
+                                    for (int j = 0; j < 4; ++j) {
+                                        if constexpr (C::INT4) acc[gg][j] = dp4a_uu(wq4[gg], x[k][j], acc[gg][j]);
+                                        else acc[gg][j] = dp4a_us(wq4[gg], (int)x[k][j], acc[gg][j]);
+                                    }
                             }
                         }
 #pragma unroll
                         for (int gg = 0; gg < GC; ++gg) {
-                            const float step = WQ[g0 + gg];
+                            const float step = WQ[rv * G + g0 + gg];
+                            const float step_odd = C::INT4 ? step * 0.0625f : step;
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) o[g0 + gg][j] = fmaf((float)acc[gg][j], step, o[g0 + gg][j]);
+                            for (int j = 0; j < 4; ++j)
+                                o[g0 + gg][j] = fmaf((float)acc[gg][j], (j & 1) ? step_odd : step, o[g0 + gg][j]);
                         }
                     }
                 } else {
@@ -697,37 +778,18 @@ decode_partial_kernel(const DecodeParams p) {
                 for (int k = 0; k < UNIT / C::VT; ++k) {
                     const int t = v_tok + k * C::VT;
                     if (t < n_valid) {
-                        float c[C::VCH];  // this lane's codes of token t, exactly as fp32
-                        if constexpr (C::INT8) {
-                            uint32_t words[C::VCH / 4];
-                            if constexpr (C::VCH == 8) {
-                                const uint2 r = *reinterpret_cast<const uint2*>(stg + C::VC + t * D + v_c0);
-                                words[0] = r.x;
-                                words[1] = r.y;
-                            } else {
-                                words[0] = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * D + v_c0);
-                            }
-#pragma unroll
-                            for (int i = 0; i < C::VCH / 4; ++i) s8x4_to_float(words[i], c + 4 * i);
-                        } else if constexpr (!C::INT4) {
-                            uint32_t words[C::VCH / 4];
-                            if constexpr (C::VCH == 8) {
-                                const uint2 r = *reinterpret_cast<const uint2*>(stg + C::VC + t * D + v_c0);
-                                words[0] = r.x;
-                                words[1] = r.y;
-                            } else {
-                                words[0] = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * D + v_c0);
-                            }
-#pragma unroll
-                            for (int i = 0; i < C::VCH / 4; ++i) e4m3x4_to_float(words[i], c + 4 * i);
+                        // FP8: this lane's codes of token t, exactly as fp32
+                        float c[C::VCH];
+                        uint32_t words[C::VCH / 4];
+                        if constexpr (C::VCH == 8) {
+                            const uint2 r = *reinterpret_cast<const uint2*>(stg + C::VC + t * D + v_c0);
+                            words[0] = r.x;
+                            words[1] = r.y;
                         } else {
-                            uint32_t r;
-                            if constexpr (C::VCH == 8) r = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * (D / 2) + v_c0 / 2);
-                            else r = *reinterpret_cast<const uint16_t*>(stg + C::VC + t * (D / 2) + v_c0 / 2);
-#pragma unroll
-                            for (int i = 0; i < C::VCH; ++i)
-                                c[i] = __uint_as_float(((r >> (4 * i)) & 0xFu) | 0x4B000000u) - 8388608.0f;
+                            words[0] = *reinterpret_cast<const uint32_t*>(stg + C::VC + t * D + v_c0);
                         }
+#pragma unroll
+                        for (int i = 0; i < C::VCH / 4; ++i) e4m3x4_to_float(words[i], c + 4 * i);
                         float wg[G];
 #pragma unroll
                         for (int g = 0; g < G; g += 4) {
@@ -739,23 +801,10 @@ decode_partial_kernel(const DecodeParams p) {
                                 for (int gg = 0; gg < G; ++gg) wg[gg] = Wt[t * G + gg];
                             }
                         }
-                        if constexpr (!C::INT4) {
 #pragma unroll
-                            for (int g = 0; g < G; ++g)
+                        for (int g = 0; g < G; ++g)
 #pragma unroll
-                                for (int jj = 0; jj < C::VCH; ++jj) o[g][jj] = fmaf(wg[g], c[jj], o[g][jj]);
-                        } else {
-                            const int gi = t * C::NGR + v_c0 / 32;
-                            const float vs = __half2float(reinterpret_cast<const __half*>(stg + C::VS)[gi]);
-                            const float vz = __half2float(reinterpret_cast<const __half*>(stg + C::VZ)[gi]);
-#pragma unroll
-                            for (int g = 0; g < G; ++g) {
-                                zacc[g] = fmaf(wg[g], vz, zacc[g]);
-                                const float a = wg[g] * vs;
-#pragma unroll
-                                for (int jj = 0; jj < C::VCH; ++jj) o[g][jj] = fmaf(a, c[jj], o[g][jj]);
-                            }
-                        }
+                            for (int jj = 0; jj < C::VCH; ++jj) o[g][jj] = fmaf(wg[g], c[jj], o[g][jj]);
                     }
                 }
                 }
@@ -768,13 +817,28 @@ decode_partial_kernel(const DecodeParams p) {
         // is final, any other piece leaves a partial in the warp's slot
 #pragma unroll
         for (int off = C::KL; off < 32; off <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
+        if constexpr (C::INT4) {
+            // the zero-point term sum_t p * zero of each (group, head), summed
+            // over the token slots, goes to the value lanes through ZS
+            const int w_r0 = ((lane % C::DUP) * C::GPL) % C::NGW;
+            const bool w_writer = (lane % C::DUP) * C::GPL < C::NGW;
+#pragma unroll
+            for (int j = 0; j < C::GPL; ++j) {
+                float z = zr[j];
+#pragma unroll
+                for (int off = C::KL; off < 32; off <<= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+                if (w_writer && k_tok == 0) ZS[(w_r0 + j) * G + k_head] = z;
+            }
+            __syncwarp();
+        }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
 #pragma unroll
             for (int jj = 0; jj < C::VCH; ++jj) {
-                float v = o[g][jj] + zacc[g];
+                float v = o[g][jj];
 #pragma unroll
                 for (int off = C::VL; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if constexpr (C::INT4) v += ZS[(v_c0 / 32) * G + g];
                 o[g][jj] = v;
             }
         }
