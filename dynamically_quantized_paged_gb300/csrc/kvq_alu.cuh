@@ -89,9 +89,10 @@ struct DecodeCfg {
     // INT8: each lane takes ONE query head (DUP = KL / G lanes per head) and
     // D / DUP of its channels, so its dot product needs no transpose across
     // heads, only a sum over the DUP lanes.  FP8 / INT4: each lane takes 16
-    // (or 8) channels of all G heads and a transpose-reduction sorts them out.
+    // (or 8; INT4 at d 128: 32, one scale group) channels of all G heads and a
+    // transpose-reduction sorts them out.
     static constexpr bool SHEAD = INT8;
-    static constexpr int CPL = SHEAD ? D * G / 8 : ((D == 64 && G == 8) ? 8 : 16);
+    static constexpr int CPL = SHEAD ? D * G / 8 : (INT4 && D == 128) ? 32 : ((D == 64 && G == 8) ? 8 : 16);
     static constexpr int KL = SHEAD ? 8 : D / CPL;
     static constexpr int QROWS = SHEAD ? 1 : G;  // query rows held per lane
     static constexpr int TPP = 32 / KL;
@@ -121,12 +122,15 @@ struct DecodeCfg {
     static constexpr int OFF_STAGES = 0;
     static constexpr int OFF_W = OFF_STAGES + WARPS * STAGES * STAGE;
     // per warp: weights (fp32 Wt[UNIT][G], or on the dp4a path the words
-    // WB[UNIT/4][hi, lo][NGW][G] of 4 token bytes), then the weights'
-    // fixed-point step WQ[NGW][G] (dp4a path), alpha[G], and (INT4) the
+    // WB[hi, lo][NGW][UNIT/4][G] of 4 token bytes, an order in which the
+    // score lanes' stores fall in distinct banks), then the weights'
+    // fixed-point step WQ[G] (dp4a path), alpha[G], and (INT4) the
     // zero-point sums ZS[NGR][G] of a finished piece
-    static constexpr int WB_BYTES = VDP ? UNIT * 2 * NGW * G : UNIT * G * 4;
+    static constexpr int NB = UNIT / 4;             // 4-token blocks per unit
+    static constexpr int WB_HALF = NGW * NB * G;     // words of one byte plane (hi or lo)
+    static constexpr int WB_BYTES = VDP ? 2 * WB_HALF * 4 : UNIT * G * 4;
     static constexpr int W_OFF_WQ = WB_BYTES;
-    static constexpr int W_OFF_AL = W_OFF_WQ + NGW * G * 4;
+    static constexpr int W_OFF_AL = W_OFF_WQ + G * 4;
     static constexpr int W_OFF_ZS = W_OFF_AL + G * 4;
     static constexpr int W_BYTES = (W_OFF_ZS + (INT4 ? NGR * G * 4 : 0) + 15) / 16 * 16;
     static constexpr int OFF_MISC = OFF_W + WARPS * W_BYTES;
@@ -159,6 +163,21 @@ __device__ __forceinline__ void transpose_reduce(T* v, int lane) {
         } else {
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], OFF);
             transpose_reduce<T, 1, OFF / 2>(v, lane);
+        }
+    }
+}
+
+// N consecutive fp16 values from shared memory (2N-byte aligned) -> fp32
+template <int N>
+__device__ __forceinline__ void load_halves(const uint8_t* src, float* f) {
+    if constexpr (N == 1) {
+        f[0] = __half2float(*reinterpret_cast<const __half*>(src));
+    } else {
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float2 v = __half22float2(reinterpret_cast<const __half2*>(src)[i]);
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
         }
     }
 }
@@ -318,7 +337,7 @@ decode_partial_kernel(const DecodeParams p) {
     uint8_t* wbase = smem + C::OFF_W + warp * C::W_BYTES;
     float* Wt = reinterpret_cast<float*>(wbase);                   // [UNIT][G]
     uint32_t* WB = reinterpret_cast<uint32_t*>(wbase);             // dp4a path: weight words
-    float* WQ = reinterpret_cast<float*>(wbase + C::W_OFF_WQ);     // [NGW][G]
+    float* WQ = reinterpret_cast<float*>(wbase + C::W_OFF_WQ);     // [G]
     float* AL = reinterpret_cast<float*>(wbase + C::W_OFF_AL);     // [G]
     float* ZS = reinterpret_cast<float*>(wbase + C::W_OFF_ZS);     // INT4: [NGR][G]
     // score-lane coordinates
@@ -342,9 +361,8 @@ decode_partial_kernel(const DecodeParams p) {
         ua = pc.u_lo;
         ub = pc.u_hi;
         uint32_t qw[C::QROWS][C::QW];  // query: INT8/INT4 fixed-point bytes, FP8 fp16 pairs
-        float sq[G];            // INT4: fixed-point step per head
         float qisum[G];         // INT4: sum of this lane's fixed-point query channels, per head
-        float my_sq = 0.0f;     // INT8: fixed-point step of this lane's head times the softmax scale
+        float my_sq = 0.0f;     // INT8, INT4: fixed-point step of the lane's score head times the softmax scale
         float m_run = -INFINITY, l_run = 0.0f;
         float o[G][C::VCH];
         float zr[C::GPL];  // INT4: this lane's running sum of p * value zero-point, per group
@@ -352,7 +370,6 @@ decode_partial_kernel(const DecodeParams p) {
         for (int j = 0; j < C::GPL; ++j) zr[j] = 0.0f;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            sq[g] = 0.0f;
             qisum[g] = 0.0f;
 #pragma unroll
             for (int j = 0; j < C::VCH; ++j) o[g][j] = 0.0f;
@@ -450,7 +467,7 @@ decode_partial_kernel(const DecodeParams p) {
                                 qw[g][4 * i + 2] = lb(b0) | (lb(b0 + 2) << 8) | (lb(b0 + 4) << 16) | (lb(b0 + 6) << 24);
                                 qw[g][4 * i + 3] = lb(b0 + 1) | (lb(b0 + 3) << 8) | (lb(b0 + 5) << 16) | (lb(b0 + 7) << 24);
                             }
-                            sq[g] = sqg;
+                            if (g == k_head) my_sq = sqg * qk_scale;
                             qisum[g] = (float)isum;
                         }
                     } else {  // FP8: the query as fp16 pairs of consecutive channels
@@ -467,6 +484,22 @@ decode_partial_kernel(const DecodeParams p) {
             if (badmask & (1u << st)) n_valid = 0;
 
             if (n_valid > 0) {
+                if constexpr (C::VDP) {
+                    if (n_valid < UNIT) {
+                        // a partial last unit: past the sequence's end the stage holds
+                        // whatever the page does; zeroing those value scales (and
+                        // zero-points) makes their weights and zero sums exactly 0
+                        // (their p is 0), with no per-token test below
+                        uint32_t* vs32 = reinterpret_cast<uint32_t*>(ring + st * C::STAGE + C::VS);
+                        uint32_t* vz32 = reinterpret_cast<uint32_t*>(ring + st * C::STAGE + C::VZ);
+                        const int i = n_valid * (C::MB / 4) + lane;
+                        if (i < UNIT * (C::MB / 4)) {
+                            vs32[i] = 0u;
+                            if constexpr (C::INT4) vz32[i] = 0u;
+                        }
+                        __syncwarp();
+                    }
+                }
                 // ---- scores for G heads x UNIT tokens
                 float sc[C::PASSES];
 #pragma unroll
@@ -511,7 +544,10 @@ decode_partial_kernel(const DecodeParams p) {
                     } else if constexpr (C::INT4) {
                         const uint8_t* src = stg + C::KC + t * (D / 2) + k_c0 / 2;
                         uint32_t wv[C::CPL / 8];
-                        if constexpr (C::CPL == 16) {
+                        if constexpr (C::CPL == 32) {
+                            const uint4 r = *reinterpret_cast<const uint4*>(src);
+                            wv[0] = r.x; wv[1] = r.y; wv[2] = r.z; wv[3] = r.w;
+                        } else if constexpr (C::CPL == 16) {
                             const uint2 r = *reinterpret_cast<const uint2*>(src);
                             wv[0] = r.x; wv[1] = r.y;
                         } else {
@@ -537,11 +573,12 @@ decode_partial_kernel(const DecodeParams p) {
                                 al = dp4a_uu(qw[g][4 * i + 2], ev[i], al);
                                 al = dp4a_uu(qw[g][4 * i + 3], od[i], al);
                             }
-                            // sum_j q_j (scale * code_j + zero) over this lane's channels
-                            part[g] = sq[g] * fmaf(ks, (float)(ah * 256 + al), kz * qisum[g]);
+                            // sum_j qi_j (scale * code_j + zero) over this lane's channels
+                            // (one group); the head's step is applied after the reduction
+                            part[g] = fmaf(ks, (float)(ah * 256 + al), kz * qisum[g]);
                         }
                         transpose_reduce<float, G, C::KL / 2>(part, lane);
-                        s = part[0] * qk_scale;
+                        s = part[0] * my_sq;
                     } else {
                         constexpr int NA1 = C::TWO_ACC ? G : 1;
                         float acc[G], acc1[NA1];
@@ -606,33 +643,40 @@ decode_partial_kernel(const DecodeParams p) {
 #pragma unroll
                     for (int pass = 0; pass < C::PASSES; ++pass) {
                         const int t = pass * C::TPP + k_tok;
-                        const bool valid = t < n_valid;
-                        const float pr = (sc[pass] == -INFINITY) ? 0.0f : fast_exp2(sc[pass] - m_new);
+                        const float pr = fast_exp2(sc[pass] - m_new);  // a masked token (-inf) gives 0
                         psum += pr;
                         if constexpr (C::INT8) {
-                            wv[0][pass] = valid ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
+                            wv[0][pass] = pr * reinterpret_cast<const float*>(stg + C::VS)[t];
                         } else {
+                            float vs[C::GPL], vz[C::GPL];
+                            load_halves<C::GPL>(stg + C::VS + 2 * (t * C::NGR + w_r0), vs);
+                            load_halves<C::GPL>(stg + C::VZ + 2 * (t * C::NGR + w_r0), vz);
 #pragma unroll
                             for (int j = 0; j < C::GPL; ++j) {
-                                const int gi = t * C::NGR + w_r0 + j;
-                                const float vs = __half2float(reinterpret_cast<const __half*>(stg + C::VS)[gi]);
-                                const float vz = __half2float(reinterpret_cast<const __half*>(stg + C::VZ)[gi]);
-                                wv[j][pass] = valid ? pr * vs : 0.0f;
-                                zs[j] += valid ? pr * vz : 0.0f;
+                                wv[j][pass] = pr * vs[j];
+                                zs[j] = fmaf(pr, vz[j], zs[j]);
                             }
                         }
 #pragma unroll
                         for (int j = 0; j < C::GPL; ++j) wmax[j] = fmaxf(wmax[j], wv[j][pass]);
                     }
+                    // one step per (unit, head) over all its groups: the max of the
+                    // head's weights over the token slots and over the lanes that
+                    // hold its other groups (or duplicates of them)
+                    float wm = wmax[0];
+#pragma unroll
+                    for (int j = 1; j < C::GPL; ++j) wm = fmaxf(wm, wmax[j]);
+#pragma unroll
+                    for (int off = C::KL; off < 32; off <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
+#pragma unroll
+                    for (int off = 1; off < C::DUP; off <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
+                    // Below 1e-30 the unit's weights are negligible next to the
+                    // running sum (>= 1 after the first token) and are dropped.
+                    const bool live = wm > 1e-30f;
+                    const float inv = live ? __fdividef(65535.0f, wm) : 0.0f;
+                    if (k_writer && k_tok == 0) WQ[k_head] = live ? wm * (1.0f / 65535.0f) : 0.0f;
 #pragma unroll
                     for (int j = 0; j < C::GPL; ++j) {
-                        float wm = wmax[j];
-#pragma unroll
-                        for (int off = C::KL; off < 32; off <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
-                        // Below 1e-30 the unit's weights are negligible next to the
-                        // running sum (>= 1 after the first token) and are dropped.
-                        const bool live = wm > 1e-30f;
-                        const float inv = live ? __fdividef(65535.0f, wm) : 0.0f;
                         // round to nearest in the low mantissa bits of 2^23 + W * inv;
                         // W * inv <= 65535 (1 + 2^-22) never rounds up to 65536
                         uint32_t bits[C::PASSES];
@@ -648,16 +692,15 @@ decode_partial_kernel(const DecodeParams p) {
                         }
                         if (w_writer) {
                             const int blk = k_tok / C::LPB;
-                            const int wi = ((blk * 2) * C::NGW + w_r0 + j) * G + k_head;  // hi word; lo is one half-block on
+                            const int wi = ((w_r0 + j) * C::NB + blk) * G + k_head;  // hi word; lo is WB_HALF on
                             if constexpr (C::PASSES == 4) {
                                 WB[wi] = hi;
-                                WB[wi + C::NGW * G] = lo;
+                                WB[wi + C::WB_HALF] = lo;
                             } else {
                                 uint16_t* wb16 = reinterpret_cast<uint16_t*>(WB);
                                 wb16[2 * wi + k_tok % 2] = (uint16_t)hi;
-                                wb16[2 * (wi + C::NGW * G) + k_tok % 2] = (uint16_t)lo;
+                                wb16[2 * (wi + C::WB_HALF) + k_tok % 2] = (uint16_t)lo;
                             }
-                            if (k_tok == 0) WQ[(w_r0 + j) * G + k_head] = live ? wm * (1.0f / 65535.0f) : 0.0f;
                         }
                         if constexpr (C::INT4) zr[j] = fmaf(zr[j], alpha, zs[j]);
                     }
@@ -665,7 +708,7 @@ decode_partial_kernel(const DecodeParams p) {
 #pragma unroll
                     for (int pass = 0; pass < C::PASSES; ++pass) {
                         const int t = pass * C::TPP + k_tok;
-                        const float pr = (sc[pass] == -INFINITY) ? 0.0f : fast_exp2(sc[pass] - m_new);
+                        const float pr = fast_exp2(sc[pass] - m_new);  // a masked token (-inf) gives 0
                         psum += pr;
                         if (k_writer)
                             Wt[t * G + k_head] = (t < n_valid) ? pr * reinterpret_cast<const float*>(stg + C::VS)[t] : 0.0f;
@@ -744,7 +787,7 @@ decode_partial_kernel(const DecodeParams p) {
 #pragma unroll
                             for (int k = 0; k < C::NBLK; ++k) {
                                 const int blk = v_tok + k * C::VT;
-                                const uint32_t* wsrc = WB + ((blk * 2 + half) * C::NGW + rv) * G + g0;
+                                const uint32_t* wsrc = WB + half * C::WB_HALF + (rv * C::NB + blk) * G + g0;
                                 uint32_t wq4[GC];
                                 if constexpr (GC == 4) {
                                     const uint4 r = *reinterpret_cast<const uint4*>(wsrc);
@@ -766,7 +809,7 @@ decode_partial_kernel(const DecodeParams p) {
                         }
 #pragma unroll
                         for (int gg = 0; gg < GC; ++gg) {
-                            const float step = WQ[rv * G + g0 + gg];
+                            const float step = WQ[g0 + gg];
                             const float step_odd = C::INT4 ? step * 0.0625f : step;
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
