@@ -68,8 +68,11 @@ struct DecodeCfg {
     static constexpr bool INT4 = SCHEME == KVQ_INT4_ASYM_G32;
     static constexpr bool INT8 = SCHEME == KVQ_INT8_SYM_TOKEN;
     // One CTA per SM: with several co-resident CTAs the older CTA's warps win
-    // the issue slots and finish first, leaving the SM under-occupied.
-    static constexpr int WARPS = 12;
+    // the issue slots and finish first, leaving the SM under-occupied.  INT8
+    // fits 128 registers a thread, so 16 warps (with a 2-deep ring each, for
+    // shared memory); the others need more registers: 12 warps.
+    static constexpr int WARPS = INT8 ? 16 : 12;
+    static_assert(WARPS == decode_alu_warps(SCHEME, G), "the workspace is sized for this many warps");
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int CB = INT4 ? D / 2 : D;        // code bytes per token row
     static constexpr int NGR = D / 32;                 // INT4 groups per row
@@ -84,7 +87,7 @@ struct DecodeCfg {
     static constexpr int VZ = KZ + (INT4 ? UNIT * MB : 0);
     static constexpr int QO = VZ + (INT4 ? UNIT * MB : 0);
     static constexpr int STAGE = QO + Q_BYTES;
-    static constexpr int STAGES = (STAGE >= 4096) ? 3 : 4;  // ring depth per warp: STAGES-1 units in flight
+    static constexpr int STAGES = WARPS == 16 ? 2 : (STAGE >= 4096) ? 3 : 4;  // ring depth per warp: STAGES-1 units in flight
     // scores: KL lanes per token, CPL channels per lane, TPP tokens per pass.
     // INT8: each lane takes ONE query head (DUP = KL / G lanes per head) and
     // D / DUP of its channels, so its dot product needs no transpose across

@@ -75,10 +75,11 @@ struct DecodeParams {
 // The CUDA-core kernel (kvq_alu.cuh) serves GQA ratios up to 4 of the INT8,
 // FP8 and asymmetric INT4 schemes, the tensor-core kernel (kvq_tc.cuh) the
 // rest; decode_alu_warps gives the former's warps per CTA, 0 for the latter.
-inline int decode_alu_warps(int scheme, int G) {
-    const bool alu = G <= 4 && (scheme == KVQ_INT8_SYM_TOKEN || scheme == KVQ_FP8E4M3_TOKEN ||
-                                scheme == KVQ_INT4_ASYM_G32);
-    return alu ? 12 : 0;
+constexpr int decode_alu_warps(int scheme, int G) {
+    return !(G <= 4 && (scheme == KVQ_INT8_SYM_TOKEN || scheme == KVQ_FP8E4M3_TOKEN ||
+                        scheme == KVQ_INT4_ASYM_G32))
+               ? 0
+               : (scheme == KVQ_INT8_SYM_TOKEN ? 16 : 12);
 }
 
 // Workspace layout for n_ctas persistent CTAs (two partial slots per CTA):
