@@ -71,7 +71,7 @@ struct DecodeCfg {
     // the issue slots and finish first, leaving the SM under-occupied.  INT8
     // fits 128 registers a thread, so 16 warps (with a 2-deep ring each, for
     // shared memory); the others need more registers: 12 warps.
-    static constexpr int WARPS = INT8 ? 16 : 12;
+    static constexpr int WARPS = (INT8 || INT4) ? 16 : 12;
     static_assert(WARPS == decode_alu_warps(SCHEME, G), "the workspace is sized for this many warps");
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int CB = INT4 ? D / 2 : D;        // code bytes per token row
@@ -87,7 +87,6 @@ struct DecodeCfg {
     static constexpr int VZ = KZ + (INT4 ? UNIT * MB : 0);
     static constexpr int QO = VZ + (INT4 ? UNIT * MB : 0);
     static constexpr int STAGE = QO + Q_BYTES;
-    static constexpr int STAGES = WARPS == 16 ? 2 : (STAGE >= 4096) ? 3 : 4;  // ring depth per warp: STAGES-1 units in flight
     // scores: KL lanes per token, CPL channels per lane, TPP tokens per pass.
     // INT8: each lane takes ONE query head (DUP = KL / G lanes per head) and
     // D / DUP of its channels, so its dot product needs no transpose across
@@ -95,7 +94,7 @@ struct DecodeCfg {
     // (or 8; INT4 at d 128: 32, one scale group) channels of all G heads and a
     // transpose-reduction sorts them out.
     static constexpr bool SHEAD = INT8;
-    static constexpr int CPL = SHEAD ? D * G / 8 : (INT4 && D == 128) ? 32 : ((D == 64 && G == 8) ? 8 : 16);
+    static constexpr int CPL = SHEAD ? D * G / 8 : (INT4 && D == 128 && false) ? 32 : ((D == 64 && G == 8) ? 8 : 16);
     static constexpr int KL = SHEAD ? 8 : D / CPL;
     static constexpr int QROWS = SHEAD ? 1 : G;  // query rows held per lane
     static constexpr int TPP = 32 / KL;
@@ -123,7 +122,6 @@ struct DecodeCfg {
     static constexpr int GPL = NGW > DUP ? NGW / DUP : 1;
     // shared memory layout (bytes)
     static constexpr int OFF_STAGES = 0;
-    static constexpr int OFF_W = OFF_STAGES + WARPS * STAGES * STAGE;
     // per warp: weights (fp32 Wt[UNIT][G], or on the dp4a path the words
     // WB[hi, lo][NGW][UNIT/4][G] of 4 token bytes, an order in which the
     // score lanes' stores fall in distinct banks), then the weights'
@@ -136,6 +134,13 @@ struct DecodeCfg {
     static constexpr int W_OFF_AL = W_OFF_WQ + G * 4;
     static constexpr int W_OFF_ZS = W_OFF_AL + G * 4;
     static constexpr int W_BYTES = (W_OFF_ZS + (INT4 ? NGR * G * 4 : 0) + 15) / 16 * 16;
+    // ring depth per warp (STAGES-1 units in flight): as deep as shared memory
+    // allows next to the weights and a plan of MAX_SEQS sequences (227 KB a
+    // CTA, less 4 KB for the static arrays), at most 4
+    static constexpr int FIT = (232448 - 4096 - WARPS * W_BYTES - 16 - (MAX_SEQS + 1) * 4) / (WARPS * STAGE);
+    static constexpr int STAGES = FIT < 4 ? FIT : 4;
+    static_assert(STAGES >= 2, "at least one unit in flight while one is computed");
+    static constexpr int OFF_W = OFF_STAGES + WARPS * STAGES * STAGE;
     static constexpr int OFF_MISC = OFF_W + WARPS * W_BYTES;
     static constexpr int OFF_PLAN = OFF_MISC + 16;
     static size_t smem_bytes(int B) { return OFF_PLAN + (size_t)(B + 1) * 4; }

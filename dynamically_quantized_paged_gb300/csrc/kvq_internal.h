@@ -79,7 +79,7 @@ constexpr int decode_alu_warps(int scheme, int G) {
     return !(G <= 4 && (scheme == KVQ_INT8_SYM_TOKEN || scheme == KVQ_FP8E4M3_TOKEN ||
                         scheme == KVQ_INT4_ASYM_G32))
                ? 0
-               : (scheme == KVQ_INT8_SYM_TOKEN ? 16 : 12);
+               : ((scheme == KVQ_INT8_SYM_TOKEN || scheme == KVQ_INT4_ASYM_G32) ? 16 : 12);
 }
 
 // Workspace layout for n_ctas persistent CTAs (two partial slots per CTA):
