@@ -126,20 +126,26 @@ struct DecodeCfg {
     // WB[hi, lo][NGW][UNIT/4][G] of 4 token bytes, an order in which the
     // score lanes' stores fall in distinct banks), then the weights'
     // fixed-point step WQ[G] (dp4a path), alpha[G], and (INT4) the
-    // zero-point sums ZS[NGR][G] of a finished piece
+    // zero-point sums ZS[NGR][G] of a finished piece, and the queue of the
+    // pieces the feed has reached (b, h, u_lo, u_hi, len, whole, slot; a
+    // negative u_lo ends the list).  The feed runs STAGES - 1 units ahead of
+    // the compute and seeks the next piece as it issues a piece's last unit,
+    // so it is at most STAGES pieces ahead: 8 slots (STAGES <= 4) never
+    // overwrite the compute's current piece.
     static constexpr int NB = UNIT / 4;             // 4-token blocks per unit
     static constexpr int WB_HALF = NGW * NB * G;     // words of one byte plane (hi or lo)
     static constexpr int WB_BYTES = VDP ? 2 * WB_HALF * 4 : UNIT * G * 4;
     static constexpr int W_OFF_WQ = WB_BYTES;
     static constexpr int W_OFF_AL = W_OFF_WQ + G * 4;
     static constexpr int W_OFF_ZS = W_OFF_AL + G * 4;
-    static constexpr int W_BYTES = (W_OFF_ZS + (INT4 ? NGR * G * 4 : 0) + 15) / 16 * 16;
+    static constexpr int W_OFF_PQ = W_OFF_ZS + (INT4 ? NGR * G * 4 : 0);  // piece queue [8][8] int32
+    static constexpr int W_BYTES = (W_OFF_PQ + 8 * 8 * 4 + 15) / 16 * 16;
     // ring depth per warp (STAGES-1 units in flight): as deep as shared memory
     // allows next to the weights and a plan of MAX_SEQS sequences (227 KB a
     // CTA, less 4 KB for the static arrays), at most 4
     static constexpr int FIT = (232448 - 4096 - WARPS * W_BYTES - 16 - (MAX_SEQS + 1) * 4) / (WARPS * STAGE);
     static constexpr int STAGES = FIT < 4 ? FIT : 4;
-    static_assert(STAGES >= 2, "at least one unit in flight while one is computed");
+    static_assert(STAGES >= 2 && STAGES <= 4, "at least one unit in flight while one is computed; the piece queue");
     static constexpr int OFF_W = OFF_STAGES + WARPS * STAGES * STAGE;
     static constexpr int OFF_MISC = OFF_W + WARPS * W_BYTES;
     static constexpr int OFF_PLAN = OFF_MISC + 16;
@@ -252,6 +258,8 @@ decode_partial_kernel(const DecodeParams p) {
     int fu = 0, fua = 0, fub = 0;
     int flp = 0, foff = 0;  // logical page of unit fu and its token offset inside the page
     bool fdone = true;
+    int fq = 0;             // pieces the feed has queued for the compute
+    int* PQ = reinterpret_cast<int*>(smem + C::OFF_W + warp * C::W_BYTES + C::W_OFF_PQ);
     auto feed_seek = [&]() {
         fdone = true;
         while (!fw.done()) {
@@ -263,10 +271,22 @@ decode_partial_kernel(const DecodeParams p) {
                 flp = (fu * UNIT) / P;  // once per piece; then advanced incrementally
                 foff = (fu * UNIT) - flp * P;
                 fdone = false;
+                if (lane == 0) {
+                    int* d = PQ + (fq & 7) * 8;
+                    d[0] = fpc.b;
+                    d[1] = fpc.h;
+                    d[2] = fpc.u_lo;
+                    d[3] = fpc.u_hi;
+                    d[4] = fpc.len;
+                    d[5] = fpc.whole ? 1 : 0;
+                    d[6] = fpc.slot;
+                }
+                ++fq;
                 return;
             }
             fw.next();
         }
+        if (lane == 0) PQ[(fq & 7) * 8 + 2] = -1;  // the end of this warp's pieces
     };
     feed_seek();
     int bt_b = -1, bt0 = 0, pid = -1, pid_next = -1;  // block-table batch [bt0, bt0 + 32) and the next one
@@ -361,13 +381,14 @@ decode_partial_kernel(const DecodeParams p) {
 #pragma unroll 1
     for (int i = 0; i < STAGES_ - 1; ++i) issue_one();  // prologue
     int cst = 0;  // stage the next computed unit sits in
-    PieceWalk walk;
-    walk.begin(plan, prefix, worker, plan.Sw);
-    for (; !walk.done(); walk.next()) {
-        const Piece pc = walk.get(p);
-        int ua, ub;
-        ua = pc.u_lo;
-        ub = pc.u_hi;
+    __syncwarp();  // the queued pieces are visible to every lane
+#pragma unroll 1
+    for (int qi = 0;; ++qi) {
+        const int* pd = PQ + (qi & 7) * 8;  // this piece (read again at its end)
+        const int ua = pd[2];
+        if (ua < 0) break;
+        const int ub = pd[3];
+        const int plen = pd[4];
         uint32_t qw[C::QROWS][C::QW];  // query: INT8/INT4 fixed-point bytes, FP8 fp16 pairs
         float qisum[G];         // INT4: sum of this lane's fixed-point query channels, per head
         float my_sq = 0.0f;     // INT8, INT4: fixed-point step of the lane's score head times the softmax scale
@@ -487,7 +508,7 @@ decode_partial_kernel(const DecodeParams p) {
                     }
                 }
             }
-            int n_valid = pc.len - u * UNIT;
+            int n_valid = plen - u * UNIT;
             n_valid = n_valid > UNIT ? UNIT : n_valid;
             if (badmask & (1u << st)) n_valid = 0;
 
@@ -893,8 +914,8 @@ decode_partial_kernel(const DecodeParams p) {
                 o[g][jj] = v;
             }
         }
-        if (pc.whole) {
-            const OutRow row = out_row(p, ((int64_t)pc.b * p.Hq + (int64_t)pc.h * G) * D);
+        if (pd[5]) {
+            const OutRow row = out_row(p, ((int64_t)pd[0] * p.Hq + (int64_t)pd[1] * G) * D);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float lg = __shfl_sync(0xffffffffu, l_run, g * C::DUP);  // lane g*DUP holds head g
@@ -907,7 +928,7 @@ decode_partial_kernel(const DecodeParams p) {
                 }
             }
         } else {
-            const int64_t slot = pc.slot;
+            const int64_t slot = pd[6];
             if (v_tok == 0) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
