@@ -12,6 +12,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -46,7 +47,11 @@ class CacheStruct(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
                 ("k_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
-                ("k_zeros", ctypes.c_void_p), ("v_zeros", ctypes.c_void_p)]
+                ("k_zeros", ctypes.c_void_p), ("v_zeros", ctypes.c_void_p),
+                ("host_pages", ctypes.c_int32),
+                ("host_k_codes", ctypes.c_void_p), ("host_v_codes", ctypes.c_void_p),
+                ("host_k_scales", ctypes.c_void_p), ("host_v_scales", ctypes.c_void_p),
+                ("host_k_zeros", ctypes.c_void_p), ("host_v_zeros", ctypes.c_void_p)]
 
 
 def _load() -> ctypes.CDLL:
@@ -116,16 +121,23 @@ def cache_bytes(scheme: str | int, num_pages: int, page_size: int, num_kv_heads:
     return c.value, s.value, z.value
 
 
+POOLS = ("k_codes", "v_codes", "k_scales", "v_scales", "k_zeros", "v_zeros")
+
+
 class PagedKVCache:
     """One layer's paged quantized cache: six caller-owned device pools (torch
-    uint8 tensors) laid out as include/kvq.h describes."""
+    uint8 tensors) laid out as include/kvq.h describes, and optionally a host
+    tier of host_pages more pages (page ids num_pages .. num_pages +
+    host_pages - 1) in page-locked host memory that the kernels read and
+    write in place."""
 
     def __init__(self, scheme: str, num_pages: int, page_size: int, num_kv_heads: int,
-                 head_dim: int, device="cuda", zero_init: bool = True):
+                 head_dim: int, device="cuda", zero_init: bool = True, host_pages: int = 0):
         self.scheme = scheme
         self.sid = SCHEMES[scheme]
         self.num_pages, self.page_size = num_pages, page_size
         self.num_kv_heads, self.head_dim = num_kv_heads, head_dim
+        self.host_pages = host_pages
         self.group = 32 if scheme in ("int4", "int4sym") else 0
         cb, sb, zb = cache_bytes(scheme, num_pages, page_size, num_kv_heads, head_dim)
         alloc = torch.zeros if zero_init else torch.empty
@@ -135,18 +147,41 @@ class PagedKVCache:
         self.v_scales = alloc(sb, dtype=torch.uint8, device=device)
         self.k_zeros = alloc(zb, dtype=torch.uint8, device=device) if zb else None
         self.v_zeros = alloc(zb, dtype=torch.uint8, device=device) if zb else None
+        self.host = {}
+        if host_pages > 0:
+            hcb, hsb, hzb = cache_bytes(scheme, host_pages, page_size, num_kv_heads, head_dim)
+            for name, nb in (("k_codes", hcb), ("v_codes", hcb), ("k_scales", hsb), ("v_scales", hsb),
+                             ("k_zeros", hzb), ("v_zeros", hzb)):
+                self.host[name] = torch.zeros(nb, dtype=torch.uint8).pin_memory() if nb else None
+        hp = lambda n: self.host[n].data_ptr() if self.host.get(n) is not None else None  # noqa: E731
         self.struct = CacheStruct(self.sid, num_pages, page_size, num_kv_heads, head_dim, self.group,
                                   self.k_codes.data_ptr(), self.v_codes.data_ptr(),
                                   self.k_scales.data_ptr(), self.v_scales.data_ptr(),
                                   self.k_zeros.data_ptr() if zb else None,
-                                  self.v_zeros.data_ptr() if zb else None)
+                                  self.v_zeros.data_ptr() if zb else None,
+                                  host_pages, hp("k_codes"), hp("v_codes"), hp("k_scales"),
+                                  hp("v_scales"), hp("k_zeros"), hp("v_zeros"))
+
+    def tier_of(self, page: int) -> str:
+        """"device" or "host": where page id `page` lives."""
+        return "device" if page < self.num_pages else "host"
+
+    def pool(self, name: str):
+        """Host copy of one pool over both tiers (uint8, page ids in order:
+        the device tier, then the host tier)."""
+        d = getattr(self, name)
+        if d is None:
+            return None
+        d = d.cpu().numpy()
+        h = self.host.get(name)
+        return d if h is None else np.concatenate([d, h.numpy()])
 
     def codes_rowmajor(self, which: str):
-        """Host copy of the K or V codes (which = "k" or "v") as
-        uint8 [num_pages][num_kv_heads][page_size][code bytes per token]."""
-        t = (self.k_codes if which == "k" else self.v_codes).cpu().numpy()
+        """Host copy of the K or V codes (which = "k" or "v") over both tiers as
+        uint8 [num_pages + host_pages][num_kv_heads][page_size][code bytes per token]."""
+        t = self.pool(which + "_codes")
         cb = self.head_dim // 2 if self.scheme in ("int4", "int4sym") else self.head_dim
-        return t.reshape(self.num_pages, self.num_kv_heads, self.page_size, cb)
+        return t.reshape(self.num_pages + self.host_pages, self.num_kv_heads, self.page_size, cb)
 
     @property
     def nbytes(self) -> int:
@@ -155,7 +190,8 @@ class PagedKVCache:
 
 
 def copy_page(cache: PagedKVCache, src: int, dst: int, stream=None) -> None:
-    """kvq_copy_page: copy-on-write of page src into page dst (every pool)."""
+    """kvq_copy_page: copy page src into page dst (every pool), within a tier
+    (copy-on-write) or between the device and host tiers (offload, fetch)."""
     _check(lib.kvq_copy_page(ctypes.byref(cache.struct), src, dst, _stream(stream)), "kvq_copy_page")
 
 

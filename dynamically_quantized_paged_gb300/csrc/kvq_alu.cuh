@@ -221,6 +221,24 @@ decode_partial_kernel(const DecodeParams p) {
     int64_t* misc = reinterpret_cast<int64_t*>(smem + C::OFF_MISC);
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + C::OFF_PLAN);
 
+    // pool bases of the device tier [0] and the host tier [1]: codes K, V,
+    // scales K, V, zero-points K, V (read per unit from shared memory rather
+    // than held in registers)
+    __shared__ const uint8_t* pool_tab[2][6];
+    if (threadIdx.x == 0) {
+        pool_tab[0][0] = p.c.k_codes;
+        pool_tab[0][1] = p.c.v_codes;
+        pool_tab[0][2] = static_cast<const uint8_t*>(p.c.k_scales);
+        pool_tab[0][3] = static_cast<const uint8_t*>(p.c.v_scales);
+        pool_tab[0][4] = static_cast<const uint8_t*>(p.c.k_zeros);
+        pool_tab[0][5] = static_cast<const uint8_t*>(p.c.v_zeros);
+        pool_tab[1][0] = p.c.hk_codes;
+        pool_tab[1][1] = p.c.hv_codes;
+        pool_tab[1][2] = static_cast<const uint8_t*>(p.c.hk_scales);
+        pool_tab[1][3] = static_cast<const uint8_t*>(p.c.hv_scales);
+        pool_tab[1][4] = static_cast<const uint8_t*>(p.c.hk_zeros);
+        pool_tab[1][5] = static_cast<const uint8_t*>(p.c.hv_zeros);
+    }
     const Plan plan = build_plan<C::THREADS, C::WARPS>(p, prefix, misc);  // contains __syncthreads
     if (blockIdx.x == 0) {
         // publish the plan for the merge kernel: [U, S] then prefix[0..B]
@@ -319,11 +337,14 @@ decode_partial_kernel(const DecodeParams p) {
                     if (NQ % 32 == 0 || i < NQ) cp_async16(stg + C::QO + 16 * i, qsrc + 16 * i);
                 }
             }
-            if (page >= 0 && page < p.c.num_pages) {
+            if (page >= 0 && page < p.c.num_pages + p.c.host_pages) {
                 badmask &= ~(1u << st);
-                const int64_t row = ((int64_t)page * Hkv + fpc.h) * P + foff;
-                const uint8_t* kc = p.c.k_codes + row * C::CB;
-                const uint8_t* vc = p.c.v_codes + row * C::CB;
+                // the page's tier (warp-uniform): its pool bases from the CTA's table
+                const int host = page >= p.c.num_pages;
+                const uint8_t* const* tb = pool_tab[host];
+                const int64_t row = ((int64_t)(page - (host ? p.c.num_pages : 0)) * Hkv + fpc.h) * P + foff;
+                const uint8_t* kc = tb[0] + row * C::CB;
+                const uint8_t* vc = tb[1] + row * C::CB;
                 constexpr int NC = UNIT * C::CB / 16;  // 16-byte pieces of one code run
 #pragma unroll
                 for (int k = 0; k < (NC + 31) / 32; ++k) {
@@ -335,13 +356,13 @@ decode_partial_kernel(const DecodeParams p) {
                 }
                 constexpr int NS = UNIT * C::MB / 16;  // 16-byte pieces of one scale (or zero) run
                 const int which = lane / NS, part = lane % NS;
-                const void* src = nullptr;
-                int dst = 0;
-                if (which == 0) { src = p.c.k_scales; dst = C::KS; }
-                else if (which == 1) { src = p.c.v_scales; dst = C::VS; }
-                else if (C::INT4 && which == 2) { src = p.c.k_zeros; dst = C::KZ; }
-                else if (C::INT4 && which == 3) { src = p.c.v_zeros; dst = C::VZ; }
-                if (src) cp_async16(stg + dst + 16 * part, static_cast<const uint8_t*>(src) + row * C::MB + 16 * part);
+                // lane group `which` copies K scales, V scales, (INT4) K zeros, V zeros
+                constexpr int NARR = C::INT4 ? 4 : 2;
+                static_assert(C::VS == C::KS + UNIT * C::MB && (!C::INT4 || (C::KZ == C::VS + UNIT * C::MB &&
+                                                                               C::VZ == C::KZ + UNIT * C::MB)),
+                              "the scale and zero runs are consecutive in the stage");
+                if (which < NARR)
+                    cp_async16(stg + C::KS + which * (UNIT * C::MB) + 16 * part, tb[2 + which] + row * C::MB + 16 * part);
             } else {
                 badmask |= (1u << st);
                 if (lane == 0) flag_error(p.err, ERR_BAD_TABLE);

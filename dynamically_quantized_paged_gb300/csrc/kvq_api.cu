@@ -49,8 +49,20 @@ kvq_status check_cache(const kvq_cache* c) {
         if (!c->k_zeros || !c->v_zeros || !aligned(c->k_zeros, 16) || !aligned(c->v_zeros, 16))
             return KVQ_ERR_INVALID_ARG;
     }
-    // the pool must be addressable with 64-bit row arithmetic and int32 page ids
-    const int64_t rows = (int64_t)c->num_pages * c->num_kv_heads * c->page_size;
+    if (c->host_pages < 0) return KVQ_ERR_INVALID_ARG;
+    if (c->host_pages > 0) {  // the host tier's pools, as the device tier's
+        const void* hneed[4] = {c->host_k_codes, c->host_v_codes, c->host_k_scales, c->host_v_scales};
+        for (const void* p : hneed)
+            if (!p || !aligned(p, 16)) return KVQ_ERR_INVALID_ARG;
+        if (c->scheme == KVQ_INT4_ASYM_G32 && (!c->host_k_zeros || !c->host_v_zeros ||
+                                               !aligned(c->host_k_zeros, 16) || !aligned(c->host_v_zeros, 16)))
+            return KVQ_ERR_INVALID_ARG;
+    }
+    // the pools must be addressable with 64-bit row arithmetic and int32 page
+    // ids (both tiers)
+    const int64_t pages = (int64_t)c->num_pages + c->host_pages;
+    if (pages > INT32_MAX) return KVQ_ERR_INVALID_ARG;
+    const int64_t rows = pages * c->num_kv_heads * c->page_size;
     if (rows <= 0 || rows > ((int64_t)1 << 40)) return KVQ_ERR_INVALID_ARG;
     return KVQ_OK;
 }
@@ -69,6 +81,14 @@ kvq::CacheView view_of(const kvq_cache* c) {
     v.v_scales = c->v_scales;
     v.k_zeros = c->k_zeros;
     v.v_zeros = c->v_zeros;
+    const bool ht = c->host_pages > 0;
+    v.host_pages = ht ? c->host_pages : 0;
+    v.hk_codes = ht ? static_cast<const uint8_t*>(c->host_k_codes) : nullptr;
+    v.hv_codes = ht ? static_cast<const uint8_t*>(c->host_v_codes) : nullptr;
+    v.hk_scales = ht ? c->host_k_scales : nullptr;
+    v.hv_scales = ht ? c->host_v_scales : nullptr;
+    v.hk_zeros = ht ? c->host_k_zeros : nullptr;
+    v.hv_zeros = ht ? c->host_v_zeros : nullptr;
     return v;
 }
 
@@ -267,7 +287,7 @@ kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_
     if (scheme != cache->scheme) return KVQ_ERR_SCHEME_MISMATCH;
     if (num_tokens < 0) return KVQ_ERR_INVALID_ARG;
     // slots and rows are indexed in 32 bits on the device
-    if ((int64_t)cache->num_pages * cache->page_size >= ((int64_t)1 << 31) ||
+    if (((int64_t)cache->num_pages + cache->host_pages) * cache->page_size >= ((int64_t)1 << 31) ||
         (int64_t)num_tokens * cache->num_kv_heads * 2 >= ((int64_t)1 << 31))
         return KVQ_ERR_INVALID_ARG;
     if (block_table && (num_seqs < 0 || max_pages_per_seq < 1 || !aligned(block_table, 4)))
@@ -297,7 +317,15 @@ kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_
     p.slot_mapping = slot_mapping;
     p.k = static_cast<const uint16_t*>(k);
     p.v = static_cast<const uint16_t*>(v);
-    p.num_slots = (int64_t)cache->num_pages * cache->page_size;
+    p.num_slots = ((int64_t)cache->num_pages + cache->host_pages) * cache->page_size;
+    p.num_pages = cache->num_pages;
+    const bool ht = cache->host_pages > 0;
+    p.hk_codes = ht ? static_cast<uint8_t*>(cache->host_k_codes) : nullptr;
+    p.hv_codes = ht ? static_cast<uint8_t*>(cache->host_v_codes) : nullptr;
+    p.hk_scales = ht ? cache->host_k_scales : nullptr;
+    p.hv_scales = ht ? cache->host_v_scales : nullptr;
+    p.hk_zeros = ht ? cache->host_k_zeros : nullptr;
+    p.hv_zeros = ht ? cache->host_v_zeros : nullptr;
     p.num_tokens = num_tokens;
     p.num_kv_heads = cache->num_kv_heads;
     p.page_size = cache->page_size;
@@ -403,8 +431,8 @@ kvq_status kvq_validate_tables(const kvq_cache* cache, const int32_t* block_tabl
 kvq_status kvq_copy_page(const kvq_cache* cache, int32_t src, int32_t dst, kvq_stream_t stream) {
     kvq_status st = check_cache(cache);
     if (st != KVQ_OK) return st;
-    if (src < 0 || src >= cache->num_pages || dst < 0 || dst >= cache->num_pages || src == dst)
-        return KVQ_ERR_INVALID_ARG;
+    const int64_t total = (int64_t)cache->num_pages + cache->host_pages;
+    if (src < 0 || src >= total || dst < 0 || dst >= total || src == dst) return KVQ_ERR_INVALID_ARG;
     if (current_device() < 0) return KVQ_ERR_CUDA;
     // every pool is page-major: a page's rows ([Hkv][page_size], any interleave
     // inside) are one contiguous block of the same size in each
@@ -412,17 +440,24 @@ kvq_status kvq_copy_page(const kvq_cache* cache, int32_t src, int32_t dst, kvq_s
     const bool int4 = cache->scheme == KVQ_INT4_ASYM_G32, int4s = cache->scheme == KVQ_INT4_SYM_G32;
     const size_t code_b = rows * (int4 || int4s ? cache->head_dim / 2 : cache->head_dim);
     const size_t meta_b = rows * (int4 ? (cache->head_dim / 32) * 2 : int4s ? (cache->head_dim / 32) * 4 : 4);
-    struct Pool { void* base; size_t bytes; } pools[6] = {
-        {cache->k_codes, code_b}, {cache->v_codes, code_b}, {cache->k_scales, meta_b},
-        {cache->v_scales, meta_b}, {int4 ? cache->k_zeros : nullptr, meta_b},
-        {int4 ? cache->v_zeros : nullptr, meta_b}};
+    // pool bases of each tier: device, host
+    struct Pool { void* base[2]; size_t bytes; } pools[6] = {
+        {{cache->k_codes, cache->host_k_codes}, code_b},
+        {{cache->v_codes, cache->host_v_codes}, code_b},
+        {{cache->k_scales, cache->host_k_scales}, meta_b},
+        {{cache->v_scales, cache->host_v_scales}, meta_b},
+        {{int4 ? cache->k_zeros : nullptr, int4 ? cache->host_k_zeros : nullptr}, meta_b},
+        {{int4 ? cache->v_zeros : nullptr, int4 ? cache->host_v_zeros : nullptr}, meta_b}};
+    const int ts = src >= cache->num_pages, td = dst >= cache->num_pages;
+    const size_t is = (size_t)(src - (ts ? cache->num_pages : 0)), id = (size_t)(dst - (td ? cache->num_pages : 0));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     for (const Pool& pl : pools) {
-        if (!pl.base) continue;
-        uint8_t* b = static_cast<uint8_t*>(pl.base);
-        if (cudaMemcpyAsync(b + (size_t)dst * pl.bytes, b + (size_t)src * pl.bytes, pl.bytes,
-                            cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-            return KVQ_ERR_CUDA;
+        if (!pl.base[0]) continue;
+        const uint8_t* from = static_cast<const uint8_t*>(pl.base[ts]) + is * pl.bytes;
+        uint8_t* to = static_cast<uint8_t*>(pl.base[td]) + id * pl.bytes;
+        // the host tier is page-locked memory the device addresses (unified
+        // addressing): the runtime infers each copy's direction
+        if (cudaMemcpyAsync(to, from, pl.bytes, cudaMemcpyDefault, s) != cudaSuccess) return KVQ_ERR_CUDA;
     }
     return KVQ_OK;
 }

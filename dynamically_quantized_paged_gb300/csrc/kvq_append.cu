@@ -130,7 +130,11 @@ __device__ __forceinline__ void e4m3_quotients(const float* x, float s, float r,
 // and stored.  LPR lanes hold a row; `li` is this lane's index in it.
 template <int SCHEME, int D, int LPR>
 __device__ __forceinline__ void quantize_store(const AppendParams& p, const uint4 (&raw)[2], int kv, bool valid,
-                                               int64_t prow, int li) {
+                                               bool host, int64_t prow, int li) {
+    // the pools of this row's tier (device, or host for page ids >= num_pages)
+    uint8_t* const codes = host ? (kv ? p.hv_codes : p.hk_codes) : (kv ? p.v_codes : p.k_codes);
+    void* const scales = host ? (kv ? p.hv_scales : p.hk_scales) : (kv ? p.v_scales : p.k_scales);
+    void* const zeros = host ? (kv ? p.hv_zeros : p.hk_zeros) : (kv ? p.v_zeros : p.k_zeros);
     float x[16];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -168,9 +172,9 @@ __device__ __forceinline__ void quantize_store(const AppendParams& p, const uint
             }
         }
         if (valid) {
-            uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * D + li * 16;
+            uint8_t* dst = codes + prow * D + li * 16;
             *reinterpret_cast<uint4*>(dst) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-            if (li == 0) static_cast<float*>(kv ? p.v_scales : p.k_scales)[prow] = scale;
+            if (li == 0) static_cast<float*>(scales)[prow] = scale;
         }
     } else {
         // INT4: a 32-channel group is two lanes (xor 1)
@@ -194,8 +198,7 @@ __device__ __forceinline__ void quantize_store(const AppendParams& p, const uint
                 for (int i = 0; i < 8; ++i) w |= ((uint32_t)q[8 * h + i] & 0xFu) << (4 * i);
                 packed[h] = w;
             }
-            if (valid && (li & 1) == 0)
-                static_cast<float*>(kv ? p.v_scales : p.k_scales)[prow * (D / 32) + li / 2] = sc;
+            if (valid && (li & 1) == 0) static_cast<float*>(scales)[prow * (D / 32) + li / 2] = sc;
         } else {
             float mn = x[0], mx = x[0];
 #pragma unroll
@@ -227,12 +230,12 @@ __device__ __forceinline__ void quantize_store(const AppendParams& p, const uint
             }
             if (valid && (li & 1) == 0) {
                 const int64_t gi = prow * (D / 32) + li / 2;
-                static_cast<__half*>(kv ? p.v_scales : p.k_scales)[gi] = sh;
-                static_cast<__half*>(kv ? p.v_zeros : p.k_zeros)[gi] = zh;
+                static_cast<__half*>(scales)[gi] = sh;
+                static_cast<__half*>(zeros)[gi] = zh;
             }
         }
         if (valid) {
-            uint8_t* dst = (kv ? p.v_codes : p.k_codes) + prow * (D / 2) + li * 8;
+            uint8_t* dst = codes + prow * (D / 2) + li * 8;
             *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
         }
     }
@@ -339,12 +342,14 @@ __global__ void __launch_bounds__(APPEND_THREADS, 2) append_kernel(AppendParams 
         const bool valid = sl >= 0;
         const uint32_t t = fast_div((uint32_t)(in_chunk ? pi : 0), p.heads_mul, p.heads_shift);
         const int h = (int)((uint32_t)(in_chunk ? pi : 0) - t * (uint32_t)H);
-        // pool row of this (slot, head): [page][head][offset]
+        // pool row of this (slot, head): [page][head][offset] in the page's tier
         const uint32_t pg = valid ? fast_div((uint32_t)sl, p.page_mul, p.page_shift) : 0u;
         const uint32_t off = valid ? (uint32_t)sl - pg * (uint32_t)p.page_size : 0u;
-        const int64_t prow = ((int64_t)pg * H + h) * p.page_size + off;
-        quantize_store<SCHEME, D, LPR>(p, rk, 0, valid, prow, li);
-        quantize_store<SCHEME, D, LPR>(p, rv, 1, valid, prow, li);
+        const bool host = pg >= (uint32_t)p.num_pages;
+        const uint32_t pi_t = host ? pg - (uint32_t)p.num_pages : pg;
+        const int64_t prow = ((int64_t)pi_t * H + h) * p.page_size + off;
+        quantize_store<SCHEME, D, LPR>(p, rk, 0, valid, host, prow, li);
+        quantize_store<SCHEME, D, LPR>(p, rv, 1, valid, host, prow, li);
     }
     cp_async_wait<0>();
 }
@@ -436,7 +441,7 @@ cudaError_t launch_validate(const CacheView& c, const int32_t* block_table,
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    validate_kernel<<<(unsigned)blocks, 256, 0, s>>>(c.num_pages, c.page_size, block_table,
+    validate_kernel<<<(unsigned)blocks, 256, 0, s>>>(c.num_pages + c.host_pages, c.page_size, block_table,
                                                      seq_lens, B, max_pages, err);
     return cudaGetLastError();
 }

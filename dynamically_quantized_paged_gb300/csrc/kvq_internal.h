@@ -29,7 +29,41 @@ struct CacheView {
     const void* v_scales;
     const void* k_zeros;
     const void* v_zeros;
+    // host tier: page ids [num_pages, num_pages + host_pages) live in these
+    // pools (page-locked host memory the device reads in place)
+    int host_pages;
+    const uint8_t* hk_codes;
+    const uint8_t* hv_codes;
+    const void* hk_scales;
+    const void* hv_scales;
+    const void* hk_zeros;
+    const void* hv_zeros;
 };
+
+// The pools that hold page id `page` (the device tier below num_pages, the
+// host tier from there on) and the page's index within them.  `page` must
+// lie in [0, num_pages + host_pages).
+struct PagePools {
+    const uint8_t* k_codes;
+    const uint8_t* v_codes;
+    const uint8_t* k_scales;
+    const uint8_t* v_scales;
+    const uint8_t* k_zeros;
+    const uint8_t* v_zeros;
+    int index;
+};
+__host__ __device__ inline PagePools page_pools(const CacheView& c, int page) {
+    const bool host = page >= c.num_pages;
+    PagePools r;
+    r.k_codes = host ? c.hk_codes : c.k_codes;
+    r.v_codes = host ? c.hv_codes : c.v_codes;
+    r.k_scales = static_cast<const uint8_t*>(host ? c.hk_scales : c.k_scales);
+    r.v_scales = static_cast<const uint8_t*>(host ? c.hv_scales : c.v_scales);
+    r.k_zeros = static_cast<const uint8_t*>(host ? c.hk_zeros : c.k_zeros);
+    r.v_zeros = static_cast<const uint8_t*>(host ? c.hv_zeros : c.v_zeros);
+    r.index = host ? page - c.num_pages : page;
+    return r;
+}
 
 struct AppendParams {
     uint8_t* k_codes;
@@ -38,10 +72,18 @@ struct AppendParams {
     void* v_scales;
     void* k_zeros;
     void* v_zeros;
+    // host tier (pages num_pages .. num_pages + host_pages - 1)
+    uint8_t* hk_codes;
+    uint8_t* hv_codes;
+    void* hk_scales;
+    void* hv_scales;
+    void* hk_zeros;
+    void* hv_zeros;
+    int num_pages;
     const int64_t* slot_mapping;
     const uint16_t* k;  // bf16 bits
     const uint16_t* v;
-    int64_t num_slots;  // num_pages * page_size
+    int64_t num_slots;  // (num_pages + host_pages) * page_size: both tiers
     int num_tokens, num_kv_heads, page_size;
     unsigned* err;
     // n / num_kv_heads and n / page_size for 0 <= n < 2^31 as

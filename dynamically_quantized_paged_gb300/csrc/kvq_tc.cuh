@@ -522,15 +522,17 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
             }
             // units whose page id lies outside the pool are not copied (every
             // warp sees the whole mask; warp 0 publishes it)
-            const uint32_t bad = __ballot_sync(0xffffffffu, lane < nu && (my_page < 0 || my_page >= p.c.num_pages));
+            const uint32_t bad =
+                __ballot_sync(0xffffffffu, lane < nu && (my_page < 0 || my_page >= p.c.num_pages + p.c.host_pages));
             for (int uu = pw; uu < nu; uu += C::NPW) {
                 const int page = __shfl_sync(0xffffffffu, my_page, uu);
                 if ((bad >> uu) & 1u) continue;
                 const int u = it.u0 + uu;
                 const int off = u * UNIT - ((u * UNIT) / P) * P;
-                const int64_t row = ((int64_t)page * Hkv + pc.h) * P + off;
-                const uint8_t* kc = p.c.k_codes + row * C::CB;
-                const uint8_t* vc = p.c.v_codes + row * C::CB;
+                const PagePools pp = page_pools(p.c, page);  // the page's tier (warp-uniform)
+                const int64_t row = ((int64_t)pp.index * Hkv + pc.h) * P + off;
+                const uint8_t* kc = pp.k_codes + row * C::CB;
+                const uint8_t* vc = pp.v_codes + row * C::CB;
                 constexpr int NC = UNIT * C::NCH;  // 16-byte chunks of one unit's codes
 #pragma unroll
                 for (int k = 0; k < (NC + 31) / 32; ++k) {
@@ -543,15 +545,13 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                 }
                 constexpr int NS16 = UNIT * C::MB / 16;  // 16-byte chunks of one scale (or zero) run
                 const int which = lane / NS16, part = lane % NS16;
-                const void* src = nullptr;
+                const uint8_t* src = nullptr;
                 int dst = 0;
-                if (which == 0) { src = p.c.k_scales; dst = C::RKS; }
-                else if (which == 1) { src = p.c.v_scales; dst = C::RVS; }
-                else if (C::INT4 && !C::SYM4 && which == 2) { src = p.c.k_zeros; dst = C::RKZ; }
-                else if (C::INT4 && !C::SYM4 && which == 3) { src = p.c.v_zeros; dst = C::RVZ; }
-                if (src)
-                    cp_async16(st + dst + uu * UNIT * C::MB + 16 * part,
-                               static_cast<const uint8_t*>(src) + row * C::MB + 16 * part);
+                if (which == 0) { src = pp.k_scales; dst = C::RKS; }
+                else if (which == 1) { src = pp.v_scales; dst = C::RVS; }
+                else if (C::INT4 && !C::SYM4 && which == 2) { src = pp.k_zeros; dst = C::RKZ; }
+                else if (C::INT4 && !C::SYM4 && which == 3) { src = pp.v_zeros; dst = C::RVZ; }
+                if (src) cp_async16(st + dst + uu * UNIT * C::MB + 16 * part, src + row * C::MB + 16 * part);
             }
             if (pw == 0 && lane == 0) {
                 sm.stage_bad()[s] = bad;

@@ -14,7 +14,9 @@
  *
  * Conventions shared by every call:
  *  - Every pointer argument named as device memory must be device memory of
- *    the current CUDA device, allocated and owned by the caller.  The library
+ *    the current CUDA device, allocated and owned by the caller (the one
+ *    exception: the host-tier pools of kvq_cache, below, are page-locked
+ *    host memory that the device addresses directly).  The library
  *    calls no allocator and keeps no pointer after a call returns; its own
  *    device memory is static: a per-device error word, and the fixed scratch
  *    array of kvq_decode_attn_noalloc.
@@ -91,7 +93,22 @@ typedef enum kvq_scheme {
  * The token stored at physical slot s lives in page s / page_size at
  * offset s % page_size.  Supported: head_dim 64 or 128, page_size a positive
  * multiple of 16, num_kv_heads >= 1.  Several layers share one block table
- * by using one descriptor per layer. */
+ * by using one descriptor per layer.
+ *
+ * Cold-page tier ([P3] section "KV Cache Offloading: Moving Data Between GPU
+ * and CPU": inactive cache kept in CPU RAM instead of GPU memory).  With
+ * host_pages > 0 the page ids num_pages .. num_pages + host_pages - 1 name
+ * pages of a second set of pools, host_k_codes .. host_v_zeros, laid out
+ * exactly as above with host_pages pages and living in page-locked host
+ * memory that the device can address (cudaHostAlloc / pinned memory: on
+ * GB300 the GPU reads it over NVLink-C2C).  That id range is the residency
+ * map: a block-table entry >= num_pages says the page is host-resident.
+ * Every call treats both tiers alike: the append writes, and both decode
+ * kernels read, host-resident pages in place (no staging copy), and
+ * kvq_copy_page moves a page between the tiers (offload: device page to a
+ * free host page; fetch: the reverse), after which the caller rewrites the
+ * block-table entry.  host_pages = 0 (with NULL host pools) is the plain
+ * device-only cache.  A slot s names page s / page_size in either tier. */
 typedef struct kvq_cache {
     int32_t scheme;       /* kvq_scheme */
     int32_t num_pages;
@@ -105,6 +122,13 @@ typedef struct kvq_cache {
     void* v_scales;
     void* k_zeros;        /* INT4 only */
     void* v_zeros;        /* INT4 only */
+    int32_t host_pages;   /* pages of the host tier (0: none) */
+    void* host_k_codes;   /* host-tier pools, same layout with host_pages pages */
+    void* host_v_codes;
+    void* host_k_scales;
+    void* host_v_scales;
+    void* host_k_zeros;   /* asymmetric INT4 only */
+    void* host_v_zeros;   /* asymmetric INT4 only */
 } kvq_cache;
 
 /* Human-readable name of a status.  Never NULL; static storage. */
@@ -297,13 +321,16 @@ kvq_status kvq_share_pages(kvq_allocator* alloc, int32_t n, const int32_t* pages
 kvq_status kvq_page_refcount(const kvq_allocator* alloc, int32_t page, int32_t* refs);
 int32_t kvq_allocator_free_count(const kvq_allocator* alloc);
 
-/* Copy-on-write of one page: copies every pool's contents of page src (codes,
- * scales, INT4 zero-points: all of its KV heads and slots) to page dst on the
- * stream, so that a sequence whose shared prefix ends inside a page can take
- * its own copy of that page before appending past the prefix (then update its
- * block-table entry and drop its reference to src).  One device-to-device
- * copy per pool; no kernel.  KVQ_ERR_INVALID_ARG if src or dst is outside the
- * pool or src == dst; KVQ_ERR_CUDA if a copy cannot be enqueued. */
+/* Copies every pool's contents of page src (codes, scales, INT4 zero-points:
+ * all of its KV heads and slots) to page dst on the stream.  Two uses:
+ * copy-on-write, so that a sequence whose shared prefix ends inside a page
+ * can take its own copy of that page before appending past the prefix; and
+ * moving a page between the device and host tiers (offload of a cold page,
+ * fetch of a page needed again).  Either way the caller then updates the
+ * block-table entry and drops its reference to src.  One asynchronous copy
+ * per pool (device-to-device, device-to-host, host-to-device or host-to-
+ * host); no kernel.  KVQ_ERR_INVALID_ARG if src or dst is outside both
+ * tiers or src == dst; KVQ_ERR_CUDA if a copy cannot be enqueued. */
 kvq_status kvq_copy_page(const kvq_cache* cache, int32_t src, int32_t dst, kvq_stream_t stream);
 
 #ifdef __cplusplus

@@ -30,7 +30,10 @@ class Case:
     def __init__(self, w: inp.Workload, lens: np.ndarray, layer: int = 0, spare: int = 3,
                  oracle_seqs=None, chunk: int = 4096, table_seed: int | None = None,
                  block_table: np.ndarray | None = None, num_pages: int | None = None,
-                 kv_override=None):
+                 kv_override=None, host_pages: int = 0, extra_host_pages: int = 0):
+        """host_pages: the last host_pages of the table's page ids live in the
+        cache's host tier; extra_host_pages: more host-tier pages beyond the
+        table's ids (targets for moving pages between the tiers)."""
         self.w, self.layer = w, layer
         self.lens = np.asarray(lens, np.int32)
         if block_table is None:
@@ -38,7 +41,8 @@ class Case:
                                                     w.seed if table_seed is None else table_seed, spare)
         self.bt, self.num_pages = block_table, num_pages
         self.oracle_seqs = list(range(len(self.lens))) if oracle_seqs is None else list(oracle_seqs)
-        self.g = kvq.PagedKVCache(w.scheme, num_pages, w.page_size, w.kv_heads, w.head_dim, device=DEV)
+        self.g = kvq.PagedKVCache(w.scheme, num_pages - host_pages, w.page_size, w.kv_heads, w.head_dim,
+                                  device=DEV, host_pages=host_pages + extra_host_pages)
         self.o = oracle.OracleCache(w.scheme, num_pages, w.page_size, w.kv_heads, w.head_dim)
         for b, L in enumerate(self.lens):
             for s0 in range(0, int(L), chunk):
@@ -97,8 +101,10 @@ class Case:
         names = ["k_codes", "v_codes", "k_scales", "v_scales"] + (["k_zeros", "v_zeros"] if w.scheme == "int4" else [])
         rows = None if full else self.used_rows()
         for name in names:
-            g = self.g.codes_rowmajor(name[0]).reshape(-1) if "codes" in name else getattr(self.g, name).cpu().numpy()
-            o = getattr(self.o, name).view(np.uint8)
+            g = self.g.pool(name)  # both tiers, page ids in order
+            o = getattr(self.o, name).view(np.uint8).reshape(-1)
+            assert not g[o.size:].any(), f"{name}: bytes written past the table's pages"
+            g = g[:o.size]
             width = cb if "codes" in name else mb
             if rows is not None:
                 g = g.reshape(-1, width)[rows]

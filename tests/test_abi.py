@@ -13,6 +13,8 @@ import torch
 import dynamically_quantized_paged_gb300 as kvq
 import oracle
 
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kvq.h")
 
 
@@ -177,12 +179,48 @@ def test_copy_page_argument_errors_before_any_device_access():
     assert kvq.lib.kvq_copy_page(ctypes.byref(fake_cache(head_dim=96)), 0, 1, None) == 7
 
 
-def fake_cache(scheme=1, head_dim=128, page_size=16, heads=8, align=256, group=32, num_pages=4):
+def fake_cache(scheme=1, head_dim=128, page_size=16, heads=8, align=256, group=32, num_pages=4, host_pages=0):
     base = 1 << 20  # never dereferenced: argument checks run before any device access
     p = lambda i: base + i * (1 << 16) + (0 if align >= 16 else align)
+    h = lambda i: p(6 + i) if host_pages > 0 else None
     return kvq.CacheStruct(scheme, num_pages, page_size, heads, head_dim, group if scheme == 3 else 0,
                            p(0), p(1), p(2), p(3), p(4) if scheme == 3 else None,
-                           p(5) if scheme == 3 else None)
+                           p(5) if scheme == 3 else None,
+                           host_pages, h(0), h(1), h(2), h(3), h(4) if scheme == 3 else None,
+                           h(5) if scheme == 3 else None)
+
+
+def test_cache_struct_layout_matches_the_header():
+    """The binding's mirror of kvq_cache: field order and offsets as in
+    include/kvq.h (int32 fields, then the six pools, then the host tier)."""
+    hdr = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    body = re.search(r"typedef struct kvq_cache \{(.*?)\} kvq_cache;", hdr, re.S).group(1)
+    names = re.findall(r"^\s*(?:int32_t|void\*)\s+(\w+);", body, re.M)
+    assert names == [f[0] for f in kvq.CacheStruct._fields_]
+    off = {f[0]: getattr(kvq.CacheStruct, f[0]).offset for f in kvq.CacheStruct._fields_}
+    assert off["k_codes"] == 24 and off["host_pages"] == 72 and off["host_k_codes"] == 80
+    assert ctypes.sizeof(kvq.CacheStruct) == 128
+
+
+def test_host_tier_argument_errors_before_any_device_access():
+    """A host tier needs its pools (16-byte aligned; zero-point pools for
+    asymmetric INT4) and a non-negative size; page ids of both tiers are
+    valid copy_page arguments, ids past both are not."""
+    c = fake_cache(num_pages=4, host_pages=3)
+    for src, dst in ((0, 7), (7, 0), (-1, 5), (6, 6)):
+        assert kvq.lib.kvq_copy_page(ctypes.byref(c), src, dst, None) == 1
+    assert call_append(fake_cache(host_pages=-1)) == 1
+    c = fake_cache(host_pages=2)
+    c.host_v_scales = None
+    assert call_append(c) == 1
+    c = fake_cache(host_pages=2)
+    c.host_k_codes += 8
+    assert call_append(c) == 1
+    c = fake_cache(scheme=3, host_pages=2)
+    c.host_v_zeros = None
+    assert call_append(c) == 1
+    # both tiers count toward the 2^31-slot limit of 32-bit slot indexing
+    assert call_append(fake_cache(num_pages=1 << 26, host_pages=1 << 26)) == 1
 
 
 def call_append(c, scheme=None, T=1, k=1 << 24, v=1 << 25, slots=1 << 26):

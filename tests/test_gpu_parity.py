@@ -470,3 +470,71 @@ def test_shared_prefix_pages_with_copy_on_write(scheme):
     ref = o.decode_attn(q, bt, lens, w.q_heads, 0.0)
     assert_attn_close(out.cpu().numpy().astype(np.float64), ref, f"{scheme} shared prefix")
     alloc.close()
+
+
+# ------------------------------------------------------------ host (cold) tier
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4", "int4sym"])
+@pytest.mark.parametrize("Hq", [32, 64], ids=["gqa4", "gqa8"])
+def test_host_tier_pages_are_written_and_read_in_place(scheme, Hq):
+    """Half of the pool's pages live in the host tier (page-locked host
+    memory): the append writes them and both decode kernels (GQA 4 on the CUDA
+    cores, GQA 8 on the tensor cores) read them in place.  The pools over both
+    tiers equal the oracle's one-tier pool byte for byte, and the decode equals
+    that of an all-device cache with the same tables bit for bit."""
+    w = small(scheme, Hq, 8, 128, 16)
+    lens = np.array([700, 1, 2049, 16, 333, 0, 1500], np.int32)
+    a = Case(w, lens, spare=4, table_seed=3)
+    split = Case(w, lens, spare=4, table_seed=3, host_pages=a.num_pages // 2)
+    assert split.g.num_pages + split.g.host_pages == a.num_pages
+    used = np.unique(split.bt[split.bt >= 0])
+    assert (used >= split.g.num_pages).any() and (used < split.g.num_pages).any()
+    split.compare_cache(full=True)
+    got = split.decode()
+    assert np.array_equal(got, a.decode())
+    assert_attn_close(got, split.oracle_decode(), f"{scheme} G{Hq // 8} host tier")
+
+
+@pytest.mark.parametrize("scheme", ["int8", "int4"])
+def test_pages_offloaded_to_the_host_tier_and_fetched_back(scheme):
+    """kvq_copy_page moves pages between the tiers: every other page of the
+    first sequence goes to free host-tier pages (offload; the block table is
+    rewritten), then comes back to fresh device pages (fetch).  The decode
+    is bit-identical after each move, and a token appended while its page is
+    host-resident lands there."""
+    w = small(scheme, 32, 8, 128, 16)
+    lens = np.array([1000, 300], np.int32)
+    c = Case(w, lens, spare=70, extra_host_pages=40)
+    ref = c.decode()
+    ever_used = set(c.bt[c.bt >= 0].tolist())
+    n0 = (int(lens[0]) + 15) // 16
+    moved = list(range(0, n0, 2))
+    homes = c.bt[0, moved].copy()
+    for j, lp in enumerate(moved):           # offload
+        dst = c.g.num_pages + j
+        kvq.copy_page(c.g, int(c.bt[0, lp]), dst)
+        c.bt[0, lp] = dst
+    assert all(c.g.tier_of(int(x)) == "host" for x in c.bt[0, moved])
+    assert np.array_equal(c.decode(), ref)
+    used = set(c.bt[c.bt >= 0].tolist())
+    fresh = [x for x in range(c.g.num_pages) if x not in used and x not in set(homes.tolist())][:len(moved)]
+    assert len(fresh) == len(moved)
+    for lp, dst in zip(moved, fresh):        # fetch
+        kvq.copy_page(c.g, int(c.bt[0, lp]), dst)
+        c.bt[0, lp] = dst
+    assert all(c.g.tier_of(int(x)) == "device" for x in c.bt[0, moved])
+    assert np.array_equal(c.decode(), ref)
+    # append one token into a host-resident page: the page's bytes match
+    # the same append into a device page
+    host_page = c.g.num_pages + 39
+    dev_page = [x for x in range(c.g.num_pages) if x not in ever_used and x not in fresh][0]  # never written
+    k, v = inp.kv_rows(w, 0, 5, 0, 1)
+    kvq.append(c.g, dev(np.array([host_page * 16 + 3], np.int64)), dev_bits(k), dev_bits(v))
+    kvq.append(c.g, dev(np.array([dev_page * 16 + 3], np.int64)), dev_bits(k), dev_bits(v))
+    torch.cuda.synchronize()
+    assert kvq.last_device_error() == kvq.OK
+    for name in ["k_codes", "v_codes", "k_scales", "v_scales"] + (["k_zeros", "v_zeros"] if scheme == "int4" else []):
+        pool = c.g.pool(name)
+        per_page = pool.size // (c.g.num_pages + c.g.host_pages)
+        hp = pool[host_page * per_page:(host_page + 1) * per_page]
+        dp = pool[dev_page * per_page:(dev_page + 1) * per_page]
+        assert hp.any() and np.array_equal(hp, dp), name
