@@ -61,6 +61,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 HEADLINE = 4
+HOST_FRACTION = 0.0  # fraction of each layer's page ids in the host tier (--host-fraction)
 
 
 # ---------------------------------------------------------------- accounting
@@ -310,7 +311,11 @@ class Bench:
         workers = min(16, os.cpu_count() or 1)
         with ThreadPoolExecutor(max_workers=workers) as ex:
             for layer in range(w.layers):
-                c = kvq.PagedKVCache(w.scheme, num_pages, P, w.kv_heads, w.head_dim, device=dev, zero_init=False)
+                # the last host pages of the id space live in the cache's host
+                # tier (page-locked host memory read over NVLink-C2C)
+                host = min(int(round(HOST_FRACTION * num_pages)), num_pages - 1)
+                c = kvq.PagedKVCache(w.scheme, num_pages - host, P, w.kv_heads, w.head_dim, device=dev,
+                                     zero_init=False, host_pages=host)
                 ks, vs = [], []
                 # the rows are generated on host threads, a bounded window ahead
                 pending = {}
@@ -568,7 +573,8 @@ def measure_workload(w, dev, local_rank, args, world, rank, barrier, headline: b
                    "cached_tokens": int(inp.seq_lens(w).sum()), "kv_codes": w.scheme,
                    "l2": "flushed before every timed step (256 MB write, then a 256 MB read, outside the timed events)",
                    "parallelism": (f"sequences partitioned over {world} GPUs, no collective" if world > 1
-                                   else "1 GPU")},
+                                   else "1 GPU"),
+                   **({"host_tier_fraction": HOST_FRACTION} if HOST_FRACTION > 0 else {})},
         "hbm_frac_of_8tbs": round(job_throughput(total_step, ms_per_step) / NOMINAL_HBM_GBS / max(world, 1), 4),
         "decode_kv_gbs_step": round(job_throughput(total_decode, ms_per_step), 2),
         "decode_tokens_per_s": round(total_seqs / (ms_per_step * 1e-3), 1),
@@ -677,12 +683,19 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling runs only: override the workload's layer count (the per-launch work is "
                          "per layer; the JSON line names the layers it ran)")
+    ap.add_argument("--host-fraction", type=float, default=0.0,
+                    help="place this fraction of each layer's page ids in the cache's host tier (read in place "
+                         "over NVLink-C2C); 0 (default): every page in device memory")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the eager launches only (default: the step is also replayed from a CUDA graph "
                          "and that time is the headline value)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if not 0.0 <= args.host_fraction <= 1.0:
+        ap.error("--host-fraction must lie in [0, 1]")
+    global HOST_FRACTION
+    HOST_FRACTION = args.host_fraction
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
