@@ -62,6 +62,7 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 HEADLINE = 4
 HOST_FRACTION = 0.0  # fraction of each layer's page ids in the host tier (--host-fraction)
+APPEND_MODE = "separate"  # --append-mode
 
 
 # ---------------------------------------------------------------- accounting
@@ -116,14 +117,16 @@ def partition_sequences(lens, world: int) -> list:
     return [np.array(sorted(s), np.int64) for s in shares]
 
 
-def append_line(nb: dict, w: inp.Workload, k1_mean_ms: float, peak_gbs: float) -> dict:
+def append_line(nb: dict, w: inp.Workload, k1_mean_ms: float, peak_gbs: float, fused: bool = False) -> dict:
     """The quantize-append launch on its own: tokens per second, and its
     algorithmic bytes (bf16 K/V read, slots read, codes and scales written)
-    per second against the HBM peak."""
+    per second against the HBM peak.  Fused into the decode launch, its time
+    is taken as that whole launch's (k1_mean_ms is then the decode's)."""
     T = nb["append_tokens"] // w.layers      # tokens per launch
     b = nb["append"] // w.layers             # algorithmic bytes per launch
     t = k1_mean_ms * 1e-3
-    return {"kernel": "append_kernel (quantize-append)", "tokens_per_launch": T,
+    return {"kernel": "fused into the decode launch (its whole time counted)" if fused
+            else "append_kernel (quantize-append)", "tokens_per_launch": T,
             "mean_launch_us": round(k1_mean_ms * 1e3, 3), "tokens_per_s": round(T / t, 1),
             "algorithmic_bytes_per_launch": b, "achieved_gbs": round(b / t / 1e9, 2),
             "roofline_tokens_per_s": round(peak_gbs * 1e9 / (b / T), 1) if T else None,
@@ -291,6 +294,12 @@ class Bench:
         self.seqs = np.asarray(seqs, np.int64)
         self.lens = inp.seq_lens(w)[self.seqs]
         self.n_new = step_plan(w, self.lens)
+        # the decode that appends its step's token (one launch per layer)
+        # serves steps of one new token per sequence on the CUDA-core kernel
+        # (GQA <= 4 of INT8, FP8, asymmetric INT4)
+        eligible = bool(np.all(self.n_new == 1)) and w.scheme in ("int8", "fp8", "int4") and \
+            w.q_heads // w.kv_heads <= 4
+        self.fused = eligible and APPEND_MODE == "fused"
         B, P = len(self.seqs), w.page_size
         need = inp.pages_needed(self.lens, P)
         self.max_pages = int(need.max())
@@ -371,10 +380,15 @@ class Bench:
         for layer, c in enumerate(self.caches):
             if events is not None:
                 events[layer][2].record()
-            kvq.append(c, slots, k_new[layer], v_new[layer], stream=stream)
+            if not self.fused:
+                kvq.append(c, slots, k_new[layer], v_new[layer], stream=stream)
             if events is not None:
                 events[layer][0].record()
-            kvq.decode_attn(c, q[layer], bt, lens, out, self.ws, stream=stream)  # one launch, splits merged in place
+            if self.fused:  # one launch: the decode quantizes and stores each sequence's new token itself
+                kvq.decode_attn_append(c, k_new[layer], v_new[layer], q[layer], bt, lens, out, self.ws,
+                                       stream=stream)
+            else:
+                kvq.decode_attn(c, q[layer], bt, lens, out, self.ws, stream=stream)  # one launch, splits merged in place
             if events is not None:
                 events[layer][1].record()
 
@@ -523,11 +537,14 @@ def describe(w: inp.Workload) -> str:
             f"d={w.head_dim}, page {w.page_size}, {w.scheme} KV codes, {step}")
 
 
-def roofline_block(w, nb, k2_ms, peak, peak_kind):
+def roofline_block(w, nb, k2_ms, peak, peak_kind, fused=False):
+    """The decode launch against the HBM roofline; with the append fused into
+    it, the launch's algorithmic bytes include the append's."""
     mean = statistics.mean(k2_ms)
-    b = nb["decode"] // w.layers
+    b = (nb["step"] if fused else nb["decode"]) // w.layers
     achieved = b / (mean * 1e-3) / 1e9
-    return {"kernel": "decode kernel (split-K fused-dequant decode, merge fused)",
+    return {"kernel": "decode kernel (split-K fused-dequant decode, merge fused"
+                      + (", appends each sequence's new token)" if fused else ")"),
             "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -574,14 +591,16 @@ def measure_workload(w, dev, local_rank, args, world, rank, barrier, headline: b
                    "l2": "flushed before every timed step (256 MB write, then a 256 MB read, outside the timed events)",
                    "parallelism": (f"sequences partitioned over {world} GPUs, no collective" if world > 1
                                    else "1 GPU"),
-                   **({"host_tier_fraction": HOST_FRACTION} if HOST_FRACTION > 0 else {})},
+                   **({"host_tier_fraction": HOST_FRACTION} if HOST_FRACTION > 0 else {}),
+                   "append": ("fused into each layer's decode launch" if bench.fused
+                              else "append kernel, then the decode (programmatic launch overlap)")},
         "hbm_frac_of_8tbs": round(job_throughput(total_step, ms_per_step) / NOMINAL_HBM_GBS / max(world, 1), 4),
         "decode_kv_gbs_step": round(job_throughput(total_decode, ms_per_step), 2),
         "decode_tokens_per_s": round(total_seqs / (ms_per_step * 1e-3), 1),
         "append_tokens_per_s_step": round(total_append / (ms_per_step * 1e-3), 1),
         "algorithmic_bytes_per_step": total_step,
-        "roofline": roofline_block(w, nb, k2_ms, peak, peak_kind),
-        "append": append_line(nb, w, statistics.mean(k1_ms), peak),
+        "roofline": roofline_block(w, nb, k2_ms, peak, peak_kind, fused=bench.fused),
+        "append": append_line(nb, w, statistics.mean(k2_ms if bench.fused else k1_ms), peak, fused=bench.fused),
         "kernel_loop": {"steps": loop_steps, "wall_s": round(loop_wall, 3),
                         "what": "eager steps, each launch bracketed by CUDA events; the clocks below are "
                                 "sampled across the timed steps and this loop"},
@@ -686,6 +705,10 @@ def main(argv=None):
     ap.add_argument("--host-fraction", type=float, default=0.0,
                     help="place this fraction of each layer's page ids in the cache's host tier (read in place "
                          "over NVLink-C2C); 0 (default): every page in device memory")
+    ap.add_argument("--append-mode", default="separate", choices=["separate", "fused"],
+                    help="separate (default): the append kernel, then the decode; fused: each layer's step is "
+                         "one decode launch that appends its token itself (steps of one new token per sequence "
+                         "on the CUDA-core kernel; elsewhere separate)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the eager launches only (default: the step is also replayed from a CUDA graph "
                          "and that time is the headline value)")
@@ -694,8 +717,9 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if not 0.0 <= args.host_fraction <= 1.0:
         ap.error("--host-fraction must lie in [0, 1]")
-    global HOST_FRACTION
+    global HOST_FRACTION, APPEND_MODE
     HOST_FRACTION = args.host_fraction
+    APPEND_MODE = args.append_mode
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

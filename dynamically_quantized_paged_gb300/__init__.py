@@ -32,7 +32,8 @@ EXPORTS = ["kvq_status_string", "kvq_cache_bytes", "kvq_append", "kvq_decode_wor
            "kvq_decode_attn", "kvq_decode_partial", "kvq_decode_merge", "kvq_validate_tables",
            "kvq_last_device_error", "kvq_allocator_create", "kvq_allocator_destroy",
            "kvq_alloc_pages", "kvq_free_pages", "kvq_allocator_free_count", "kvq_decode_attn_noalloc",
-           "kvq_share_pages", "kvq_page_refcount", "kvq_copy_page", "kvq_decode_attn_out"]
+           "kvq_share_pages", "kvq_page_refcount", "kvq_copy_page", "kvq_decode_attn_out",
+           "kvq_decode_attn_append"]
 
 
 class KvqError(RuntimeError):
@@ -69,6 +70,8 @@ def _load() -> ctypes.CDLL:
     dec = [cachep, P, P, P, P, i32, i32, i32, ctypes.c_float, P, ctypes.c_size_t, P]
     L.kvq_decode_attn.argtypes = dec
     L.kvq_decode_attn_out.argtypes = [cachep, P, P, P, P, i32, i32, i32, i32, ctypes.c_float, P, ctypes.c_size_t, P]
+    L.kvq_decode_attn_append.argtypes = [cachep, P, P, P, P, P, P, i32, i32, i32, i32, ctypes.c_float, P,
+                                         ctypes.c_size_t, P]
     L.kvq_decode_partial.argtypes = dec
     L.kvq_decode_merge.argtypes = dec
     L.kvq_validate_tables.argtypes = [cachep, P, P, i32, i32, P]
@@ -256,6 +259,31 @@ def decode_attn(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
     else:
         _decode_call(lib.kvq_decode_attn, "kvq_decode_attn", cache, q, block_table, seq_lens, out,
                      workspace, softmax_scale, stream)
+    return out
+
+
+def decode_attn_append(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                       block_table: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor,
+                       workspace: torch.Tensor, softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+    """kvq_decode_attn_append: one decode step that appends its own token --
+    k_new, v_new bf16 [B, Hkv, d] are each sequence's new key and value,
+    stored at position seq_lens[b] - 1 (seq_lens include them) -- then the
+    attention of q over the whole cache into out (fp32 or bf16).  The same
+    pools and output as append followed by decode_attn."""
+    B = seq_lens.numel()
+    if k_new.shape != v_new.shape or k_new.numel() != B * cache.num_kv_heads * cache.head_dim \
+            or k_new.element_size() != 2:
+        raise ValueError("kvq_decode_attn_append: k_new, v_new must be bf16 [B, Hkv, d]")
+    if q.dim() != 3 or q.shape[0] != B or tuple(out.shape) != tuple(q.shape) or block_table.shape[0] != B:
+        raise ValueError("kvq_decode_attn_append: shapes of q, out, block_table, seq_lens do not agree")
+    if out.dtype not in (torch.float32, torch.bfloat16) or q.element_size() != 2 \
+            or seq_lens.element_size() != 4 or block_table.element_size() != 4:
+        raise ValueError("kvq_decode_attn_append: q bf16, out fp32 or bf16, tables int32")
+    dt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    _check(lib.kvq_decode_attn_append(ctypes.byref(cache.struct), _ptr(k_new), _ptr(v_new), _ptr(q),
+                                      _ptr(block_table), _ptr(seq_lens), _ptr(out), dt, B, q.shape[1],
+                                      block_table.shape[1], float(softmax_scale), _ptr(workspace),
+                                      workspace.numel(), _stream(stream)), "kvq_decode_attn_append")
     return out
 
 

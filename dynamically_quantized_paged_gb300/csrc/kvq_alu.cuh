@@ -59,6 +59,7 @@
 #include "kvq_decode.cuh"
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_quant.cuh"
 
 namespace kvq {
 namespace alu {
@@ -127,8 +128,9 @@ struct DecodeCfg {
     // score lanes' stores fall in distinct banks), then the weights'
     // fixed-point step WQ[G] (dp4a path), alpha[G], and (INT4) the
     // zero-point sums ZS[NGR][G] of a finished piece, and the queue of the
-    // pieces the feed has reached (b, h, u_lo, u_hi, len, whole, slot; a
-    // negative u_lo ends the list).  The feed runs STAGES - 1 units ahead of
+    // pieces the feed has reached (b, h, u_lo, u_hi, len, whole, slot, and
+    // whether the piece appends its sequence's new token; a negative u_lo
+    // ends the list).  The feed runs STAGES - 1 units ahead of
     // the compute and seeks the next piece as it issues a piece's last unit,
     // so it is at most STAGES pieces ahead: 8 slots (STAGES <= 4) never
     // overwrite the compute's current piece.
@@ -139,7 +141,10 @@ struct DecodeCfg {
     static constexpr int W_OFF_AL = W_OFF_WQ + G * 4;
     static constexpr int W_OFF_ZS = W_OFF_AL + G * 4;
     static constexpr int W_OFF_PQ = W_OFF_ZS + (INT4 ? NGR * G * 4 : 0);  // piece queue [8][8] int32
-    static constexpr int W_BYTES = (W_OFF_PQ + 8 * 8 * 4 + 15) / 16 * 16;
+    // the appended token's codes, scales (and zeros) as the cache stores them:
+    // K codes, V codes [CB], K scales, V scales, K zeros, V zeros [MB]
+    static constexpr int W_OFF_NB = (W_OFF_PQ + 8 * 8 * 4 + 15) / 16 * 16;  // 16-byte stores into it
+    static constexpr int W_BYTES = (W_OFF_NB + 2 * CB + 4 * MB + 15) / 16 * 16;
     // ring depth per warp (STAGES-1 units in flight): as deep as shared memory
     // allows next to the weights and a plan of MAX_SEQS sequences (227 KB a
     // CTA, less 4 KB for the static arrays), at most 4
@@ -152,7 +157,7 @@ struct DecodeCfg {
     static size_t smem_bytes(int B) { return OFF_PLAN + (size_t)(B + 1) * 4; }
     static_assert(G <= KL, "each lane must end the reduction holding one head");
     static_assert(STAGE % 16 == 0 && Q_BYTES % 16 == 0 && (UNIT * MB) % 16 == 0, "16-byte copies");
-    static_assert(OFF_W % 16 == 0, "alignment");
+    static_assert(OFF_W % 16 == 0 && W_BYTES % 16 == 0 && W_OFF_NB % 16 == 0, "alignment");
     static_assert(4 * (UNIT * MB / 16) <= 32, "one lane per 16 bytes of scales and zeros");
     static_assert(!VDP || PASSES == 4 || PASSES == 2, "a lane's weight bytes fill a word or a half word");
     static_assert(!VDP || (NGW % GPL == 0 && NGW / GPL <= DUP), "every group has a writer lane");
@@ -205,7 +210,9 @@ struct EndPiece {
     int slot;       // CTA partial slot, or -1: the segment ends here (final rows)
 };
 
-template <int SCHEME, int D, int G>
+// APP: the instantiation of a decode that appends its step's token (kept
+// apart so that the plain decode carries none of its registers)
+template <int SCHEME, int D, int G, bool APP>
 __global__ void __launch_bounds__(DecodeCfg<SCHEME, D, G>::THREADS, 1)
 decode_partial_kernel(const DecodeParams p) {
     using C = DecodeCfg<SCHEME, D, G>;
@@ -277,6 +284,7 @@ decode_partial_kernel(const DecodeParams p) {
     int flp = 0, foff = 0;  // logical page of unit fu and its token offset inside the page
     bool fdone = true;
     int fq = 0;             // pieces the feed has queued for the compute
+    bool fnew = false;      // the current piece appends its sequence's new token
     int* PQ = reinterpret_cast<int*>(smem + C::OFF_W + warp * C::W_BYTES + C::W_OFF_PQ);
     auto feed_seek = [&]() {
         fdone = true;
@@ -289,6 +297,9 @@ decode_partial_kernel(const DecodeParams p) {
                 flp = (fu * UNIT) / P;  // once per piece; then advanced incrementally
                 foff = (fu * UNIT) - flp * P;
                 fdone = false;
+                // the piece holds its sequence's last position: with an append,
+                // the new token is quantized at the piece's first unit
+                fnew = APP && fpc.len > 0 && (int64_t)fpc.u_hi * UNIT >= fpc.len;
                 if (lane == 0) {
                     int* d = PQ + (fq & 7) * 8;
                     d[0] = fpc.b;
@@ -298,6 +309,7 @@ decode_partial_kernel(const DecodeParams p) {
                     d[4] = fpc.len;
                     d[5] = fpc.whole ? 1 : 0;
                     d[6] = fpc.slot;
+                    d[7] = fnew ? 1 : 0;
                 }
                 ++fq;
                 return;
@@ -327,6 +339,16 @@ decode_partial_kernel(const DecodeParams p) {
                 pid_next = (bt0 + 32 + lane < p.max_pages) ? __ldg(bt_row + bt0 + 32 + lane) : -1;
             }
             const int page = __shfl_sync(0xffffffffu, pid, lp - bt0);
+            if (fu == fua && fnew) {
+                // the new token's bf16 K and V rows of this head and the
+                // block-table entry of the sequence's last position, read at the
+                // piece's start: brought into L2 now
+                constexpr int NP = D * 2 / 16;  // 16-byte pieces of one bf16 row
+                const int64_t nr = ((int64_t)fpc.b * Hkv + fpc.h) * D;
+                if (lane < 2 * NP)
+                    prefetch_l2(reinterpret_cast<const uint8_t*>((lane < NP ? p.k_new : p.v_new) + nr) + 16 * (lane % NP));
+                if (lane == 0) prefetch_l2(bt_row + (fpc.len - 1) / P);
+            }
             if (fu == fua) {  // the piece's query rows travel with the warp's first unit
                 const uint8_t* qsrc =
                     reinterpret_cast<const uint8_t*>(p.q + ((int64_t)fpc.b * p.Hq + (int64_t)fpc.h * G) * D);
@@ -410,6 +432,39 @@ decode_partial_kernel(const DecodeParams p) {
         if (ua < 0) break;
         const int ub = pd[3];
         const int plen = pd[4];
+        const bool pd7 = pd[7] != 0;  // the piece appends its sequence's new token
+        if (APP && pd7) {
+            // a decode that appends its step's token: before the piece's units
+            // (outside the unit loop, so that the quantization shares no
+            // registers with the loop's state), the warp quantizes the token by
+            // the append's rule (the same device code) into the cache and into
+            // its buffer NB, from its bf16 rows (prefetched into L2 by the feed).
+            // This warp alone reads that slot in the launch.
+            uint8_t* nb = wbase + C::W_OFF_NB;
+            constexpr int LPR = D / 16;
+            const int r = (lane / LPR) & 1;  // 0: K row, 1: V row (lanes past 2 LPR repeat them)
+            const int li = lane % LPR;
+            const int64_t nr = ((int64_t)pd[0] * Hkv + pd[1]) * D;
+            const uint4* src = reinterpret_cast<const uint4*>((r ? p.v_new : p.k_new) + nr) + li * 2;
+            const uint4 raw[2] = {__ldg(src), __ldg(src + 1)};
+            const int page = __ldg(p.block_table + (int64_t)pd[0] * p.max_pages + (plen - 1) / P);
+            const LaneCodes lc = quantize_lane<SCHEME, LPR>(raw);
+            const bool ok = page >= 0 && page < p.c.num_pages + p.c.host_pages;
+            if (lane < 2 * LPR) {
+                store_lane<SCHEME, D>(lc, nb + r * C::CB, nb + 2 * C::CB + r * C::MB,
+                                      nb + 2 * C::CB + (2 + r) * C::MB, 0, li);
+                if (ok) {
+                    const int tier = page >= p.c.num_pages;
+                    const uint8_t* const* tb = pool_tab[tier];
+                    const int64_t prow = ((int64_t)(page - (tier ? p.c.num_pages : 0)) * Hkv + pd[1]) * P +
+                                         (plen - 1) % P;
+                    store_lane<SCHEME, D>(lc, const_cast<uint8_t*>(tb[r]), const_cast<uint8_t*>(tb[2 + r]),
+                                          const_cast<uint8_t*>(tb[4 + r]), prow, li);
+                }
+            }
+            if (!ok && lane == 0) flag_error(p.err, ERR_BAD_TABLE);
+            __syncwarp();
+        }
         uint32_t qw[C::QROWS][C::QW];  // query: INT8/INT4 fixed-point bytes, FP8 fp16 pairs
         float qisum[G];         // INT4: sum of this lane's fixed-point query channels, per head
         float my_sq = 0.0f;     // INT8, INT4: fixed-point step of the lane's score head times the softmax scale
@@ -432,6 +487,31 @@ decode_partial_kernel(const DecodeParams p) {
             const int st = cst;
             cst = (cst + 1 == STAGES_) ? 0 : cst + 1;
             const uint8_t* stg = ring + st * C::STAGE;
+            if (APP && pd7 && u == ub - 1) {
+                // the unit of the sequence's last position: the appended token
+                // (quantized at the piece's start into NB) is patched into the
+                // staged page, whose copy may predate the cache write
+                const uint8_t* nb = wbase + C::W_OFF_NB;
+                {
+                    uint8_t* sw = ring + st * C::STAGE;
+                    const int tl = plen - 1 - u * UNIT;
+                    const uint32_t* n32 = reinterpret_cast<const uint32_t*>(nb);
+                    for (int i = lane; i < C::CB / 4; i += 32) {
+                        reinterpret_cast<uint32_t*>(sw + C::KC + tl * C::CB)[i] = n32[i];
+                        reinterpret_cast<uint32_t*>(sw + C::VC + tl * C::CB)[i] = n32[C::CB / 4 + i];
+                    }
+                    constexpr int MW = C::MB / 4;  // words of one token's scales (or zeros)
+                    if (lane < MW) {
+                        reinterpret_cast<uint32_t*>(sw + C::KS + tl * C::MB)[lane] = n32[2 * C::CB / 4 + lane];
+                        reinterpret_cast<uint32_t*>(sw + C::VS + tl * C::MB)[lane] = n32[2 * C::CB / 4 + MW + lane];
+                        if constexpr (C::INT4) {
+                            reinterpret_cast<uint32_t*>(sw + C::KZ + tl * C::MB)[lane] = n32[2 * C::CB / 4 + 2 * MW + lane];
+                            reinterpret_cast<uint32_t*>(sw + C::VZ + tl * C::MB)[lane] = n32[2 * C::CB / 4 + 3 * MW + lane];
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
             if (u == ua && C::SHEAD) {
                 // ---- this lane's head of the query -> 16-bit fixed point bytes:
                 // q ~ sq * qi, qi = 256 hi + lo (hi a signed byte, lo an unsigned
@@ -1043,7 +1123,7 @@ decode_partial_kernel(const DecodeParams p) {
 // Shared memory attribute per device, set once (host-only state).  Safe to
 // call from several host threads: the attribute call is idempotent, and the
 // flag only records that it succeeded.
-template <int SCHEME, int D, int G>
+template <int SCHEME, int D, int G, bool APP>
 cudaError_t configure_decode_t() {
     using C = DecodeCfg<SCHEME, D, G>;
     static std::atomic<int> configured[64];
@@ -1051,7 +1131,7 @@ cudaError_t configure_decode_t() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
     if (!configured[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(decode_partial_kernel<SCHEME, D, G>,
+        e = cudaFuncSetAttribute(decode_partial_kernel<SCHEME, D, G, APP>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(MAX_SEQS));
         if (e != cudaSuccess) return e;
         configured[dev].store(1, std::memory_order_release);
@@ -1071,8 +1151,8 @@ int decode_ctas_per_sm_t(int /*B*/) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     int n = cached[dev].load(std::memory_order_acquire);
     if (n > 0) return n;
-    if (configure_decode_t<SCHEME, D, G>() != cudaSuccess) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partial_kernel<SCHEME, D, G>, C::THREADS,
+    if (configure_decode_t<SCHEME, D, G, false>() != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partial_kernel<SCHEME, D, G, false>, C::THREADS,
                                                       C::smem_bytes(MAX_SEQS)) != cudaSuccess)
         return 0;
     if (n > 0) cached[dev].store(n, std::memory_order_release);
@@ -1082,7 +1162,8 @@ int decode_ctas_per_sm_t(int /*B*/) {
 template <int SCHEME, int D, int G>
 cudaError_t launch_decode_partial_t(const DecodeParams& p, cudaStream_t s) {
     using C = DecodeCfg<SCHEME, D, G>;
-    cudaError_t e = configure_decode_t<SCHEME, D, G>();
+    const bool app = p.k_new != nullptr;
+    cudaError_t e = app ? configure_decode_t<SCHEME, D, G, true>() : configure_decode_t<SCHEME, D, G, false>();
     if (e != cudaSuccess) return e;
     // programmatic stream serialization: the grid may be scheduled while the
     // kernel ahead of it (typically the append) runs; it waits for it in-kernel
@@ -1096,7 +1177,8 @@ cudaError_t launch_decode_partial_t(const DecodeParams& p, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_partial_kernel<SCHEME, D, G>, p);
+    e = app ? cudaLaunchKernelEx(&cfg, decode_partial_kernel<SCHEME, D, G, true>, p)
+            : cudaLaunchKernelEx(&cfg, decode_partial_kernel<SCHEME, D, G, false>, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -176,6 +176,7 @@ kvq_status prepare_decode(const kvq_cache* cache, const void* q, const int32_t* 
     p.gen = next_generation();
     p.seg_ctr = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) +
                                                       kvq::decode_counter_offset(n_ctas, G, cache->head_dim, B));
+    p.k_new = p.v_new = nullptr;
     return KVQ_OK;
 }
 
@@ -279,6 +280,36 @@ kvq_status kvq_cache_bytes(int32_t scheme, int32_t num_pages, int32_t page_size,
     return KVQ_OK;
 }
 
+// The append kernel's arguments for num_tokens rows of k, v into the slots
+// slot_mapping of the cache (both tiers).
+static kvq::AppendParams append_params(const kvq_cache* cache, const int64_t* slot_mapping, const void* k, const void* v,
+                                int32_t num_tokens, unsigned* err) {
+    kvq::AppendParams p;
+    p.k_codes = static_cast<uint8_t*>(cache->k_codes);
+    p.v_codes = static_cast<uint8_t*>(cache->v_codes);
+    p.k_scales = cache->k_scales;
+    p.v_scales = cache->v_scales;
+    p.k_zeros = cache->k_zeros;
+    p.v_zeros = cache->v_zeros;
+    p.slot_mapping = slot_mapping;
+    p.k = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.num_slots = ((int64_t)cache->num_pages + cache->host_pages) * cache->page_size;
+    p.num_pages = cache->num_pages;
+    const bool ht = cache->host_pages > 0;
+    p.hk_codes = ht ? static_cast<uint8_t*>(cache->host_k_codes) : nullptr;
+    p.hv_codes = ht ? static_cast<uint8_t*>(cache->host_v_codes) : nullptr;
+    p.hk_scales = ht ? cache->host_k_scales : nullptr;
+    p.hv_scales = ht ? cache->host_v_scales : nullptr;
+    p.hk_zeros = ht ? cache->host_k_zeros : nullptr;
+    p.hv_zeros = ht ? cache->host_v_zeros : nullptr;
+    p.num_tokens = num_tokens;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.page_size = cache->page_size;
+    p.err = err;
+    return p;
+}
+
 kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_t num_seqs,
                       int32_t max_pages_per_seq, const int64_t* slot_mapping, const void* k,
                       const void* v, int32_t num_tokens, int32_t scheme, kvq_stream_t stream) {
@@ -307,29 +338,7 @@ kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_
             return KVQ_ERR_CUDA;
     }
     if (num_tokens == 0) return KVQ_OK;
-    kvq::AppendParams p;
-    p.k_codes = static_cast<uint8_t*>(cache->k_codes);
-    p.v_codes = static_cast<uint8_t*>(cache->v_codes);
-    p.k_scales = cache->k_scales;
-    p.v_scales = cache->v_scales;
-    p.k_zeros = cache->k_zeros;
-    p.v_zeros = cache->v_zeros;
-    p.slot_mapping = slot_mapping;
-    p.k = static_cast<const uint16_t*>(k);
-    p.v = static_cast<const uint16_t*>(v);
-    p.num_slots = ((int64_t)cache->num_pages + cache->host_pages) * cache->page_size;
-    p.num_pages = cache->num_pages;
-    const bool ht = cache->host_pages > 0;
-    p.hk_codes = ht ? static_cast<uint8_t*>(cache->host_k_codes) : nullptr;
-    p.hv_codes = ht ? static_cast<uint8_t*>(cache->host_v_codes) : nullptr;
-    p.hk_scales = ht ? cache->host_k_scales : nullptr;
-    p.hv_scales = ht ? cache->host_v_scales : nullptr;
-    p.hk_zeros = ht ? cache->host_k_zeros : nullptr;
-    p.hv_zeros = ht ? cache->host_v_zeros : nullptr;
-    p.num_tokens = num_tokens;
-    p.num_kv_heads = cache->num_kv_heads;
-    p.page_size = cache->page_size;
-    p.err = err;
+    const kvq::AppendParams p = append_params(cache, slot_mapping, k, v, num_tokens, err);
     if (kvq::launch_append(p, cache->scheme, cache->head_dim, s) != cudaSuccess) return KVQ_ERR_CUDA;
     return KVQ_OK;
 }
@@ -408,6 +417,44 @@ kvq_status kvq_decode_attn_out(const kvq_cache* cache, const void* q, const int3
     p.out_bf16 = out_dtype == KVQ_OUT_BF16;
     if (kvq::launch_decode_partial(p, G, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_attn_append(const kvq_cache* cache, const void* k_new, const void* v_new, const void* q,
+                                  const int32_t* block_table, const int32_t* seq_lens, void* out,
+                                  int32_t out_dtype, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_pages_per_seq, float softmax_scale, void* workspace,
+                                  size_t workspace_bytes, kvq_stream_t stream) {
+    if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
+    kvq::DecodeParams p;
+    int G = 0;
+    kvq_status st = prepare_decode(cache, q, block_table, seq_lens, out, num_seqs, num_q_heads,
+                                   max_pages_per_seq, softmax_scale, workspace, workspace_bytes, p, G);
+    if (st != KVQ_OK || num_seqs == 0) return st;
+    if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return KVQ_ERR_INVALID_ARG;
+    if (((int64_t)cache->num_pages + cache->host_pages) * cache->page_size >= ((int64_t)1 << 31))
+        return KVQ_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    p.fuse_merge = 1;
+    p.out_bf16 = out_dtype == KVQ_OUT_BF16;
+    if (kvq::decode_alu_warps(cache->scheme, G) > 0) {
+        // one launch: the warp that reads a sequence's last position quantizes
+        // its new token there and writes it to the cache
+        p.k_new = static_cast<const uint16_t*>(k_new);
+        p.v_new = static_cast<const uint16_t*>(v_new);
+        if (kvq::launch_decode_partial(p, G, s) != cudaSuccess) return KVQ_ERR_CUDA;
+        return KVQ_OK;
+    }
+    // the tensor-core kernel: the append kernel first (slots from the tables,
+    // kept in the partials area of the workspace, which the decode writes only
+    // after the append has completed), then the decode
+    int64_t* slots = reinterpret_cast<int64_t*>(p.ws_o);
+    if (kvq::launch_last_slots(p.c, block_table, seq_lens, num_seqs, max_pages_per_seq, slots, p.err, s) !=
+        cudaSuccess)
+        return KVQ_ERR_CUDA;
+    const kvq::AppendParams ap = append_params(cache, slots, k_new, v_new, num_seqs, p.err);
+    if (kvq::launch_append(ap, cache->scheme, cache->head_dim, s) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (kvq::launch_decode_partial(p, G, s) != cudaSuccess) return KVQ_ERR_CUDA;
     return KVQ_OK;
 }
 

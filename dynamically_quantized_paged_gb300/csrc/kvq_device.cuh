@@ -37,6 +37,10 @@ __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddep
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
+// Brings the line holding `p` into L2 (no register result, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 // 8-byte asynchronous copy global -> shared (through L1; both addresses
 // 8-byte aligned).
 __device__ __forceinline__ void cp_async8(void* dst, const void* src) {

@@ -112,6 +112,12 @@ struct DecodeParams {
     int out_bf16;                       // 1: the output rows are bf16 (round to nearest even), else fp32
     uint32_t gen;                       // call generation tagging the arrival counters
     unsigned long long* seg_ctr;        // [B * Hkv] arrival counters: (gen << 32) | arrivals
+    // the step's appended token (CUDA-core kernel): bf16 [B][Hkv][D] key and
+    // value of each sequence's last position (seq_lens[b] - 1), quantized by
+    // the warp that reads that position and written to the cache by it; null
+    // when the call appends nothing
+    const uint16_t* k_new;
+    const uint16_t* v_new;
 };
 
 // The CUDA-core kernel (kvq_alu.cuh) serves GQA ratios up to 4 of the INT8,
@@ -149,6 +155,11 @@ inline size_t decode_workspace_bytes(int n_ctas, int G, int D, int B, int Hkv, i
 }
 
 cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaStream_t s);
+// slots[b] = the physical slot of position seq_lens[b] - 1 of sequence b (from
+// its block-table row), -1 for an empty sequence or a page id outside the
+// pool (flagged)
+cudaError_t launch_last_slots(const CacheView& c, const int32_t* block_table, const int32_t* seq_lens, int B,
+                              int max_pages, int64_t* slots, unsigned* err, cudaStream_t s);
 cudaError_t launch_decode_partial(const DecodeParams& p, int G, cudaStream_t s);
 cudaError_t launch_decode_merge(const DecodeParams& p, int G, cudaStream_t s);
 // Resident decode CTAs per SM for this configuration (0 if the query fails).

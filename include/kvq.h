@@ -224,6 +224,30 @@ kvq_status kvq_decode_attn_out(const kvq_cache* cache, const void* q, const int3
                                int32_t num_q_heads, int32_t max_pages_per_seq, float softmax_scale,
                                void* workspace, size_t workspace_bytes, kvq_stream_t stream);
 
+/* One decode step that appends its own token ([P1] section "Recap of KV
+ * Caching": each step stores the new token's key and value, then attends
+ * over the whole cache; [P2] "Technical Architecture": capture, quantize,
+ * store, fused dequantized attention).  Equivalent to kvq_append of one new
+ * token per sequence followed by kvq_decode_attn_out, and bit-identical to
+ * that pair (pools and output):
+ *   k_new, v_new  device, bf16 [num_seqs][num_kv_heads][head_dim], 16-byte
+ *                 aligned: each sequence's new key and value projections;
+ *   seq_lens      counts that INCLUDE the new token, which is stored at
+ *                 position seq_lens[b] - 1 of sequence b: the slot its
+ *                 block-table row names for that position (a sequence of
+ *                 length 0 appends nothing).
+ * Other arguments, rules and errors as kvq_decode_attn_out.  Where the
+ * CUDA-core kernel serves the GQA ratio (up to 4 for INT8, FP8 and
+ * asymmetric INT4) this is ONE launch: the warp that reads a sequence's last
+ * position quantizes the new token by the append's rule (the same device
+ * code) into its staged copy of the page and into the cache.  Elsewhere it
+ * is the append kernel followed by the decode, on the stream. */
+kvq_status kvq_decode_attn_append(const kvq_cache* cache, const void* k_new, const void* v_new, const void* q,
+                                  const int32_t* block_table, const int32_t* seq_lens, void* out,
+                                  int32_t out_dtype, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_pages_per_seq, float softmax_scale, void* workspace,
+                                  size_t workspace_bytes, kvq_stream_t stream);
+
 /* The first launch of the two-launch form of kvq_decode_attn: every
  * (sequence, KV head) whose tokens one CTA covers entirely gets its final
  * output row; the rest leave split partials (max, sum, unnormalized output)

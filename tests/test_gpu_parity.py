@@ -538,3 +538,75 @@ def test_pages_offloaded_to_the_host_tier_and_fetched_back(scheme):
         hp = pool[host_page * per_page:(host_page + 1) * per_page]
         dp = pool[dev_page * per_page:(dev_page + 1) * per_page]
         assert hp.any() and np.array_equal(hp, dp), name
+
+
+# --------------------------------------------------- decode that appends its token
+@pytest.mark.parametrize("scheme,Hq,D,P", [("int8", 32, 128, 16), ("int8", 8, 64, 32), ("fp8", 16, 128, 16),
+                                           ("int4", 32, 128, 32), ("int4", 16, 64, 16), ("int8", 64, 128, 16),
+                                           ("int4sym", 32, 128, 16)],
+                         ids=lambda x: str(x))
+@pytest.mark.parametrize("host", [False, True], ids=["device", "host-tier"])
+def test_decode_that_appends_its_token_equals_append_then_decode(scheme, Hq, D, P, host):
+    """kvq_decode_attn_append (one launch on the CUDA-core kernel, the
+    append kernel then the decode on the tensor-core one) leaves the same
+    pools and the same output, bit for bit, as kvq_append of each sequence's
+    new token followed by kvq_decode_attn; also replayed from a CUDA graph,
+    with part of the pages in the host tier, and with bf16 output."""
+    w = small(scheme, Hq, 8, D, P)
+    full = np.array([3001, 17, 1, 0, 800, 2500, 32, 33], np.int32)
+    bt, num_pages = inp.page_table(full, P, w.seed, 3)
+    hp = num_pages // 3 if host else 0
+    a = Case(w, np.maximum(full - 1, 0), block_table=bt, num_pages=num_pages, host_pages=hp)
+    b = Case(w, np.maximum(full - 1, 0), block_table=bt, num_pages=num_pages, host_pages=hp, oracle_seqs=[])
+    H = w.kv_heads
+    k_new = np.zeros((len(full), H, D), np.uint16)
+    v_new = np.zeros((len(full), H, D), np.uint16)
+    for i, L in enumerate(full):
+        if L > 0:
+            k, v = inp.kv_rows(w, 0, i, int(L) - 1, int(L))
+            k_new[i], v_new[i] = k.reshape(H, D), v.reshape(H, D)
+    live = np.nonzero(full > 0)[0]
+    slots = np.concatenate([inp.slots(bt, int(i), np.array([full[i] - 1]), P) for i in live])
+    assert a.o.append(slots, k_new[live].reshape(-1, H, D), v_new[live].reshape(-1, H, D)) == 0
+    ref = a.o.decode_attn(a.q, bt, full, w.q_heads, 0.0)
+
+    q, d_bt, d_len = dev_bits(a.q), dev(bt), dev(full)
+    # a: the fused call
+    out_a = torch.full((len(full), w.q_heads, D), float("nan"), dtype=torch.float32, device=DEV)
+    ws_a = kvq.alloc_workspace(a.g, len(full), w.q_heads, bt.shape[1], device=DEV)
+    kvq.decode_attn_append(a.g, dev_bits(k_new), dev_bits(v_new), q, d_bt, d_len, out_a, ws_a)
+    assert kvq.last_device_error() == kvq.OK
+    # b: append then decode
+    out_b = torch.full_like(out_a, float("nan"))
+    ws_b = kvq.alloc_workspace(b.g, len(full), w.q_heads, bt.shape[1], device=DEV)
+    kvq.append(b.g, dev(slots), dev_bits(k_new[live]), dev_bits(v_new[live]))
+    kvq.decode_attn(b.g, q, d_bt, d_len, out_b, ws_b)
+    assert kvq.last_device_error() == kvq.OK
+    got = out_a.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, out_b.cpu().numpy().astype(np.float64))
+    for name in kvq.POOLS:
+        ga, gb = a.g.pool(name), b.g.pool(name)
+        assert (ga is None and gb is None) or np.array_equal(ga, gb), name
+    a.compare_cache(full=True)
+    assert_attn_close(got, ref, f"{scheme} decode with append")
+    assert np.all(got[3] == 0)  # the empty sequence
+
+    # replayed from a CUDA graph (the token is re-quantized to the same bytes)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    dk, dv = dev_bits(k_new), dev_bits(v_new)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        kvq.decode_attn_append(a.g, dk, dv, q, d_bt, d_len, out_a, ws_a, stream=stream)
+    for _ in range(2):
+        out_a.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert kvq.last_device_error() == kvq.OK
+        assert np.array_equal(out_a.cpu().numpy().astype(np.float64), got)
+    a.compare_cache(full=True)
+    # bf16 output: the fp32 result rounded to nearest even
+    out16 = torch.empty((len(full), w.q_heads, D), dtype=torch.bfloat16, device=DEV)
+    kvq.decode_attn_append(a.g, dk, dv, q, d_bt, d_len, out16, ws_a)
+    assert kvq.last_device_error() == kvq.OK
+    assert torch.equal(out16, out_a.to(torch.bfloat16))
