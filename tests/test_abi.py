@@ -288,3 +288,15 @@ def test_decode_attn_out_rejects_an_unknown_output_dtype():
     st = kvq.lib.kvq_decode_attn_out(None, None, None, None, None, 7, 1, 8, 1, ctypes.c_float(0.0), None, 0, None)
     assert st == 1  # KVQ_ERR_INVALID_ARG
 
+
+
+def test_decode_attn_append_argument_errors_before_any_launch():
+    c = fake_cache()
+    call = lambda c, dt=0, Hq=32: kvq.lib.kvq_decode_attn_append(  # noqa: E731
+        ctypes.byref(c), 1 << 23, 1 << 22, 1 << 24, 1 << 25, 1 << 26, 1 << 27, dt, 2, Hq, 4, 0.0,
+        1 << 28, 1 << 30, None)
+    assert call(c, dt=7) == 1                  # unknown output dtype
+    assert call(c, Hq=24) == 7                 # GQA ratio 3
+    assert call(fake_cache(head_dim=96)) == 7  # unsupported head_dim
+    assert kvq.lib.kvq_decode_attn_append(None, None, None, None, None, None, None, 0, 2, 32, 4, 0.0,
+                                          None, 0, None) == 1
