@@ -92,10 +92,10 @@ struct DecodeCfg {
     // INT8: each lane takes ONE query head (DUP = KL / G lanes per head) and
     // D / DUP of its channels, so its dot product needs no transpose across
     // heads, only a sum over the DUP lanes.  FP8 / INT4: each lane takes 16
-    // (or 8; INT4 at d 128: 32, one scale group) channels of all G heads and a
-    // transpose-reduction sorts them out.
+    // (or 8) channels of all G heads (INT4: half of one 32-channel scale
+    // group) and a transpose-reduction sorts them out.
     static constexpr bool SHEAD = INT8;
-    static constexpr int CPL = SHEAD ? D * G / 8 : (INT4 && D == 128 && false) ? 32 : ((D == 64 && G == 8) ? 8 : 16);
+    static constexpr int CPL = SHEAD ? D * G / 8 : ((D == 64 && G == 8) ? 8 : 16);
     static constexpr int KL = SHEAD ? 8 : D / CPL;
     static constexpr int QROWS = SHEAD ? 1 : G;  // query rows held per lane
     static constexpr int TPP = 32 / KL;
@@ -674,10 +674,7 @@ decode_partial_kernel(const DecodeParams p) {
                     } else if constexpr (C::INT4) {
                         const uint8_t* src = stg + C::KC + t * (D / 2) + k_c0 / 2;
                         uint32_t wv[C::CPL / 8];
-                        if constexpr (C::CPL == 32) {
-                            const uint4 r = *reinterpret_cast<const uint4*>(src);
-                            wv[0] = r.x; wv[1] = r.y; wv[2] = r.z; wv[3] = r.w;
-                        } else if constexpr (C::CPL == 16) {
+                        if constexpr (C::CPL == 16) {
                             const uint2 r = *reinterpret_cast<const uint2*>(src);
                             wv[0] = r.x; wv[1] = r.y;
                         } else {
