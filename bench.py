@@ -148,7 +148,8 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dynamically_quantized_paged_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith("kvq_decode") or name in ("kvq_device.cuh", "kvq_internal.h", "kvq_tc.cuh", "kvq_alu.cuh"):
+        if name.startswith("kvq_decode") or name in ("kvq_device.cuh", "kvq_internal.h", "kvq_tc.cuh", "kvq_alu.cuh",
+                                                     "kvq_quant.cuh"):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
     return h.hexdigest()
