@@ -1059,7 +1059,7 @@ decode_partial_kernel(const DecodeParams p) {
             const Piece pc = cw.get(p);
             const int64_t units = prefix[pc.b + 1] - prefix[pc.b];
             const int64_t a = (int64_t)Hkv * prefix[pc.b] + (int64_t)pc.h * units;
-            const int64_t k0 = (a + pc.u_lo) / plan.Sw, k1 = (a + pc.u_hi - 1) / plan.Sw;
+            const int64_t k0 = div_line(a + pc.u_lo, plan.Sw), k1 = div_line(a + pc.u_hi - 1, plan.Sw);
             if (pc.whole && k0 == k1) continue;  // inside one warp's slice: already final
             EndPiece& e = eps[np++];
             e.a = a;
@@ -1096,7 +1096,7 @@ decode_partial_kernel(const DecodeParams p) {
             EndPiece& e = eps[tid];
             if (e.slot >= 0) {
                 const unsigned long long n =
-                    (unsigned long long)((e.a + e.units - 1) / plan.S - e.a / plan.S + 1);
+                    (unsigned long long)(div_line(e.a + e.units - 1, plan.S) - div_line(e.a, plan.S) + 1);
                 if (!count_arrival(p, e.b, e.h, n)) e.slot = -2;  // not the last: nothing to merge
             } else {
                 e.slot = -2;  // final rows already written above
@@ -1108,7 +1108,7 @@ decode_partial_kernel(const DecodeParams p) {
             const int it = i0 + lane;
             const EndPiece& e = eps[(it < np * NE ? it : i0) / NE];
             const int elem = it % NE;
-            const int64_t k0 = e.a / plan.S, n = (e.a + e.units - 1) / plan.S - k0 + 1;
+            const int64_t k0 = div_line(e.a, plan.S), n = div_line(e.a + e.units - 1, plan.S) - k0 + 1;
             merge_element<D, G>(p.ws_o, p.ws_m, p.ws_l, e.a, plan.S, k0, e.slot == -2 ? 0 : (int)n,
                                 elem / (D / 4), (elem % (D / 4)) * 4, lane, it < np * NE && e.slot != -2,
                                 out_row(p, ((int64_t)e.b * p.Hq + (int64_t)e.h * G) * D), nullptr, nullptr, nullptr);

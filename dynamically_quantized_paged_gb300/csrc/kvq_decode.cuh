@@ -60,6 +60,11 @@ __device__ __forceinline__ void store_out4(const OutRow& r, int64_t i, float4 v)
 // Sw = max(ceil(U / (n_ctas * WPC)), MIN_SLICE_UNITS) and CTA slice
 // S = WPC * Sw (the tensor-core kernel: one worker per CTA; the CUDA-core
 // kernel: every warp is a worker).
+// Quotient of two work-line quantities (unit indices, counts, slice lengths),
+// all in [0, 2^32): the host refuses calls whose line has 2^31 units or more,
+// so 32-bit division is exact here and much cheaper than 64-bit division.
+__device__ __forceinline__ int64_t div_line(int64_t a, int64_t b) { return (int64_t)((uint32_t)a / (uint32_t)b); }
+
 struct Plan {
     int B, Hkv;
     int64_t U;
@@ -130,7 +135,7 @@ __device__ __forceinline__ Plan build_plan(const DecodeParams& p, int32_t* prefi
     pl.Hkv = p.c.num_kv_heads;
     pl.U = (int64_t)pl.Hkv * misc[0];
     const int64_t workers = (int64_t)p.n_ctas * WPC;
-    const int64_t Sw = (pl.U + workers - 1) / workers;
+    const int64_t Sw = div_line(pl.U + workers - 1, workers);
     pl.Sw = Sw < MIN_SLICE_UNITS ? MIN_SLICE_UNITS : Sw;
     pl.S = pl.Sw * WPC;
     return pl;
@@ -175,7 +180,7 @@ struct PieceWalk {
                 else lo = mid + 1;
             }
             b = lo;
-            h = (int)((x - (int64_t)Hkv * prefix[b]) / units(b));
+            h = (int)div_line(x - (int64_t)Hkv * prefix[b], units(b));
         }
     }
     __device__ bool done() const { return x >= end; }
@@ -232,7 +237,7 @@ __device__ __forceinline__ void merge_workers(const float* so, const float* sm, 
     constexpr int UNR = 8;                           // partials per round
     static_assert(UNR <= LPH, "one lane per partial of a round");
     const int n = (int)(k1 - k0 + 1);
-    const int64_t k_start = a / S;  // the worker whose slice holds the segment's first unit
+    const int64_t k_start = div_line(a, S);  // the worker whose slice holds the segment's first unit
     const bool start_odd = a != k_start * S;
     const int lane = tid & 31, base = lane / LPH * LPH, sub = lane % LPH;
     auto slot_of = [&](int i) -> int64_t {
@@ -319,7 +324,7 @@ __device__ __forceinline__ void merge_element(const float* so, const float* sm, 
                                               OutRow row, float* dst_o, float* dst_m, float* dst_l) {
     constexpr int LPH = D / 4 < 32 ? D / 4 : 32;
     constexpr int UNR = 8;
-    const int64_t k_start = a / S;
+    const int64_t k_start = div_line(a, S);
     const bool start_odd = a != k_start * S;
     const int base = lane / LPH * LPH, sub = lane % LPH;
     auto slot_of = [&](int i) -> int64_t {
@@ -445,8 +450,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) decode_merge_kernel(const Decod
         return;
     }
     const int64_t a = (int64_t)p.c.num_kv_heads * prefix[b] + (int64_t)h * units;
-    if (a / S == (a + units - 1) / S) return;  // finished inside one CTA's slice
-    merge_workers<D, G, MERGE_THREADS>(p.ws_o, p.ws_m, p.ws_l, a, S, a / S, (a + units - 1) / S, threadIdx.x,
+    if (div_line(a, S) == div_line(a + units - 1, S)) return;  // finished inside one CTA's slice
+    merge_workers<D, G, MERGE_THREADS>(p.ws_o, p.ws_m, p.ws_l, a, S, div_line(a, S), div_line(a + units - 1, S), threadIdx.x,
                                        out_row(p, ((int64_t)b * p.Hq + (int64_t)h * G) * D), nullptr, nullptr, nullptr);
 }
 

@@ -1136,11 +1136,12 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
         if (have && !e.whole && !(tid == 1 && idx == 1)) {
             const int units = prefix[e.b + 1] - prefix[e.b];
             const int64_t a = (int64_t)Hkv * prefix[e.b] + (int64_t)e.h * units;
-            const unsigned long long n = (unsigned long long)((a + units - 1) / plan.S - a / plan.S + 1);
+            const unsigned long long n =
+                (unsigned long long)(div_line(a + units - 1, plan.S) - div_line(a, plan.S) + 1);
             if (count_arrival(p, e.b, e.h, n)) {
                 s_merge[tid][0] = e.b;
                 s_merge[tid][1] = e.h;
-                s_merge[tid][2] = (int)(a - (a / plan.S) * plan.S);  // offset of the start in its slice
+                s_merge[tid][2] = (int)(a - div_line(a, plan.S) * plan.S);  // offset of the start in its slice
                 s_merge[tid][3] = units;
             }
         }
@@ -1152,7 +1153,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
         if (s_merge[e][0] < 0) continue;
         const int b = s_merge[e][0], h = s_merge[e][1], units = s_merge[e][3];
         const int64_t a = (int64_t)Hkv * prefix[b] + (int64_t)h * units;
-        const int64_t k0 = a / plan.S, n = (a + units - 1) / plan.S - k0 + 1;
+        const int64_t k0 = div_line(a, plan.S), n = div_line(a + units - 1, plan.S) - k0 + 1;
         for (int i0 = warp * 32; i0 < NE; i0 += C::THREADS) {  // warp-uniform trip count
             const int it = i0 + lane;
             merge_element<D, G>(p.ws_o, p.ws_m, p.ws_l, a, plan.S, k0, (int)n, (it % NE) / (D / 4),
