@@ -148,12 +148,14 @@ struct DecodeCfg {
     // ring depth per warp (STAGES-1 units in flight): as deep as shared memory
     // allows next to the weights and a plan of MAX_SEQS sequences (227 KB a
     // CTA, less 4 KB for the static arrays), at most 4
-    static constexpr int FIT = (232448 - 4096 - WARPS * W_BYTES - 16 - (MAX_SEQS + 1) * 4) / (WARPS * STAGE);
+    static constexpr int FIT = (232448 - 4096 - WARPS * W_BYTES - 16 - (WARPS + 1) * 48 - (MAX_SEQS + 1) * 4) /
+                               (WARPS * STAGE);
     static constexpr int STAGES = FIT < 4 ? FIT : 4;
     static_assert(STAGES >= 2 && STAGES <= 4, "at least one unit in flight while one is computed; the piece queue");
     static constexpr int OFF_W = OFF_STAGES + WARPS * STAGES * STAGE;
     static constexpr int OFF_MISC = OFF_W + WARPS * W_BYTES;
-    static constexpr int OFF_PLAN = OFF_MISC + 16;
+    static constexpr int OFF_EPS = OFF_MISC + 16;  // the CTA's end pieces (EndPiece[WARPS + 1])
+    static constexpr int OFF_PLAN = OFF_EPS + (WARPS + 1) * 48;
     static size_t smem_bytes(int B) { return OFF_PLAN + (size_t)(B + 1) * 4; }
     static_assert(G <= KL, "each lane must end the reduction holding one head");
     static_assert(STAGE % 16 == 0 && Q_BYTES % 16 == 0 && (UNIT * MB) % 16 == 0, "16-byte copies");
@@ -265,6 +267,34 @@ decode_partial_kernel(const DecodeParams p) {
             const OutRow row = out_row(p, (int64_t)b * p.Hq * D);
             for (int i = threadIdx.x; i < p.Hq * D; i += blockDim.x) store_out(row, i, 0.0f);
         }
+    }
+    // The CTA's pieces that span more than one warp's slice, or that continue
+    // in another CTA (at most one per warp boundary plus the two ends): listed
+    // now, by one thread, from the plan alone, so that the end phase starts
+    // with the list ready.  Read after the end phase's barrier.
+    EndPiece* eps = reinterpret_cast<EndPiece*>(smem + C::OFF_EPS);
+    static_assert(sizeof(EndPiece) <= 48, "room for the list");
+    __shared__ int s_np;
+    if (threadIdx.x == 0) {
+        int np = 0;
+        PieceWalk cw;
+        cw.begin(plan, prefix, blockIdx.x, plan.S);
+        for (; !cw.done(); cw.next()) {
+            const Piece pc = cw.get(p);
+            const int64_t units = prefix[pc.b + 1] - prefix[pc.b];
+            const int64_t a = (int64_t)Hkv * prefix[pc.b] + (int64_t)pc.h * units;
+            const int64_t k0 = div_line(a + pc.u_lo, plan.Sw), k1 = div_line(a + pc.u_hi - 1, plan.Sw);
+            if (pc.whole && k0 == k1) continue;  // inside one warp's slice: already final
+            EndPiece& e = eps[np++];
+            e.a = a;
+            e.units = units;
+            e.k0 = k0;
+            e.n = (int)(k1 - k0 + 1);
+            e.b = pc.b;
+            e.h = pc.h;
+            e.slot = pc.whole ? -1 : pc.slot;
+        }
+        s_np = np;
     }
     uint8_t* ring = smem + C::OFF_STAGES + warp * STAGES_ * C::STAGE;
 
@@ -1048,31 +1078,6 @@ decode_partial_kernel(const DecodeParams p) {
     // pieces at once (at most one per warp boundary plus the two ends)
     cp_async_wait<0>();
     __syncthreads();  // all warps' rows and partials are written; the rings are idle
-    EndPiece* eps = reinterpret_cast<EndPiece*>(smem + C::OFF_STAGES);
-    static_assert((C::WARPS + 1) * sizeof(EndPiece) <= (size_t)C::WARPS * STAGES_ * C::STAGE, "room for the list");
-    __shared__ int s_np;
-    if (tid == 0) {
-        int np = 0;
-        PieceWalk cw;
-        cw.begin(plan, prefix, blockIdx.x, plan.S);
-        for (; !cw.done(); cw.next()) {
-            const Piece pc = cw.get(p);
-            const int64_t units = prefix[pc.b + 1] - prefix[pc.b];
-            const int64_t a = (int64_t)Hkv * prefix[pc.b] + (int64_t)pc.h * units;
-            const int64_t k0 = div_line(a + pc.u_lo, plan.Sw), k1 = div_line(a + pc.u_hi - 1, plan.Sw);
-            if (pc.whole && k0 == k1) continue;  // inside one warp's slice: already final
-            EndPiece& e = eps[np++];
-            e.a = a;
-            e.units = units;
-            e.k0 = k0;
-            e.n = (int)(k1 - k0 + 1);
-            e.b = pc.b;
-            e.h = pc.h;
-            e.slot = pc.whole ? -1 : pc.slot;
-        }
-        s_np = np;
-    }
-    __syncthreads();
     const int np = s_np;
     constexpr int NE = G * D / 4;  // float4 elements of one piece's G output rows
     for (int i0 = warp * 32; i0 < np * NE; i0 += C::THREADS) {  // warp-uniform trip count
