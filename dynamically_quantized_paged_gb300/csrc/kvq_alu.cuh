@@ -221,10 +221,11 @@ decode_partial_kernel(const DecodeParams p) {
     constexpr int STAGES_ = C::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
     // Launched with programmatic stream serialization: the CTAs may be
-    // resident before the previous kernel in the stream ends; nothing that
-    // kernel may have written (cache, tables, lengths, queries) is read
-    // before it has completed.
-    grid_dependency_wait();
+    // resident before the kernel ahead of them in the stream ends.  Only the
+    // kernel's own parameters are used before the wait below; every array
+    // behind a pointer (lengths, tables, queries, cache, workspace) is read
+    // or written after it, once that kernel has completed and its writes are
+    // visible.
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     int64_t* misc = reinterpret_cast<int64_t*>(smem + C::OFF_MISC);
@@ -248,6 +249,7 @@ decode_partial_kernel(const DecodeParams p) {
         pool_tab[1][4] = static_cast<const uint8_t*>(p.c.hk_zeros);
         pool_tab[1][5] = static_cast<const uint8_t*>(p.c.hv_zeros);
     }
+    grid_dependency_wait();  // the kernel ahead has completed
     const Plan plan = build_plan<C::THREADS, C::WARPS>(p, prefix, misc);  // contains __syncthreads
     if (blockIdx.x == 0) {
         // publish the plan for the merge kernel: [U, S] then prefix[0..B]

@@ -411,9 +411,12 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
     using C = Cfg<SCHEME, D, G>;
     constexpr int T = C::T, TU = C::TU, R = C::R;
     extern __shared__ __align__(128) uint8_t smem[];
-    // Launched with programmatic stream serialization: nothing the kernel
-    // ahead of it may have written is read before it has completed.
-    grid_dependency_wait();
+    // Launched with programmatic stream serialization: the CTAs may be
+    // resident before the kernel ahead of them in the stream ends.  The
+    // set-up that uses no array behind a pointer (barriers, tensor memory,
+    // zeroing shared memory) runs at once; lengths, tables, queries, cache
+    // and workspace are touched only after the wait, once that kernel has
+    // completed and its writes are visible.
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     Small<C, G> sm{smem + C::OFF_SMALL};
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + C::OFF_PREFIX);
@@ -459,6 +462,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
     // and blocks never written, weight columns >= NO_USED
     for (int i = tid; i < (2 * C::VS_BYTES + 2 * C::QB_BYTES + 2 * C::WB_BYTES) / 16; i += C::THREADS)
         reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+    grid_dependency_wait();  // the kernel ahead has completed
     const Plan plan = build_plan<C::THREADS>(p, prefix, sm.plan_misc());  // contains __syncthreads
     if (blockIdx.x == 0) {
         // publish the plan for the merge kernel: [U, S] then prefix[0..B]

@@ -197,8 +197,9 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_seqs,
  * as no two calls sharing a workspace run at the same time).  The kernel is
  * launched with programmatic stream serialization: its CTAs may become
  * resident while the kernel ahead of it on the stream (e.g. kvq_append) is
- * still running, but read no argument and no cache byte before that kernel
- * has completed.
+ * still running and set up what needs no input (barriers, tensor memory),
+ * but read or write no array argument, cache or workspace byte before that
+ * kernel has completed and its writes are visible.
  * kvq_decode_partial followed by kvq_decode_merge is the equivalent
  * two-launch form and gives bitwise the same output. */
 kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const int32_t* block_table,
