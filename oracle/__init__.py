@@ -31,8 +31,8 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-INT8, FP8, INT4, INT4SYM = 1, 2, 3, 4
-SCHEME_IDS = {"int8": INT8, "fp8": FP8, "int4": INT4, "int4sym": INT4SYM}
+INT8, FP8, INT4, INT4SYM, INT8KC = 1, 2, 3, 4, 5
+SCHEME_IDS = {"int8": INT8, "fp8": FP8, "int4": INT4, "int4sym": INT4SYM, "int8kc": INT8KC}
 
 
 def build(force: bool = False) -> str:
@@ -53,7 +53,9 @@ class _Cache(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
                 ("k_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
-                ("k_zeros", ctypes.c_void_p), ("v_zeros", ctypes.c_void_p)]
+                ("k_zeros", ctypes.c_void_p), ("v_zeros", ctypes.c_void_p),
+                ("k_chan", ctypes.c_void_p), ("k_resid", ctypes.c_void_p),
+                ("resid_slots", ctypes.c_int32)]
 
 
 def lib():
@@ -74,6 +76,10 @@ def lib():
             L.orc_quant_int4_row.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P]
             L.orc_quant_int4sym_row.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P]
             L.orc_append.argtypes, L.orc_append.restype = [ctypes.POINTER(_Cache), P, P, P, c_i32], ctypes.c_int
+            L.orc_append_kc.argtypes = [ctypes.POINTER(_Cache), P, P, P, P, c_i32]
+            L.orc_append_kc.restype = ctypes.c_int
+            L.orc_seal_pages.argtypes, L.orc_seal_pages.restype = [ctypes.POINTER(_Cache), P, P, c_i32], ctypes.c_int
+            L.orc_quant_kchan_page.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P]
             L.orc_decode_attn.argtypes = [ctypes.POINTER(_Cache), P, P, P, c_i32, c_i32, c_i32,
                                           ctypes.c_double, P]
             L.orc_decode_attn.restype = ctypes.c_int
@@ -154,6 +160,18 @@ def quant_int4sym_row(x: np.ndarray, group: int = 32):
     return packed, sc
 
 
+def quant_kchan_page(x: np.ndarray):
+    """Per-channel INT8 of one (page, KV head) K block x[P][D] (bf16 bits):
+    codes [P][D] int8, channel factors [D] (fp16 bits), token scales [P] fp32."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    P, D = x.shape
+    codes = np.empty((P, D), np.int8)
+    chan = np.empty(D, np.uint16)
+    tok = np.empty(P, np.float32)
+    lib().orc_quant_kchan_page(_p(x), P, D, _p(codes), _p(chan), _p(tok))
+    return codes, chan, tok
+
+
 def unpack_int4sym(packed: np.ndarray) -> np.ndarray:
     """The signed codes of a packed symmetric INT4 row (even channel in the
     low nibble, two's complement)."""
@@ -171,10 +189,13 @@ class OracleCache:
     Layout: codes [page][kv_head][page_size][head_dim] (INT4 and symmetric
     INT4: head_dim/2 bytes, two codes per byte), scales [page][kv_head]
     [page_size] fp32 (INT4: fp16 bits [..][head_dim/group], plus zeros of the
-    same shape; symmetric INT4: fp32 [..][head_dim/group], no zeros)."""
+    same shape; symmetric INT4: fp32 [..][head_dim/group], no zeros).  The
+    per-channel K scheme ("int8kc") is INT8 plus channel factors k_chan
+    [page][kv_head][head_dim] (fp16 bits) and a residual pool k_resid
+    [resid_slots][kv_head][page_size][head_dim] (bf16 bits)."""
 
     def __init__(self, scheme: str, num_pages: int, page_size: int, num_kv_heads: int,
-                 head_dim: int, group: int = 32):
+                 head_dim: int, group: int = 32, resid_slots: int = 0):
         self.scheme = scheme
         self.sid = SCHEME_IDS[scheme]
         self.num_pages, self.page_size = num_pages, page_size
@@ -199,21 +220,45 @@ class OracleCache:
             self.k_scales = np.zeros(rows, np.float32)
             self.v_scales = np.zeros(rows, np.float32)
             self.k_zeros = self.v_zeros = None
+        self.resid_slots = resid_slots if scheme == "int8kc" else 0
+        if scheme == "int8kc":
+            self.k_chan = np.zeros(num_pages * num_kv_heads * head_dim, np.uint16)
+            self.k_resid = np.zeros(max(self.resid_slots, 1) * num_kv_heads * page_size * head_dim, np.uint16)
+        else:
+            self.k_chan = self.k_resid = None
 
     def _struct(self) -> _Cache:
         z = lambda a: None if a is None else a.ctypes.data
         return _Cache(self.sid, self.num_pages, self.page_size, self.num_kv_heads, self.head_dim,
                       self.group, z(self.k_codes), z(self.v_codes), z(self.k_scales),
-                      z(self.v_scales), z(self.k_zeros), z(self.v_zeros))
+                      z(self.v_scales), z(self.k_zeros), z(self.v_zeros), z(self.k_chan),
+                      z(self.k_resid), self.resid_slots)
 
-    def append(self, slot_mapping: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray) -> int:
+    def append(self, slot_mapping: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
+               resid_slot: np.ndarray | None = None) -> int:
+        """resid_slot (per-channel K only): int32 [T], the residual slot that
+        keeps each token's bf16 K row (-1: none)."""
         slot_mapping = np.ascontiguousarray(slot_mapping, np.int64)
         k_bits = np.ascontiguousarray(k_bits, np.uint16)
         v_bits = np.ascontiguousarray(v_bits, np.uint16)
         T = slot_mapping.size
         assert k_bits.size == T * self.num_kv_heads * self.head_dim == v_bits.size
         s = self._struct()
-        return lib().orc_append(ctypes.byref(s), _p(slot_mapping), _p(k_bits), _p(v_bits), T)
+        if resid_slot is None:
+            return lib().orc_append(ctypes.byref(s), _p(slot_mapping), _p(k_bits), _p(v_bits), T)
+        resid_slot = np.ascontiguousarray(resid_slot, np.int32)
+        assert resid_slot.size == T
+        return lib().orc_append_kc(ctypes.byref(s), _p(slot_mapping), _p(resid_slot), _p(k_bits),
+                                   _p(v_bits), T)
+
+    def seal(self, pages: np.ndarray, resid_slots: np.ndarray) -> int:
+        """Per-channel K: re-quantize each page's K per channel from its
+        residual slot (pages[i] from resid_slots[i])."""
+        pages = np.ascontiguousarray(pages, np.int32)
+        resid_slots = np.ascontiguousarray(resid_slots, np.int32)
+        assert pages.size == resid_slots.size
+        s = self._struct()
+        return lib().orc_seal_pages(ctypes.byref(s), _p(pages), _p(resid_slots), pages.size)
 
     def decode_attn(self, q_bits: np.ndarray, block_table: np.ndarray, seq_lens: np.ndarray,
                     num_q_heads: int, softmax_scale: float = 0.0) -> np.ndarray:

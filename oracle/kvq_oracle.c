@@ -42,6 +42,19 @@
  * the dequantized cache with softmax scale 1/sqrt(head_dim) and query head g
  * reading KV head g / (Hq / Hkv).
  *
+ * Per-channel K ([P3] "KV Cache Optimization: Strategies for Faster LLM
+ * Inference", section "KV Cache Quantization: When and How to Compress":
+ * per-channel quantization keeps more than per-tensor).  Reading taken: the
+ * K scale of a channel is taken over the tokens of one page (one scale per
+ * page, KV head and channel); while a page is still filling its tokens are
+ * stored with the INT8 token rule and their bf16 K rows are kept in a
+ * residual slot; once full, the page is sealed: its K is re-quantized per
+ * channel from those bf16 rows (the INT8 rule along the token axis, in the
+ * normalized form described at orc_quant_kchan_page).  V keeps the token
+ * rule throughout.  Dequantized K = code * channel factor * token scale,
+ * where an open page has channel factors 1 and a sealed page has its
+ * largest channel scale as every token's scale.
+ *
  * Build: gcc -O2 -fno-fast-math -ffp-contract=off -fopenmp -fPIC -shared.
  * Floating-point: every fp32 step is a single IEEE operation in the order
  * written; no contraction, no reassociation.
@@ -55,7 +68,7 @@
 #endif
 
 /* ---- scheme ids (the oracle's own copy of the numbering) ----------------- */
-enum { ORC_INT8 = 1, ORC_FP8 = 2, ORC_INT4 = 3, ORC_INT4SYM = 4 };
+enum { ORC_INT8 = 1, ORC_FP8 = 2, ORC_INT4 = 3, ORC_INT4SYM = 4, ORC_INT8KC = 5 };
 
 /* ---- number formats, from their definitions ------------------------------ */
 
@@ -283,6 +296,59 @@ void orc_quant_int4sym_row(const uint16_t* x, int n, int group, uint8_t* packed,
         packed[j] = (uint8_t)(((uint8_t)q[2 * j] & 0xF) | (((uint8_t)q[2 * j + 1] & 0xF) << 4));
 }
 
+/* Per-channel INT8 of one (page, KV head) K block x[P][D] (bf16 bits): the
+ * absmax rule of [P1] "Understanding Dynamic Quantization Techniques" taken
+ * down each channel instead of along each token ([P3] "KV Cache
+ * Quantization: When and How to Compress": per-channel), in a normalized
+ * form that keeps every stored factor small:
+ *   s_j   = (max over t of |x[t][j]|) / 127                   (fp32 division)
+ *   S     = max over j of s_j                                  (the block's largest)
+ *   r_j   = fp16 round-up of s_j / S  (fp32 division), a channel factor in
+ *           [0, 1]; rounding up makes the effective scale e_j >= s_j up to
+ *           the fp32 roundings, so no quotient passes 127 by more than a
+ *           rounding step
+ *   e_j   = r_j * S                                            (fp32 product)
+ *   code  = round-half-even(x / e_j) (fp32 division), kept in [-127, 127];
+ *           0 for a channel with e_j = 0 (an all-zero channel)
+ *   tok_t = S for every token of the block.
+ * An all-zero block stores codes 0, factors 1.0 and token scales 1.0 (the
+ * zero-row convention of the INT8 rule).  Dequantized: code * r_j * tok_t. */
+void orc_quant_kchan_page(const uint16_t* x, int P, int D, int8_t* codes, uint16_t* chan, float* tok) {
+    float s[1024];
+    float S = 0.0f;
+    for (int j = 0; j < D; ++j) {
+        float absmax = 0.0f;
+        for (int t = 0; t < P; ++t) {
+            float a = fabsf(orc_bf16_to_float(x[(int64_t)t * D + j]));
+            if (a > absmax) absmax = a;
+        }
+        s[j] = absmax / 127.0f;
+        if (s[j] > S) S = s[j];
+    }
+    if (S == 0.0f) {
+        for (int64_t i = 0; i < (int64_t)P * D; ++i) codes[i] = 0;
+        for (int j = 0; j < D; ++j) chan[j] = 0x3C00; /* 1.0 */
+        for (int t = 0; t < P; ++t) tok[t] = 1.0f;
+        return;
+    }
+    for (int j = 0; j < D; ++j) {
+        float ratio = s[j] / S;
+        chan[j] = orc_fp16_round_up(ratio);
+        float e = (float)orc_fp16_value(chan[j]) * S;
+        for (int t = 0; t < P; ++t) {
+            int8_t q = 0;
+            if (e != 0.0f) {
+                float r = rintf(orc_bf16_to_float(x[(int64_t)t * D + j]) / e);
+                if (r > 127.0f) r = 127.0f;
+                if (r < -127.0f) r = -127.0f;
+                q = (int8_t)r;
+            }
+            codes[(int64_t)t * D + j] = q;
+        }
+    }
+    for (int t = 0; t < P; ++t) tok[t] = S;
+}
+
 /* ---- the paged cache image ------------------------------------------------- */
 
 /* One layer's cache.  Layout (this library's design, restated here on its
@@ -294,11 +360,17 @@ void orc_quant_int4sym_row(const uint16_t* x, int n, int group, uint8_t* packed,
  *                                                                 fp16 bits
  *   symmetric INT4: codes as INT4 (two's-complement nibbles)
  *                   scales [page][kv_head][page_size][head_dim/group] fp32
+ *   per-channel K:  codes and scales as INT8 (K scales are the token
+ *                   scales tok_t), plus
+ *                   k_chan  [page][kv_head][head_dim]             fp16 bits
+ *                   k_resid [resid_slots][kv_head][page_size][head_dim] bf16
  * A token at physical slot `slot` lives in page slot / page_size at offset
  * slot % page_size. */
 typedef struct {
     int32_t scheme, num_pages, page_size, num_kv_heads, head_dim, group;
     void *k_codes, *v_codes, *k_scales, *v_scales, *k_zeros, *v_zeros;
+    void *k_chan, *k_resid;
+    int32_t resid_slots;
 } orc_cache;
 
 static int64_t row_code_bytes(const orc_cache* c) {
@@ -307,9 +379,14 @@ static int64_t row_code_bytes(const orc_cache* c) {
 
 /* Quantize-append: token t's K and V rows ([T][Hkv][D] bf16) are quantized
  * per KV head and stored at slot_mapping[t]; a negative slot skips the token.
- * Returns 0, or -1 if a slot is outside the pool (nothing written for it). */
-int orc_append(const orc_cache* c, const int64_t* slot_mapping, const uint16_t* k,
-               const uint16_t* v, int32_t T) {
+ * Per-channel K: both rows take the INT8 token rule (the page is open); a
+ * token at offset 0 opens its page, setting that head's channel factors to
+ * 1.0; with resid_slot given and resid_slot[t] >= 0, the token's bf16 K row
+ * is also kept at offset slot % page_size of residual slot resid_slot[t].
+ * Returns 0, or -1 if a slot or residual slot is outside its pool (nothing
+ * written for it). */
+int orc_append_kc(const orc_cache* c, const int64_t* slot_mapping, const int32_t* resid_slot,
+                  const uint16_t* k, const uint16_t* v, int32_t T) {
     const int H = c->num_kv_heads, D = c->head_dim, P = c->page_size;
     const int64_t nslots = (int64_t)c->num_pages * P;
     int bad = 0;
@@ -319,12 +396,22 @@ int orc_append(const orc_cache* c, const int64_t* slot_mapping, const uint16_t* 
         if (slot < 0) continue;
         if (slot >= nslots) { bad = 1; continue; }
         int64_t page = slot / P, off = slot % P;
+        int32_t rs = resid_slot ? resid_slot[t] : -1;
+        if (c->scheme == ORC_INT8KC && rs >= c->resid_slots) { bad = 1; continue; }
         for (int h = 0; h < H; ++h) {
             int64_t row = (page * H + h) * P + off; /* row index inside the pool */
+            if (c->scheme == ORC_INT8KC) {
+                const uint16_t* x = k + ((int64_t)t * H + h) * D;
+                if (off == 0)
+                    for (int j = 0; j < D; ++j) ((uint16_t*)c->k_chan)[(page * H + h) * D + j] = 0x3C00;
+                if (rs >= 0)
+                    memcpy((uint16_t*)c->k_resid + (((int64_t)rs * H + h) * P + off) * D, x,
+                           sizeof(uint16_t) * (size_t)D);
+            }
             for (int kv = 0; kv < 2; ++kv) {
                 const uint16_t* x = (kv == 0 ? k : v) + ((int64_t)t * H + h) * D;
                 uint8_t* codes = (uint8_t*)(kv == 0 ? c->k_codes : c->v_codes) + row * row_code_bytes(c);
-                if (c->scheme == ORC_INT8) {
+                if (c->scheme == ORC_INT8 || c->scheme == ORC_INT8KC) {
                     float* sc = (float*)(kv == 0 ? c->k_scales : c->v_scales) + row;
                     orc_quant_int8_row(x, D, (int8_t*)codes, sc);
                 } else if (c->scheme == ORC_FP8) {
@@ -346,14 +433,47 @@ int orc_append(const orc_cache* c, const int64_t* slot_mapping, const uint16_t* 
     return bad ? -1 : 0;
 }
 
+int orc_append(const orc_cache* c, const int64_t* slot_mapping, const uint16_t* k,
+               const uint16_t* v, int32_t T) {
+    return orc_append_kc(c, slot_mapping, NULL, k, v, T);
+}
+
+/* Seal pages of the per-channel K scheme: for each i, page pages[i] (every KV
+ * head) takes the per-channel rule (orc_quant_kchan_page) of the page_size
+ * bf16 K rows kept in residual slot resid_slots[i]: its K codes, channel
+ * factors and token scales are replaced; V is left as it is.  Returns 0, or
+ * -1 if a page or slot id is outside its pool (that pair is skipped). */
+int orc_seal_pages(const orc_cache* c, const int32_t* pages, const int32_t* resid_slots, int32_t n) {
+    const int H = c->num_kv_heads, D = c->head_dim, P = c->page_size;
+    int bad = 0;
+    if (c->scheme != ORC_INT8KC) return -1;
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t page = pages[i], rs = resid_slots[i];
+        if (page < 0 || page >= c->num_pages || rs < 0 || rs >= c->resid_slots) { bad = 1; continue; }
+        for (int h = 0; h < H; ++h) {
+            const uint16_t* x = (const uint16_t*)c->k_resid + ((int64_t)rs * H + h) * P * D;
+            int64_t row0 = ((int64_t)page * H + h) * P;
+            orc_quant_kchan_page(x, P, D, (int8_t*)c->k_codes + row0 * D,
+                                 (uint16_t*)c->k_chan + ((int64_t)page * H + h) * D, (float*)c->k_scales + row0);
+        }
+    }
+    return bad ? -1 : 0;
+}
+
 /* Dequantize the row stored at pool row index `row` into fp64 (exact:
  * code * scale (+ zero) with every operand exactly representable). */
 static void dequant_row(const orc_cache* c, int kv, int64_t row, double* out) {
     const int D = c->head_dim;
     const uint8_t* codes = (const uint8_t*)(kv == 0 ? c->k_codes : c->v_codes) + row * row_code_bytes(c);
-    if (c->scheme == ORC_INT8) {
+    if (c->scheme == ORC_INT8 || (c->scheme == ORC_INT8KC && kv == 1)) {
         double s = ((const float*)(kv == 0 ? c->k_scales : c->v_scales))[row];
         for (int j = 0; j < D; ++j) out[j] = (double)(int8_t)codes[j] * s;
+    } else if (c->scheme == ORC_INT8KC) {
+        /* code * channel factor * token scale: 8 + 11 + 24 significant bits,
+         * exact in fp64 */
+        double s = ((const float*)c->k_scales)[row];
+        const uint16_t* r = (const uint16_t*)c->k_chan + (row / c->page_size) * D;
+        for (int j = 0; j < D; ++j) out[j] = (double)(int8_t)codes[j] * orc_fp16_value(r[j]) * s;
     } else if (c->scheme == ORC_FP8) {
         double s = ((const float*)(kv == 0 ? c->k_scales : c->v_scales))[row];
         for (int j = 0; j < D; ++j) out[j] = orc_e4m3_value(codes[j]) * s;
