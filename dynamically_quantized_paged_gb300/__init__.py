@@ -18,8 +18,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
-INT8, FP8, INT4, INT4SYM = 1, 2, 3, 4
-SCHEMES = {"int8": INT8, "fp8": FP8, "int4": INT4, "int4sym": INT4SYM}
+INT8, FP8, INT4, INT4SYM, INT8KC = 1, 2, 3, 4, 5
+SCHEMES = {"int8": INT8, "fp8": FP8, "int4": INT4, "int4sym": INT4SYM, "int8kc": INT8KC}
 
 OK = 0
 OUT_F32, OUT_BF16 = 0, 1  # kvq_out_dtype
@@ -33,7 +33,7 @@ EXPORTS = ["kvq_status_string", "kvq_cache_bytes", "kvq_append", "kvq_decode_wor
            "kvq_last_device_error", "kvq_allocator_create", "kvq_allocator_destroy",
            "kvq_alloc_pages", "kvq_free_pages", "kvq_allocator_free_count", "kvq_decode_attn_noalloc",
            "kvq_share_pages", "kvq_page_refcount", "kvq_copy_page", "kvq_decode_attn_out",
-           "kvq_decode_attn_append"]
+           "kvq_decode_attn_append", "kvq_kchan_bytes", "kvq_append_kchan", "kvq_seal_pages"]
 
 
 class KvqError(RuntimeError):
@@ -52,7 +52,9 @@ class CacheStruct(ctypes.Structure):
                 ("host_pages", ctypes.c_int32),
                 ("host_k_codes", ctypes.c_void_p), ("host_v_codes", ctypes.c_void_p),
                 ("host_k_scales", ctypes.c_void_p), ("host_v_scales", ctypes.c_void_p),
-                ("host_k_zeros", ctypes.c_void_p), ("host_v_zeros", ctypes.c_void_p)]
+                ("host_k_zeros", ctypes.c_void_p), ("host_v_zeros", ctypes.c_void_p),
+                ("k_chan", ctypes.c_void_p), ("host_k_chan", ctypes.c_void_p),
+                ("k_resid", ctypes.c_void_p), ("resid_slots", ctypes.c_int32)]
 
 
 def _load() -> ctypes.CDLL:
@@ -85,6 +87,9 @@ def _load() -> ctypes.CDLL:
     L.kvq_share_pages.argtypes = [P, i32, P]
     L.kvq_page_refcount.argtypes = [P, i32, ctypes.POINTER(ctypes.c_int32)]
     L.kvq_copy_page.argtypes = [cachep, i32, i32, P]
+    L.kvq_kchan_bytes.argtypes = [i32, i32, i32, i32, i32, sz, sz]
+    L.kvq_append_kchan.argtypes = [cachep, P, i32, i32, i64p, P, P, P, i32, P]
+    L.kvq_seal_pages.argtypes = [cachep, P, P, i32, P]
     for name in EXPORTS:
         getattr(L, name)  # every declared entry point must be exported
     return L
@@ -124,7 +129,16 @@ def cache_bytes(scheme: str | int, num_pages: int, page_size: int, num_kv_heads:
     return c.value, s.value, z.value
 
 
-POOLS = ("k_codes", "v_codes", "k_scales", "v_scales", "k_zeros", "v_zeros")
+def kchan_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int,
+                resid_slots: int) -> tuple[int, int]:
+    """(chan_bytes, resid_bytes) of the per-channel K scheme's extra pools."""
+    c, r = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib.kvq_kchan_bytes(num_pages, page_size, num_kv_heads, head_dim, resid_slots,
+                               ctypes.byref(c), ctypes.byref(r)), "kvq_kchan_bytes")
+    return c.value, r.value
+
+
+POOLS = ("k_codes", "v_codes", "k_scales", "v_scales", "k_zeros", "v_zeros", "k_chan")
 
 
 class PagedKVCache:
@@ -132,10 +146,13 @@ class PagedKVCache:
     uint8 tensors) laid out as include/kvq.h describes, and optionally a host
     tier of host_pages more pages (page ids num_pages .. num_pages +
     host_pages - 1) in page-locked host memory that the kernels read and
-    write in place."""
+    write in place.  The per-channel K scheme ("int8kc") adds the channel
+    factors k_chan (both tiers) and a device residual pool k_resid of
+    resid_slots slots."""
 
     def __init__(self, scheme: str, num_pages: int, page_size: int, num_kv_heads: int,
-                 head_dim: int, device="cuda", zero_init: bool = True, host_pages: int = 0):
+                 head_dim: int, device="cuda", zero_init: bool = True, host_pages: int = 0,
+                 resid_slots: int = 0):
         self.scheme = scheme
         self.sid = SCHEMES[scheme]
         self.num_pages, self.page_size = num_pages, page_size
@@ -150,20 +167,28 @@ class PagedKVCache:
         self.v_scales = alloc(sb, dtype=torch.uint8, device=device)
         self.k_zeros = alloc(zb, dtype=torch.uint8, device=device) if zb else None
         self.v_zeros = alloc(zb, dtype=torch.uint8, device=device) if zb else None
+        kc = scheme == "int8kc"
+        self.resid_slots = resid_slots if kc else 0
+        chb, rsb = kchan_bytes(num_pages, page_size, num_kv_heads, head_dim, self.resid_slots) if kc else (0, 0)
+        self.k_chan = alloc(chb, dtype=torch.uint8, device=device) if kc else None
+        self.k_resid = alloc(rsb, dtype=torch.uint8, device=device) if rsb else None
         self.host = {}
         if host_pages > 0:
             hcb, hsb, hzb = cache_bytes(scheme, host_pages, page_size, num_kv_heads, head_dim)
+            hchb = kchan_bytes(host_pages, page_size, num_kv_heads, head_dim, 0)[0] if kc else 0
             for name, nb in (("k_codes", hcb), ("v_codes", hcb), ("k_scales", hsb), ("v_scales", hsb),
-                             ("k_zeros", hzb), ("v_zeros", hzb)):
+                             ("k_zeros", hzb), ("v_zeros", hzb), ("k_chan", hchb)):
                 self.host[name] = torch.zeros(nb, dtype=torch.uint8).pin_memory() if nb else None
         hp = lambda n: self.host[n].data_ptr() if self.host.get(n) is not None else None  # noqa: E731
+        dp = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
         self.struct = CacheStruct(self.sid, num_pages, page_size, num_kv_heads, head_dim, self.group,
                                   self.k_codes.data_ptr(), self.v_codes.data_ptr(),
                                   self.k_scales.data_ptr(), self.v_scales.data_ptr(),
                                   self.k_zeros.data_ptr() if zb else None,
                                   self.v_zeros.data_ptr() if zb else None,
                                   host_pages, hp("k_codes"), hp("v_codes"), hp("k_scales"),
-                                  hp("v_scales"), hp("k_zeros"), hp("v_zeros"))
+                                  hp("v_scales"), hp("k_zeros"), hp("v_zeros"),
+                                  dp(self.k_chan), hp("k_chan"), dp(self.k_resid), self.resid_slots)
 
     def tier_of(self, page: int) -> str:
         """"device" or "host": where page id `page` lives."""
@@ -189,7 +214,7 @@ class PagedKVCache:
     @property
     def nbytes(self) -> int:
         return sum(t.numel() for t in (self.k_codes, self.v_codes, self.k_scales, self.v_scales,
-                                       self.k_zeros, self.v_zeros) if t is not None)
+                                       self.k_zeros, self.v_zeros, self.k_chan) if t is not None)
 
 
 def copy_page(cache: PagedKVCache, src: int, dst: int, stream=None) -> None:
@@ -209,6 +234,31 @@ def append(cache: PagedKVCache, slot_mapping: torch.Tensor, k: torch.Tensor, v: 
     B, maxp = (block_table.shape[0], block_table.shape[1]) if block_table is not None else (0, 1)
     _check(lib.kvq_append(ctypes.byref(cache.struct), _ptr(block_table), B, maxp, _ptr(slot_mapping),
                           _ptr(k), _ptr(v), T, cache.sid, _stream(stream)), "kvq_append")
+
+
+def append_kchan(cache: PagedKVCache, slot_mapping: torch.Tensor, resid_slot: torch.Tensor | None,
+                 k: torch.Tensor, v: torch.Tensor, block_table: torch.Tensor | None = None, stream=None) -> None:
+    """kvq_append_kchan: kvq_append for the per-channel K scheme, keeping each
+    token's bf16 K rows in residual slot resid_slot[t] (int32 [T]; -1 or
+    None: none)."""
+    T = slot_mapping.numel()
+    if slot_mapping.element_size() != 8 or k.shape != v.shape or k.numel() != T * cache.num_kv_heads * cache.head_dim \
+            or k.element_size() != 2 or (resid_slot is not None and (resid_slot.numel() != T
+                                                                     or resid_slot.element_size() != 4)):
+        raise ValueError("kvq_append_kchan: slot_mapping int64 [T]; resid_slot int32 [T]; k, v bf16 [T, Hkv, d]")
+    B, maxp = (block_table.shape[0], block_table.shape[1]) if block_table is not None else (0, 1)
+    _check(lib.kvq_append_kchan(ctypes.byref(cache.struct), _ptr(block_table), B, maxp, _ptr(slot_mapping),
+                                _ptr(resid_slot), _ptr(k), _ptr(v), T, _stream(stream)), "kvq_append_kchan")
+
+
+def seal_pages(cache: PagedKVCache, pages: torch.Tensor, resid_slots: torch.Tensor, stream=None) -> None:
+    """kvq_seal_pages: re-quantize K of pages[i] per channel from residual
+    slot resid_slots[i] (both int32 [n], device)."""
+    n = pages.numel()
+    if resid_slots.numel() != n or pages.element_size() != 4 or resid_slots.element_size() != 4:
+        raise ValueError("kvq_seal_pages: pages and resid_slots must be int32 [n]")
+    _check(lib.kvq_seal_pages(ctypes.byref(cache.struct), _ptr(pages), _ptr(resid_slots), n, _stream(stream)),
+           "kvq_seal_pages")
 
 
 def decode_workspace_bytes(cache: PagedKVCache, num_seqs: int, num_q_heads: int,

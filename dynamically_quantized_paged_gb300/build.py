@@ -21,7 +21,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libkvq.so")
 
 SOURCES = ["kvq_api.cu", "kvq_append.cu", "kvq_decode_int8.cu", "kvq_decode_fp8.cu",
-           "kvq_decode_int4.cu", "kvq_decode_int4sym.cu", "kvq_merge.cu", "kvq_noalloc.cu"]
+           "kvq_decode_int4.cu", "kvq_decode_int4sym.cu", "kvq_decode_int8kc.cu", "kvq_merge.cu",
+           "kvq_noalloc.cu"]
 HEADERS = ["kvq_device.cuh", "kvq_internal.h", "kvq_decode.cuh", "kvq_tc.cuh", "kvq_alu.cuh", "kvq_quant.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -35,7 +35,7 @@ int current_device() {
 
 kvq_status check_cache(const kvq_cache* c) {
     if (!c) return KVQ_ERR_INVALID_ARG;
-    if (c->scheme < KVQ_INT8_SYM_TOKEN || c->scheme > KVQ_INT4_SYM_G32) return KVQ_ERR_INVALID_ARG;
+    if (c->scheme < KVQ_INT8_SYM_TOKEN || c->scheme > KVQ_INT8_KCHAN) return KVQ_ERR_INVALID_ARG;
     if (c->num_pages < 1 || c->page_size < 1 || c->num_kv_heads < 1 || c->head_dim < 1)
         return KVQ_ERR_INVALID_ARG;
     if (c->page_size % kvq::UNIT != 0) return KVQ_ERR_UNSUPPORTED;
@@ -48,6 +48,11 @@ kvq_status check_cache(const kvq_cache* c) {
     if (c->scheme == KVQ_INT4_ASYM_G32) {
         if (!c->k_zeros || !c->v_zeros || !aligned(c->k_zeros, 16) || !aligned(c->v_zeros, 16))
             return KVQ_ERR_INVALID_ARG;
+    }
+    if (c->scheme == KVQ_INT8_KCHAN) {  // channel factors; the residual pool when it has slots
+        if (!c->k_chan || !aligned(c->k_chan, 16) || c->resid_slots < 0) return KVQ_ERR_INVALID_ARG;
+        if (c->resid_slots > 0 && (!c->k_resid || !aligned(c->k_resid, 16))) return KVQ_ERR_INVALID_ARG;
+        if (c->host_pages > 0 && (!c->host_k_chan || !aligned(c->host_k_chan, 16))) return KVQ_ERR_INVALID_ARG;
     }
     if (c->host_pages < 0) return KVQ_ERR_INVALID_ARG;
     if (c->host_pages > 0) {  // the host tier's pools, as the device tier's
@@ -89,6 +94,9 @@ kvq::CacheView view_of(const kvq_cache* c) {
     v.hv_scales = ht ? c->host_v_scales : nullptr;
     v.hk_zeros = ht ? c->host_k_zeros : nullptr;
     v.hv_zeros = ht ? c->host_v_zeros : nullptr;
+    const bool kc = c->scheme == KVQ_INT8_KCHAN;
+    v.k_chan = kc ? c->k_chan : nullptr;
+    v.hk_chan = kc && ht ? c->host_k_chan : nullptr;
     return v;
 }
 
@@ -269,7 +277,7 @@ const char* kvq_status_string(kvq_status s) {
 kvq_status kvq_cache_bytes(int32_t scheme, int32_t num_pages, int32_t page_size,
                            int32_t num_kv_heads, int32_t head_dim, size_t* code_bytes,
                            size_t* scale_bytes, size_t* zero_bytes) {
-    if (scheme < KVQ_INT8_SYM_TOKEN || scheme > KVQ_INT4_SYM_G32) return KVQ_ERR_INVALID_ARG;
+    if (scheme < KVQ_INT8_SYM_TOKEN || scheme > KVQ_INT8_KCHAN) return KVQ_ERR_INVALID_ARG;
     if (num_pages < 1 || page_size < 1 || num_kv_heads < 1 || head_dim < 1) return KVQ_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
     const size_t rows = (size_t)num_pages * num_kv_heads * page_size;
@@ -277,6 +285,15 @@ kvq_status kvq_cache_bytes(int32_t scheme, int32_t num_pages, int32_t page_size,
     if (code_bytes) *code_bytes = rows * (int4 || int4s ? head_dim / 2 : head_dim);
     if (scale_bytes) *scale_bytes = rows * (int4 ? (head_dim / 32) * 2 : int4s ? (head_dim / 32) * 4 : 4);
     if (zero_bytes) *zero_bytes = int4 ? rows * (head_dim / 32) * 2 : 0;
+    return KVQ_OK;
+}
+
+kvq_status kvq_kchan_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t resid_slots, size_t* chan_bytes, size_t* resid_bytes) {
+    if (num_pages < 1 || page_size < 1 || num_kv_heads < 1 || resid_slots < 0) return KVQ_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+    if (chan_bytes) *chan_bytes = (size_t)num_pages * num_kv_heads * head_dim * 2;
+    if (resid_bytes) *resid_bytes = (size_t)resid_slots * num_kv_heads * page_size * head_dim * 2;
     return KVQ_OK;
 }
 
@@ -303,6 +320,12 @@ static kvq::AppendParams append_params(const kvq_cache* cache, const int64_t* sl
     p.hv_scales = ht ? cache->host_v_scales : nullptr;
     p.hk_zeros = ht ? cache->host_k_zeros : nullptr;
     p.hv_zeros = ht ? cache->host_v_zeros : nullptr;
+    const bool kc = cache->scheme == KVQ_INT8_KCHAN;
+    p.k_chan = kc ? static_cast<uint16_t*>(cache->k_chan) : nullptr;
+    p.hk_chan = kc && ht ? static_cast<uint16_t*>(cache->host_k_chan) : nullptr;
+    p.k_resid = kc ? static_cast<uint16_t*>(cache->k_resid) : nullptr;
+    p.resid_slots = kc ? cache->resid_slots : 0;
+    p.resid_slot = nullptr;
     p.num_tokens = num_tokens;
     p.num_kv_heads = cache->num_kv_heads;
     p.page_size = cache->page_size;
@@ -310,12 +333,15 @@ static kvq::AppendParams append_params(const kvq_cache* cache, const int64_t* sl
     return p;
 }
 
-kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_t num_seqs,
-                      int32_t max_pages_per_seq, const int64_t* slot_mapping, const void* k,
-                      const void* v, int32_t num_tokens, int32_t scheme, kvq_stream_t stream) {
+// kvq_append and kvq_append_kchan (resid_slot: per-channel K only, may be null)
+static kvq_status append_impl(const kvq_cache* cache, const int32_t* block_table, int32_t num_seqs,
+                              int32_t max_pages_per_seq, const int64_t* slot_mapping, const int32_t* resid_slot,
+                              const void* k, const void* v, int32_t num_tokens, int32_t scheme,
+                              kvq_stream_t stream) {
     kvq_status st = check_cache(cache);
     if (st != KVQ_OK) return st;
     if (scheme != cache->scheme) return KVQ_ERR_SCHEME_MISMATCH;
+    if (resid_slot && (!aligned(resid_slot, 4) || cache->resid_slots < 1)) return KVQ_ERR_INVALID_ARG;
     if (num_tokens < 0) return KVQ_ERR_INVALID_ARG;
     // slots and rows are indexed in 32 bits on the device
     if (((int64_t)cache->num_pages + cache->host_pages) * cache->page_size >= ((int64_t)1 << 31) ||
@@ -338,8 +364,42 @@ kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_
             return KVQ_ERR_CUDA;
     }
     if (num_tokens == 0) return KVQ_OK;
-    const kvq::AppendParams p = append_params(cache, slot_mapping, k, v, num_tokens, err);
+    kvq::AppendParams p = append_params(cache, slot_mapping, k, v, num_tokens, err);
+    p.resid_slot = resid_slot;
     if (kvq::launch_append(p, cache->scheme, cache->head_dim, s) != cudaSuccess) return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_t num_seqs,
+                      int32_t max_pages_per_seq, const int64_t* slot_mapping, const void* k,
+                      const void* v, int32_t num_tokens, int32_t scheme, kvq_stream_t stream) {
+    return append_impl(cache, block_table, num_seqs, max_pages_per_seq, slot_mapping, nullptr, k, v, num_tokens,
+                       scheme, stream);
+}
+
+kvq_status kvq_append_kchan(const kvq_cache* cache, const int32_t* block_table, int32_t num_seqs,
+                            int32_t max_pages_per_seq, const int64_t* slot_mapping, const int32_t* resid_slot,
+                            const void* k, const void* v, int32_t num_tokens, kvq_stream_t stream) {
+    return append_impl(cache, block_table, num_seqs, max_pages_per_seq, slot_mapping, resid_slot, k, v, num_tokens,
+                       KVQ_INT8_KCHAN, stream);
+}
+
+kvq_status kvq_seal_pages(const kvq_cache* cache, const int32_t* pages, const int32_t* resid_slots, int32_t n,
+                          kvq_stream_t stream) {
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    if (cache->scheme != KVQ_INT8_KCHAN) return KVQ_ERR_SCHEME_MISMATCH;
+    if (n < 0 || cache->resid_slots < 1 || !cache->k_resid) return KVQ_ERR_INVALID_ARG;
+    if (n == 0) return KVQ_OK;
+    if (!pages || !resid_slots || !aligned(pages, 4) || !aligned(resid_slots, 4)) return KVQ_ERR_INVALID_ARG;
+    if (((int64_t)cache->num_pages + cache->host_pages) * cache->page_size >= ((int64_t)1 << 31))
+        return KVQ_ERR_INVALID_ARG;
+    unsigned* err = kvq::device_error_word();
+    if (!err) return KVQ_ERR_CUDA;
+    const kvq::AppendParams p = append_params(cache, nullptr, nullptr, nullptr, 0, err);
+    if (kvq::launch_seal(p, cache->head_dim, pages, resid_slots, n, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return KVQ_ERR_CUDA;
     return KVQ_OK;
 }
 
@@ -426,6 +486,7 @@ kvq_status kvq_decode_attn_append(const kvq_cache* cache, const void* k_new, con
                                   int32_t max_pages_per_seq, float softmax_scale, void* workspace,
                                   size_t workspace_bytes, kvq_stream_t stream) {
     if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
+    if (cache && cache->scheme == KVQ_INT8_KCHAN) return KVQ_ERR_UNSUPPORTED;  // its append takes residual slots
     kvq::DecodeParams p;
     int G = 0;
     kvq_status st = prepare_decode(cache, q, block_table, seq_lens, out, num_seqs, num_q_heads,
@@ -495,10 +556,14 @@ kvq_status kvq_copy_page(const kvq_cache* cache, int32_t src, int32_t dst, kvq_s
         {{cache->v_scales, cache->host_v_scales}, meta_b},
         {{int4 ? cache->k_zeros : nullptr, int4 ? cache->host_k_zeros : nullptr}, meta_b},
         {{int4 ? cache->v_zeros : nullptr, int4 ? cache->host_v_zeros : nullptr}, meta_b}};
+    const bool kc = cache->scheme == KVQ_INT8_KCHAN;  // the channel factors: [Hkv][head_dim] fp16 per page
+    const Pool chan = {{kc ? cache->k_chan : nullptr, kc ? cache->host_k_chan : nullptr},
+                       (size_t)cache->num_kv_heads * cache->head_dim * 2};
     const int ts = src >= cache->num_pages, td = dst >= cache->num_pages;
     const size_t is = (size_t)(src - (ts ? cache->num_pages : 0)), id = (size_t)(dst - (td ? cache->num_pages : 0));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    for (const Pool& pl : pools) {
+    for (int i = 0; i < 7; ++i) {
+        const Pool& pl = i < 6 ? pools[i] : chan;
         if (!pl.base[0]) continue;
         const uint8_t* from = static_cast<const uint8_t*>(pl.base[ts]) + is * pl.bytes;
         uint8_t* to = static_cast<uint8_t*>(pl.base[td]) + id * pl.bytes;

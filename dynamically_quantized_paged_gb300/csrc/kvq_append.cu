@@ -130,8 +130,18 @@ __global__ void __launch_bounds__(APPEND_THREADS, 2) append_kernel(AppendParams 
             if (li == 0) flag_error(p.err, ERR_BAD_TABLE);
             sl = -1;
         }
-        const bool valid = sl >= 0;
+        bool valid = sl >= 0;
         const uint32_t t = fast_div((uint32_t)(in_chunk ? pi : 0), p.heads_mul, p.heads_shift);
+        int32_t rs = -1;  // per-channel K: the token's residual slot
+        if constexpr (SCHEME == KVQ_INT8_KCHAN) {
+            if (valid && p.resid_slot) {
+                rs = __ldg(p.resid_slot + t);
+                if (rs >= p.resid_slots) {  // nothing is written for the token
+                    if (li == 0) flag_error(p.err, ERR_BAD_TABLE);
+                    valid = false;
+                }
+            }
+        }
         const int h = (int)((uint32_t)(in_chunk ? pi : 0) - t * (uint32_t)H);
         // pool row of this (slot, head): [page][head][offset] in the page's tier
         const uint32_t pg = valid ? fast_div((uint32_t)sl, p.page_mul, p.page_shift) : 0u;
@@ -139,16 +149,90 @@ __global__ void __launch_bounds__(APPEND_THREADS, 2) append_kernel(AppendParams 
         const bool host = pg >= (uint32_t)p.num_pages;
         const uint32_t pi_t = host ? pg - (uint32_t)p.num_pages : pg;
         const int64_t prow = ((int64_t)pi_t * H + h) * p.page_size + off;
-        const LaneCodes ck = quantize_lane<SCHEME, LPR>(rk);
-        const LaneCodes cv = quantize_lane<SCHEME, LPR>(rv);
+        // the per-channel K scheme stores an open page's rows by the INT8 token rule
+        constexpr int QS = SCHEME == KVQ_INT8_KCHAN ? KVQ_INT8_SYM_TOKEN : SCHEME;
+        const LaneCodes ck = quantize_lane<QS, LPR>(rk);
+        const LaneCodes cv = quantize_lane<QS, LPR>(rv);
         if (valid) {  // into the pools of the page's tier
-            store_lane<SCHEME, D>(ck, host ? p.hk_codes : p.k_codes, host ? p.hk_scales : p.k_scales,
-                                  host ? p.hk_zeros : p.k_zeros, prow, li);
-            store_lane<SCHEME, D>(cv, host ? p.hv_codes : p.v_codes, host ? p.hv_scales : p.v_scales,
-                                  host ? p.hv_zeros : p.v_zeros, prow, li);
+            store_lane<QS, D>(ck, host ? p.hk_codes : p.k_codes, host ? p.hk_scales : p.k_scales,
+                              host ? p.hk_zeros : p.k_zeros, prow, li);
+            store_lane<QS, D>(cv, host ? p.hv_codes : p.v_codes, host ? p.hv_scales : p.v_scales,
+                              host ? p.hv_zeros : p.v_zeros, prow, li);
+            if constexpr (SCHEME == KVQ_INT8_KCHAN) {
+                if (off == 0) {  // the page's first token opens it: channel factors 1.0
+                    const uint4 ones = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+                    uint4* f = reinterpret_cast<uint4*>((host ? p.hk_chan : p.k_chan) +
+                                                        ((int64_t)pi_t * H + h) * D + li * 16);
+                    f[0] = ones;
+                    f[1] = ones;
+                }
+                if (rs >= 0) {  // the bf16 K row, kept for the page's seal
+                    uint4* r = reinterpret_cast<uint4*>(p.k_resid +
+                                                        (((int64_t)rs * H + h) * p.page_size + off) * D + li * 16);
+                    r[0] = rk[0];
+                    r[1] = rk[1];
+                }
+            }
         }
     }
     cp_async_wait<0>();
+}
+
+// Seal of the per-channel K scheme: one CTA per (pair i, KV head h), one
+// thread per channel j.  The page rule down each channel of the residual
+// slot's rows ("KV Cache Optimization: Strategies for Faster LLM Inference",
+// section "KV Cache Quantization: When and How to Compress": per-channel
+// scales; the absmax rule of "Dynamic KV Cache Quantization for Fast LLM
+// Inference", section "Understanding Dynamic Quantization Techniques"):
+// s_j = max_t |x| / 127, S = max_j s_j, factor r_j = fp16 round-up of
+// s_j / S, code = round-half-even(x / (r_j S)), every token scale S; each
+// step one correctly rounded IEEE operation.  Not on the decode's path (once
+// per filled page), so the quotients are plain IEEE divisions.
+template <int D>
+__global__ void __launch_bounds__(D) seal_kernel(AppendParams p, const int32_t* pages, const int32_t* rslots) {
+    const int i = blockIdx.x, h = blockIdx.y, j = threadIdx.x;
+    const int H = p.num_kv_heads, P = p.page_size;
+    const int32_t page = pages[i], rs = rslots[i];
+    if (page < 0 || (int64_t)page * P >= p.num_slots || rs < 0 || rs >= p.resid_slots) {
+        if (h == 0 && j == 0) flag_error(p.err, ERR_BAD_TABLE);
+        return;
+    }
+    const uint16_t* x = p.k_resid + ((int64_t)rs * H + h) * P * D + j;
+    float amax = 0.0f;
+    for (int t = 0; t < P; ++t) amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)x[(int64_t)t * D] << 16)));
+    const float sj = __fdiv_rn(amax, 127.0f);
+    __shared__ float red[D / 32];
+    float S = sj;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) S = fmaxf(S, __shfl_xor_sync(0xffffffffu, S, o));
+    if ((j & 31) == 0) red[j >> 5] = S;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) S = fmaxf(S, red[w]);
+    const bool host = page >= p.num_pages;
+    const int64_t pg = host ? page - p.num_pages : page;
+    const int64_t row0 = (pg * H + h) * P;
+    int8_t* codes = reinterpret_cast<int8_t*>(host ? p.hk_codes : p.k_codes) + row0 * D + j;
+    float* tok = static_cast<float*>(host ? p.hk_scales : p.k_scales) + row0;
+    uint16_t* chan = (host ? p.hk_chan : p.k_chan) + (pg * H + h) * D + j;
+    if (S == 0.0f) {  // an all-zero block: the zero-row convention
+        for (int t = 0; t < P; ++t) codes[(int64_t)t * D] = 0;
+        *chan = 0x3C00;
+        for (int t = j; t < P; t += D) tok[t] = 1.0f;
+        return;
+    }
+    const __half r = __float2half_ru(__fdiv_rn(sj, S));
+    const float e = __fmul_rn(__half2float(r), S);
+    for (int t = 0; t < P; ++t) {
+        int q = 0;
+        if (e != 0.0f) {
+            const float y = rintf(__fdiv_rn(__uint_as_float((uint32_t)x[(int64_t)t * D] << 16), e));
+            q = (int)fminf(fmaxf(y, -127.0f), 127.0f);
+        }
+        codes[(int64_t)t * D] = (int8_t)q;
+    }
+    *chan = __half_as_ushort(r);
+    for (int t = j; t < P; t += D) tok[t] = S;
 }
 
 // K4: every page a sequence uses must lie in the pool, and the sequence must
@@ -218,6 +302,8 @@ cudaError_t launch_append_t(AppendParams p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaStream_t s) {
+    if (scheme == KVQ_INT8_KCHAN)
+        return head_dim == 128 ? launch_append_t<KVQ_INT8_KCHAN, 128>(p, s) : launch_append_t<KVQ_INT8_KCHAN, 64>(p, s);
     if (head_dim == 128) {
         if (scheme == KVQ_INT8_SYM_TOKEN) return launch_append_t<KVQ_INT8_SYM_TOKEN, 128>(p, s);
         if (scheme == KVQ_FP8E4M3_TOKEN) return launch_append_t<KVQ_FP8E4M3_TOKEN, 128>(p, s);
@@ -228,6 +314,14 @@ cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaS
     if (scheme == KVQ_FP8E4M3_TOKEN) return launch_append_t<KVQ_FP8E4M3_TOKEN, 64>(p, s);
     if (scheme == KVQ_INT4_SYM_G32) return launch_append_t<KVQ_INT4_SYM_G32, 64>(p, s);
     return launch_append_t<KVQ_INT4_ASYM_G32, 64>(p, s);
+}
+
+cudaError_t launch_seal(const AppendParams& p, int head_dim, const int32_t* pages, const int32_t* rslots, int n,
+                        cudaStream_t s) {
+    const dim3 grid((unsigned)n, (unsigned)p.num_kv_heads);
+    if (head_dim == 128) seal_kernel<128><<<grid, 128, 0, s>>>(p, pages, rslots);
+    else seal_kernel<64><<<grid, 64, 0, s>>>(p, pages, rslots);
+    return cudaGetLastError();
 }
 
 // slots[b]: the physical slot of position seq_lens[b] - 1 of sequence b,

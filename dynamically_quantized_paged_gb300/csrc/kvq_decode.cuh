@@ -484,9 +484,11 @@ cudaError_t launch_decode_partial_int8(const DecodeParams& p, int G, cudaStream_
 cudaError_t launch_decode_partial_fp8(const DecodeParams& p, int G, cudaStream_t s);
 cudaError_t launch_decode_partial_int4(const DecodeParams& p, int G, cudaStream_t s);
 cudaError_t launch_decode_partial_int4sym(const DecodeParams& p, int G, cudaStream_t s);
+cudaError_t launch_decode_partial_int8kc(const DecodeParams& p, int G, cudaStream_t s);
 int decode_ctas_per_sm_int8(int head_dim, int G, int B);
 int decode_ctas_per_sm_fp8(int head_dim, int G, int B);
 int decode_ctas_per_sm_int4(int head_dim, int G, int B);
 int decode_ctas_per_sm_int4sym(int head_dim, int G, int B);
+int decode_ctas_per_sm_int8kc(int head_dim, int G, int B);
 
 }  // namespace kvq

@@ -38,6 +38,9 @@ struct CacheView {
     const void* hv_scales;
     const void* hk_zeros;
     const void* hv_zeros;
+    // per-channel K scheme: channel factors of the two tiers (fp16 [page][head][D])
+    const void* k_chan;
+    const void* hk_chan;
 };
 
 // The pools that hold page id `page` (the device tier below num_pages, the
@@ -50,6 +53,7 @@ struct PagePools {
     const uint8_t* v_scales;
     const uint8_t* k_zeros;
     const uint8_t* v_zeros;
+    const uint8_t* k_chan;
     int index;
 };
 __host__ __device__ inline PagePools page_pools(const CacheView& c, int page) {
@@ -61,6 +65,7 @@ __host__ __device__ inline PagePools page_pools(const CacheView& c, int page) {
     r.v_scales = static_cast<const uint8_t*>(host ? c.hv_scales : c.v_scales);
     r.k_zeros = static_cast<const uint8_t*>(host ? c.hk_zeros : c.k_zeros);
     r.v_zeros = static_cast<const uint8_t*>(host ? c.hv_zeros : c.v_zeros);
+    r.k_chan = static_cast<const uint8_t*>(host ? c.hk_chan : c.k_chan);
     r.index = host ? page - c.num_pages : page;
     return r;
 }
@@ -79,6 +84,14 @@ struct AppendParams {
     void* hv_scales;
     void* hk_zeros;
     void* hv_zeros;
+    // per-channel K scheme: channel factors of the two tiers (fp16 bits),
+    // the residual pool (bf16 [resid_slots][H][page_size][D]) and each
+    // token's residual slot (null: none)
+    uint16_t* k_chan;
+    uint16_t* hk_chan;
+    uint16_t* k_resid;
+    const int32_t* resid_slot;
+    int resid_slots;
     int num_pages;
     const int64_t* slot_mapping;
     const uint16_t* k;  // bf16 bits
@@ -155,6 +168,9 @@ inline size_t decode_workspace_bytes(int n_ctas, int G, int D, int B, int Hkv, i
 }
 
 cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaStream_t s);
+// Per-channel K: seals pages[i] from residual slot rslots[i], i < n.
+cudaError_t launch_seal(const AppendParams& p, int head_dim, const int32_t* pages, const int32_t* rslots, int n,
+                        cudaStream_t s);
 // slots[b] = the physical slot of position seq_lens[b] - 1 of sequence b (from
 // its block-table row), -1 for an empty sequence or a page id outside the
 // pool (flagged)

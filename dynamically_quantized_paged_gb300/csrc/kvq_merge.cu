@@ -9,6 +9,7 @@ cudaError_t launch_decode_partial(const DecodeParams& p, int G, cudaStream_t s) 
         case KVQ_INT8_SYM_TOKEN: return launch_decode_partial_int8(p, G, s);
         case KVQ_FP8E4M3_TOKEN: return launch_decode_partial_fp8(p, G, s);
         case KVQ_INT4_SYM_G32: return launch_decode_partial_int4sym(p, G, s);
+        case KVQ_INT8_KCHAN: return launch_decode_partial_int8kc(p, G, s);
         default: return launch_decode_partial_int4(p, G, s);
     }
 }
@@ -18,6 +19,7 @@ int decode_ctas_per_sm(int scheme, int head_dim, int G, int B) {
         case KVQ_INT8_SYM_TOKEN: return decode_ctas_per_sm_int8(head_dim, G, B);
         case KVQ_FP8E4M3_TOKEN: return decode_ctas_per_sm_fp8(head_dim, G, B);
         case KVQ_INT4_SYM_G32: return decode_ctas_per_sm_int4sym(head_dim, G, B);
+        case KVQ_INT8_KCHAN: return decode_ctas_per_sm_int8kc(head_dim, G, B);
         default: return decode_ctas_per_sm_int4(head_dim, G, B);
     }
 }

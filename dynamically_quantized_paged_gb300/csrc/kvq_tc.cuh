@@ -251,7 +251,10 @@ __device__ __forceinline__ float fkey_inv(int k) { return __int_as_float(k ^ ((k
 // ---------------------------------------------------------------- configuration
 template <int SCHEME, int D, int G>
 struct Cfg {
-    static constexpr bool INT8 = SCHEME == KVQ_INT8_SYM_TOKEN;
+    // the per-channel K scheme is INT8 whose widened K columns are also
+    // multiplied by the page's channel factors (KCH)
+    static constexpr bool INT8 = SCHEME == KVQ_INT8_SYM_TOKEN || SCHEME == KVQ_INT8_KCHAN;
+    static constexpr bool KCH = SCHEME == KVQ_INT8_KCHAN;
     static constexpr bool FP8 = SCHEME == KVQ_FP8E4M3_TOKEN;
     // both INT4 schemes share the 4-bit layout and the group arithmetic; the
     // symmetric one has fp32 scales, no stored zero-point (zero = -8 scale
@@ -275,7 +278,10 @@ struct Cfg {
     // tensor memory columns
     static constexpr int KCOL = D / 2;  // fp16 pairs of one K row
     static constexpr int TM_K = 0;      // 2 x KCOL
-    static constexpr int TM_S = 2 * KCOL;
+    // KCH: the low parts of the K rows, 2 x KCOL more (code * factor = hi + lo
+    // exactly; the scores MMA accumulates both)
+    static constexpr int TM_KLO = 2 * KCOL;
+    static constexpr int TM_S = (KCH ? 4 : 2) * KCOL;
     static constexpr int TM_O = TM_S + 2 * NS;
     static constexpr int TM_USED = TM_O + 2 * NO;
     static constexpr int TM_COLS = TM_USED <= 32 ? 32 : TM_USED <= 64 ? 64 : TM_USED <= 128 ? 128
@@ -293,7 +299,8 @@ struct Cfg {
     static constexpr int RKZ = RVS + T * MB;
     static constexpr int RVZ = RKZ + (INT4 && !SYM4 ? T * MB : 0);
     static constexpr int RQ = RVZ + (INT4 && !SYM4 ? T * MB : 0);
-    static constexpr int STAGE = RQ + G * D * 2;
+    static constexpr int RKC = RQ + G * D * 2;             // per unit: D fp16 channel factors (KCH)
+    static constexpr int STAGE = RKC + (KCH ? TU * D * 2 : 0);
     // operand buffers: V^T (128 channel rows x T tokens, fp16, MN-major:
     // (c, t) at (c/8)*VS_SBO + (t/8)*128 + (t%8)*16 + (c%8)*2), the query
     // operand (NS rows x D, K-major: (n, c) at (n/8)*QB_SBO + (c/8)*128 +
@@ -556,6 +563,12 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                 else if (C::INT4 && !C::SYM4 && which == 2) { src = pp.k_zeros; dst = C::RKZ; }
                 else if (C::INT4 && !C::SYM4 && which == 3) { src = pp.v_zeros; dst = C::RVZ; }
                 if (src) cp_async16(st + dst + uu * UNIT * C::MB + 16 * part, src + row * C::MB + 16 * part);
+                if constexpr (C::KCH) {  // the unit's page's channel factors: lanes 16 .. 16 + D/8 - 1
+                    const int cl = lane - 16;
+                    if (cl >= 0 && cl < D / 8)
+                        cp_async16(st + C::RKC + uu * D * 2 + 16 * cl,
+                                   pp.k_chan + ((int64_t)pp.index * Hkv + pc.h) * D * 2 + 16 * cl);
+                }
             }
             if (pw == 0 && lane == 0) {
                 sm.stage_bad()[s] = bad;
@@ -605,6 +618,12 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_tmem_a(tmem + C::TM_S + b * C::NS, tmem + C::TM_K + b * C::KCOL + kk * 8,
                                smem_desc(q + kk * 256, 128, C::QB_SBO), IDS, kk > 0);
+                if constexpr (C::KCH) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_tmem_a(tmem + C::TM_S + b * C::NS, tmem + C::TM_KLO + b * C::KCOL + kk * 8,
+                                   smem_desc(q + kk * 256, 128, C::QB_SBO), IDS, true);
+                }
                 mma_commit(sdone(b));
                 if (i >= 1) issue_values(i - 1);
             }
@@ -760,6 +779,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
 #pragma unroll
             for (int c0 = 0; c0 < C::NCH; c0 += CPS) {
                 uint32_t r[16];
+                uint32_t rlo[C::KCH ? 16 : 1];  // KCH: the low parts
 #pragma unroll
                 for (int cc = 0; cc < CPS; ++cc) {
                     const uint4 raw = *reinterpret_cast<const uint4*>(st + C::RK + 16 * swz(t * C::NCH + c0 + cc));
@@ -767,6 +787,31 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                     if constexpr (C::INT8) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k) s8x4_to_h2x2(w4[k], r[cc * 8 + 2 * k], r[cc * 8 + 2 * k + 1]);
+                        if constexpr (C::KCH) {
+                            // r[cc * 8 + i] holds channels 16 (c0 + cc) + 2i, + 1:
+                            // times the unit's factors of the same channels as
+                            // hi = fp16(code * f) and lo = fp16(code * f - hi),
+                            // whose sum is the product exactly (code * f has at
+                            // most 18 significant bits on the grid of f's last
+                            // bit, so the remainder fits fp16); the token scale
+                            // follows the MMA
+                            const uint4* f =
+                                reinterpret_cast<const uint4*>(st + C::RKC + uu * D * 2 + (c0 + cc) * 32);
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const uint4 fv = f[h2];
+                                const uint32_t fw[4] = {fv.x, fv.y, fv.z, fv.w};
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const __half2 x = *reinterpret_cast<const __half2*>(&r[cc * 8 + h2 * 4 + k]);
+                                    const __half2 fk = *reinterpret_cast<const __half2*>(&fw[k]);
+                                    const __half2 hi = __hmul2(x, fk);
+                                    const __half2 lo = __hfma2(x, fk, __hneg2(hi));
+                                    r[cc * 8 + h2 * 4 + k] = *reinterpret_cast<const uint32_t*>(&hi);
+                                    rlo[cc * 8 + h2 * 4 + k] = *reinterpret_cast<const uint32_t*>(&lo);
+                                }
+                            }
+                        }
                     } else if constexpr (C::FP8) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
@@ -785,6 +830,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                     }
                 }
                 tmem_st16(ta + c0 * (C::INT4 ? 16 : 8), r);
+                if constexpr (C::KCH) tmem_st16(ta + (C::TM_KLO - C::TM_K) + c0 * 8, rlo);
             }
             tmem_st_wait();
             fence_proxy_async_smem();  // query operand writes

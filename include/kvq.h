@@ -76,7 +76,24 @@ typedef enum kvq_scheme {
      * for an all-zero group), code = round-half-even(x / scale) in [-7, 7],
      * stored as 4-bit two's complement, two codes per byte, even channel in
      * the low nibble; no zero-point ([P1] with bits = 4). */
-    KVQ_INT4_SYM_G32 = 4
+    KVQ_INT4_SYM_G32 = 4,
+    /* INT8 with per-channel K scales ([P3] section "KV Cache Quantization:
+     * When and How to Compress": per-channel keeps more than per-tensor).
+     * V is KVQ_INT8_SYM_TOKEN throughout.  K takes one scale per (page, KV
+     * head, channel), fixed when the page is sealed (kvq_seal_pages) from
+     * the page's bf16 rows, which the append keeps in a residual slot while
+     * the page fills; until then the page's K rows are stored by the token
+     * rule.  Dequantized K = code * k_chan[page][head][channel] (fp16) *
+     * k_scales[page][head][token] (fp32).  An open page has channel factors
+     * 1.0 (written by the append of the token at offset 0) and its tokens'
+     * INT8 scales.  A sealed (page, head) block x[t][j] stores, with
+     * s_j = max_t |x| / 127 and S = max_j s_j (fp32 divisions):
+     *   k_chan[j]  = fp16 round-up of s_j / S (fp32 division), in [0, 1];
+     *   code       = round-half-even(x / (k_chan[j] * S)) in [-127, 127], the
+     *                product and the quotient fp32; 0 where k_chan[j] = 0;
+     *   k_scales[t] = S for every token.
+     * An all-zero block stores codes 0, factors 1.0 and scales 1.0. */
+    KVQ_INT8_KCHAN = 5
 } kvq_scheme;
 
 /* One layer of the paged quantized cache ([P1] section "Integrating Dynamic
@@ -108,7 +125,13 @@ typedef enum kvq_scheme {
  * kvq_copy_page moves a page between the tiers (offload: device page to a
  * free host page; fetch: the reverse), after which the caller rewrites the
  * block-table entry.  host_pages = 0 (with NULL host pools) is the plain
- * device-only cache.  A slot s names page s / page_size in either tier. */
+ * device-only cache.  A slot s names page s / page_size in either tier.
+ *
+ * KVQ_INT8_KCHAN adds the channel factors, k_chan [num_pages][num_kv_heads]
+ * [head_dim] fp16 (host_k_chan likewise for the host tier), and the residual
+ * pool k_resid [resid_slots][num_kv_heads][page_size][head_dim] bf16 (device
+ * memory; resid_slots may be 0 with k_resid NULL), sized by kvq_kchan_bytes.
+ * These fields are ignored (and may be anything) for the other schemes. */
 typedef struct kvq_cache {
     int32_t scheme;       /* kvq_scheme */
     int32_t num_pages;
@@ -129,6 +152,10 @@ typedef struct kvq_cache {
     void* host_v_scales;
     void* host_k_zeros;   /* asymmetric INT4 only */
     void* host_v_zeros;   /* asymmetric INT4 only */
+    void* k_chan;         /* KVQ_INT8_KCHAN only: channel factors */
+    void* host_k_chan;    /* KVQ_INT8_KCHAN only: host-tier channel factors */
+    void* k_resid;        /* KVQ_INT8_KCHAN only: residual bf16 K rows of open pages */
+    int32_t resid_slots;  /* KVQ_INT8_KCHAN only: slots of k_resid */
 } kvq_cache;
 
 /* Human-readable name of a status.  Never NULL; static storage. */
@@ -144,6 +171,14 @@ const char* kvq_status_string(kvq_status status);
 kvq_status kvq_cache_bytes(int32_t scheme, int32_t num_pages, int32_t page_size,
                            int32_t num_kv_heads, int32_t head_dim, size_t* code_bytes,
                            size_t* scale_bytes, size_t* zero_bytes);
+
+/* KVQ_INT8_KCHAN's extra pools: chan_bytes for k_chan with num_pages pages
+ * (2 bytes per page, KV head and channel), resid_bytes for k_resid with
+ * resid_slots slots (page_size bf16 rows per slot and KV head).  Its codes
+ * and scales are sized by kvq_cache_bytes like KVQ_INT8_SYM_TOKEN.  Host
+ * only; either output may be NULL. */
+kvq_status kvq_kchan_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t resid_slots, size_t* chan_bytes, size_t* resid_bytes);
 
 /* Quantize-append ([P2] "Key-Value Tensor Capture" and "Dynamic FP8/INT8
  * Quantization"; [P1] "Understanding Dynamic Quantization Techniques").
@@ -165,6 +200,37 @@ kvq_status kvq_cache_bytes(int32_t scheme, int32_t num_pages, int32_t page_size,
 kvq_status kvq_append(const kvq_cache* cache, const int32_t* block_table, int32_t num_seqs,
                       int32_t max_pages_per_seq, const int64_t* slot_mapping, const void* k,
                       const void* v, int32_t num_tokens, int32_t scheme, kvq_stream_t stream);
+
+/* Quantize-append for KVQ_INT8_KCHAN: kvq_append (same arguments, rules and
+ * errors) plus, per token,
+ *   resid_slot    device, int32 [num_tokens], or NULL (no residual rows): the
+ *                 residual slot that keeps the token's bf16 K rows (every KV
+ *                 head), at the token's page offset; -1 keeps none.  A slot
+ *                 >= cache->resid_slots skips the token (nothing written) and
+ *                 flags KVQ_ERR_BAD_TABLE.
+ * The token at offset 0 of a page also sets that page's channel factors to
+ * 1.0 (it opens the page; a page is appended to only while open).  Pages
+ * whose bf16 rows are not all in one residual slot cannot be sealed and
+ * keep the token rule.  KVQ_ERR_SCHEME_MISMATCH unless cache->scheme is
+ * KVQ_INT8_KCHAN.  kvq_append on such a cache equals this call with
+ * resid_slot NULL. */
+kvq_status kvq_append_kchan(const kvq_cache* cache, const int32_t* block_table, int32_t num_seqs,
+                            int32_t max_pages_per_seq, const int64_t* slot_mapping, const int32_t* resid_slot,
+                            const void* k, const void* v, int32_t num_tokens, kvq_stream_t stream);
+
+/* Seals pages of a KVQ_INT8_KCHAN cache: for each i < n, page pages[i] (in
+ * either tier; every KV head) takes the per-channel K rule of the
+ * page_size bf16 rows in residual slot resid_slots[i] (the rule under
+ * KVQ_INT8_KCHAN): its K codes, channel factors and K token scales are
+ * rewritten; V is left as it is.  The caller seals a page once the append
+ * that fills it is on the stream (every offset of the slot written for
+ * that page), and may then reuse the slot.  pages, resid_slots: device,
+ * int32 [n].  An id outside its pool skips that pair and flags
+ * KVQ_ERR_BAD_TABLE.  n == 0 launches nothing; KVQ_ERR_SCHEME_MISMATCH
+ * unless cache->scheme is KVQ_INT8_KCHAN; KVQ_ERR_INVALID_ARG if the cache
+ * has no residual pool or n < 0. */
+kvq_status kvq_seal_pages(const kvq_cache* cache, const int32_t* pages, const int32_t* resid_slots, int32_t n,
+                          kvq_stream_t stream);
 
 /* Device scratch needed by kvq_decode_attn / kvq_decode_partial /
  * kvq_decode_merge for this cache geometry and query-head count on the
@@ -242,7 +308,9 @@ kvq_status kvq_decode_attn_out(const kvq_cache* cache, const void* q, const int3
  * asymmetric INT4) this is ONE launch: the warp that reads a sequence's last
  * position quantizes the new token by the append's rule (the same device
  * code) into its staged copy of the page and into the cache.  Elsewhere it
- * is the append kernel followed by the decode, on the stream. */
+ * is the append kernel followed by the decode, on the stream.
+ * KVQ_ERR_UNSUPPORTED for KVQ_INT8_KCHAN, whose append needs residual slots
+ * (kvq_append_kchan, then the decode). */
 kvq_status kvq_decode_attn_append(const kvq_cache* cache, const void* k_new, const void* v_new, const void* q,
                                   const int32_t* block_table, const int32_t* seq_lens, void* out,
                                   int32_t out_dtype, int32_t num_seqs, int32_t num_q_heads,
@@ -346,8 +414,8 @@ kvq_status kvq_share_pages(kvq_allocator* alloc, int32_t n, const int32_t* pages
 kvq_status kvq_page_refcount(const kvq_allocator* alloc, int32_t page, int32_t* refs);
 int32_t kvq_allocator_free_count(const kvq_allocator* alloc);
 
-/* Copies every pool's contents of page src (codes, scales, INT4 zero-points:
- * all of its KV heads and slots) to page dst on the stream.  Two uses:
+/* Copies every pool's contents of page src (codes, scales, INT4 zero-points,
+ * channel factors: all of its KV heads and slots) to page dst on the stream.  Two uses:
  * copy-on-write, so that a sequence whose shared prefix ends inside a page
  * can take its own copy of that page before appending past the prefix; and
  * moving a page between the device and host tiers (offload of a cold page,

@@ -179,15 +179,20 @@ def test_copy_page_argument_errors_before_any_device_access():
     assert kvq.lib.kvq_copy_page(ctypes.byref(fake_cache(head_dim=96)), 0, 1, None) == 7
 
 
-def fake_cache(scheme=1, head_dim=128, page_size=16, heads=8, align=256, group=32, num_pages=4, host_pages=0):
+def fake_cache(scheme=1, head_dim=128, page_size=16, heads=8, align=256, group=32, num_pages=4, host_pages=0,
+               resid_slots=0, k_chan=True, host_k_chan=True, k_resid=True):
     base = 1 << 20  # never dereferenced: argument checks run before any device access
     p = lambda i: base + i * (1 << 16) + (0 if align >= 16 else align)
     h = lambda i: p(6 + i) if host_pages > 0 else None
+    kc = scheme == 5
     return kvq.CacheStruct(scheme, num_pages, page_size, heads, head_dim, group if scheme == 3 else 0,
                            p(0), p(1), p(2), p(3), p(4) if scheme == 3 else None,
                            p(5) if scheme == 3 else None,
                            host_pages, h(0), h(1), h(2), h(3), h(4) if scheme == 3 else None,
-                           h(5) if scheme == 3 else None)
+                           h(5) if scheme == 3 else None,
+                           p(12) if kc and k_chan else None,
+                           p(13) if kc and host_k_chan and host_pages > 0 else None,
+                           p(14) if kc and k_resid and resid_slots > 0 else None, resid_slots)
 
 
 def test_cache_struct_layout_matches_the_header():
@@ -199,7 +204,42 @@ def test_cache_struct_layout_matches_the_header():
     assert names == [f[0] for f in kvq.CacheStruct._fields_]
     off = {f[0]: getattr(kvq.CacheStruct, f[0]).offset for f in kvq.CacheStruct._fields_}
     assert off["k_codes"] == 24 and off["host_pages"] == 72 and off["host_k_codes"] == 80
-    assert ctypes.sizeof(kvq.CacheStruct) == 128
+    assert off["k_chan"] == 128 and off["k_resid"] == 144 and off["resid_slots"] == 152
+    assert ctypes.sizeof(kvq.CacheStruct) == 160
+
+
+def test_kchan_sizes_and_argument_errors_before_any_device_access():
+    """The per-channel K scheme's pools, its append, seal and the refusal of
+    the fused decode-append: every rule of the header checked on the host."""
+    c, r = ctypes.c_size_t(), ctypes.c_size_t()
+    assert kvq.lib.kvq_kchan_bytes(10, 16, 8, 128, 3, ctypes.byref(c), ctypes.byref(r)) == 0
+    assert c.value == 10 * 8 * 128 * 2 and r.value == 3 * 8 * 16 * 128 * 2
+    assert kvq.lib.kvq_kchan_bytes(10, 16, 8, 96, 3, None, None) == 7
+    assert kvq.lib.kvq_kchan_bytes(10, 16, 8, 128, -1, None, None) == 1
+    assert kvq.cache_bytes("int8kc", 10, 16, 8, 128) == kvq.cache_bytes("int8", 10, 16, 8, 128)
+    ok = fake_cache(scheme=5, resid_slots=2)
+    # the channel-factor pool is required; the residual pool when it has slots
+    assert call_append(fake_cache(scheme=5, k_chan=False)) == 1
+    assert call_append(fake_cache(scheme=5, resid_slots=2, k_resid=False)) == 1
+    assert call_append(fake_cache(scheme=5, resid_slots=-1)) == 1
+    assert call_append(fake_cache(scheme=5, host_pages=2, host_k_chan=False)) == 1
+    assert call_append(ok, T=0) == 0  # valid: nothing to launch
+    L = kvq.lib
+    # append_kchan: scheme, alignment of the residual-slot array
+    assert L.kvq_append_kchan(ctypes.byref(fake_cache(scheme=1)), None, 0, 1, None, None, None, None, 0, None) == 2
+    assert L.kvq_append_kchan(ctypes.byref(ok), None, 0, 1, None, (1 << 20) + 2, None, None, 0, None) == 1
+    assert L.kvq_append_kchan(ctypes.byref(fake_cache(scheme=5)), None, 0, 1, None, 1 << 20, None, None, 0,
+                              None) == 1  # residual slots named, but the cache has none
+    assert L.kvq_append_kchan(ctypes.byref(ok), None, 0, 1, None, 1 << 20, None, None, 0, None) == 0
+    # seal: scheme, residual pool, n
+    assert L.kvq_seal_pages(ctypes.byref(fake_cache(scheme=1)), None, None, 0, None) == 2
+    assert L.kvq_seal_pages(ctypes.byref(fake_cache(scheme=5)), None, None, 0, None) == 1
+    assert L.kvq_seal_pages(ctypes.byref(ok), None, None, -1, None) == 1
+    assert L.kvq_seal_pages(ctypes.byref(ok), None, None, 0, None) == 0
+    assert L.kvq_seal_pages(ctypes.byref(ok), None, None, 3, None) == 1  # null arrays
+    # the fused decode-append needs residual slots: refused
+    args = [None] * 6 + [0, 1, 4, 1, ctypes.c_float(0.0), None, ctypes.c_size_t(0), None]
+    assert L.kvq_decode_attn_append(ctypes.byref(ok), *args) == 7
 
 
 def test_host_tier_argument_errors_before_any_device_access():
