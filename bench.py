@@ -3,7 +3,9 @@
 A step is one pass of the whole hot path over one batch: quantize-append of
 the step's new tokens (kvq_append) and split-K fused-dequant decode attention
 with its merge (kvq_decode_attn: one launch), for every layer of the
-workload.  Pages come from the library's host allocator (scattered ids).
+workload; with per-channel K scales (workload 6) the append keeps the new
+tokens' bf16 K rows and the pages it fills are sealed (kvq_append_kchan,
+kvq_seal_pages) before the decode.  Pages come from the library's host allocator (scattered ids).
 Inputs are resident in HBM when the timed region starts; L2 is flushed (a
 256 MB write, then a 256 MB read that evicts the write's dirty lines, so their
 write-back does not run under the timed kernels) before every timed step,
@@ -13,7 +15,7 @@ Headline workload (N=1 default): the largest single-GPU configuration, the
 8-layer INT4 workload -- 16 sequences x 32768 cached tokens, 32 query / 8 KV
 heads, head_dim 128, page 32, asymmetric INT4 in groups of 32 -- decode step
 plus 1-token append per layer.  At N=1 the same JSON line carries one
-sub-record per other workload (--sub, default 2,3,5), each with its own
+sub-record per other workload (--sub, default 2,3,5,6), each with its own
 decode roofline, append figures, end-to-end figure, clocks and CPU baseline.
 
 Timing.  The headline `ms_per_step` is the mean over exactly --steps steps
@@ -30,7 +32,7 @@ pages and block-table rows for its share and no data moves between ranks.
 `value` is all ranks' algorithmic bytes over the slowest rank's time (total
 work fixed as N grows: "scaling": "strong").
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--sub 2,3,5] [--impl kvq|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--sub 2,3,5,6] [--impl kvq|reference]
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle (the
 only reference implementation there is) on the host cores, on a bounded
@@ -96,9 +98,26 @@ def algorithmic_bytes(w: inp.Workload, lens: np.ndarray, n_new: np.ndarray) -> d
     decode = kv + table + q + out + B * 4
     T = int(n_new.sum())
     append = T * (2 * H * D * 2 + 8 + 2 * H * (cb + mb))
+    seal = 0
+    if w.scheme == "int8kc":
+        # per-channel K: the channel factors of every page in use are read;
+        # the append also reads the residual slot ids and writes each new
+        # token's bf16 K rows (and the factors of a page it opens); the seal
+        # of each page the step fills reads its residual rows and ids and
+        # writes its K codes, factors and token scales
+        decode += table // 4 * H * D * 2
+        opened = int(sum(((np.arange(L - n, L) % P) == 0).sum() for L, n in zip(lens, n_new)))
+        append += T * (4 + H * D * 2) + opened * H * D * 2
+        filled = sealed_pages_of_step(lens, n_new, P)
+        seal = filled * (8 + H * (P * D * 2 + P * D + D * 2 + P * 4))
     L = w.layers
-    return {"decode": decode * L, "append": append * L, "step": (decode + append) * L,
+    return {"decode": decode * L, "append": append * L, "seal": seal * L, "step": (decode + append + seal) * L,
             "append_tokens": T * L, "kv_bytes": kv * L}
+
+
+def sealed_pages_of_step(lens, n_new, P: int) -> int:
+    """Pages that a step's new tokens complete (their last offset written)."""
+    return int(sum(((np.arange(L - n, L) % P) == P - 1).sum() for L, n in zip(lens, n_new)))
 
 
 def partition_sequences(lens, world: int) -> list:
@@ -117,15 +136,19 @@ def partition_sequences(lens, world: int) -> list:
     return [np.array(sorted(s), np.int64) for s in shares]
 
 
-def append_line(nb: dict, w: inp.Workload, k1_mean_ms: float, peak_gbs: float, fused: bool = False) -> dict:
+def append_line(nb: dict, w: inp.Workload, k1_mean_ms: float, peak_gbs: float, fused: bool = False,
+                kchan: bool = False) -> dict:
     """The quantize-append launch on its own: tokens per second, and its
     algorithmic bytes (bf16 K/V read, slots read, codes and scales written)
     per second against the HBM peak.  Fused into the decode launch, its time
     is taken as that whole launch's (k1_mean_ms is then the decode's)."""
     T = nb["append_tokens"] // w.layers      # tokens per launch
-    b = nb["append"] // w.layers             # algorithmic bytes per launch
+    # algorithmic bytes per launch (per-channel K: the seal of the pages the
+    # step fills runs inside the same timed interval, so its bytes count too)
+    b = (nb["append"] + (nb["seal"] if kchan else 0)) // w.layers
     t = k1_mean_ms * 1e-3
     return {"kernel": "fused into the decode launch (its whole time counted)" if fused
+            else "append_kernel + seal_kernel of the pages it fills" if kchan
             else "append_kernel (quantize-append)", "tokens_per_launch": T,
             "mean_launch_us": round(k1_mean_ms * 1e3, 3), "tokens_per_s": round(T / t, 1),
             "algorithmic_bytes_per_launch": b, "achieved_gbs": round(b / t / 1e9, 2),
@@ -300,6 +323,7 @@ class Bench:
         # (GQA <= 4 of INT8, FP8, asymmetric INT4)
         eligible = bool(np.all(self.n_new == 1)) and w.scheme in ("int8", "fp8", "int4") and \
             w.q_heads // w.kv_heads <= 4
+        self.kchan = w.scheme == "int8kc"
         self.fused = eligible and APPEND_MODE == "fused"
         B, P = len(self.seqs), w.page_size
         need = inp.pages_needed(self.lens, P)
@@ -318,14 +342,22 @@ class Bench:
         new_slots = np.concatenate([inp.slots(bt, i, np.arange(self.lens[i] - self.n_new[i], self.lens[i]), P)
                                     for i in range(B)])
         self.slots_new = torch.from_numpy(new_slots).to(dev)
+        if self.kchan:  # the new tokens' residual slots, and the pages the step fills
+            self.rslots_new = torch.from_numpy((new_slots // P).astype(np.int32)).to(dev)
+            full = np.array([bt[i, t // P] for i, L in enumerate(self.lens)
+                             for t in range(int(L - self.n_new[i]), int(L)) if t % P == P - 1], np.int32)
+            self.seal_new = torch.from_numpy(full).to(dev) if full.size else None
+            self.seal_all = []  # per layer: every page sealed by the prefill
         workers = min(16, os.cpu_count() or 1)
         with ThreadPoolExecutor(max_workers=workers) as ex:
             for layer in range(w.layers):
                 # the last host pages of the id space live in the cache's host
                 # tier (page-locked host memory read over NVLink-C2C)
                 host = min(int(round(HOST_FRACTION * num_pages)), num_pages - 1)
+                # per-channel K: one residual slot per page id (slot = page id)
                 c = kvq.PagedKVCache(w.scheme, num_pages - host, P, w.kv_heads, w.head_dim, device=dev,
-                                     zero_init=False, host_pages=host)
+                                     zero_init=False, host_pages=host,
+                                     resid_slots=num_pages if self.kchan else 0)
                 ks, vs = [], []
                 # the rows are generated on host threads, a bounded window ahead
                 pending = {}
@@ -345,11 +377,22 @@ class Bench:
                     for s0 in range(0, L - n, w.prefill_chunk):     # prefill (untimed)
                         s1 = min(L - n, s0 + w.prefill_chunk)
                         sl = inp.slots(bt, i, np.arange(s0, s1), P)
-                        kvq.append(c, torch.from_numpy(sl).to(dev), kd[s0:s1], vd[s0:s1])
+                        if self.kchan:
+                            kvq.append_kchan(c, torch.from_numpy(sl).to(dev),
+                                             torch.from_numpy((sl // P).astype(np.int32)).to(dev),
+                                             kd[s0:s1], vd[s0:s1])
+                        else:
+                            kvq.append(c, torch.from_numpy(sl).to(dev), kd[s0:s1], vd[s0:s1])
                     ks.append(kd[L - n:L].clone())
                     vs.append(vd[L - n:L].clone())
                 self.k_new.append(torch.cat(ks))
                 self.v_new.append(torch.cat(vs))
+                if self.kchan:  # seal every page the prefill filled
+                    pre = self.lens - self.n_new
+                    pg = np.concatenate([bt[i, :int(pre[i]) // P] for i in range(B)]).astype(np.int32)
+                    pgd = torch.from_numpy(pg).to(dev)
+                    kvq.seal_pages(c, pgd, pgd)
+                    self.seal_all.append(pgd)
                 self.caches.append(c)
                 self.q.append(torch.from_numpy(np.ascontiguousarray(inp.queries(w, layer)[self.seqs]).view(np.int16)).to(dev))
         self.out = torch.empty((B, w.q_heads, w.head_dim), dtype=torch.float32, device=dev)
@@ -361,6 +404,8 @@ class Bench:
         if st != kvq.OK:
             raise RuntimeError(f"set-up failed: {kvq.status_string(st)}")
         self.launches_per_step = 2 * w.layers  # quantize-append + fused decode per layer
+        if self.kchan and self.seal_new is not None:
+            self.launches_per_step += w.layers  # the seal of the pages the step fills
 
     def flush_l2(self):
         """Evict the step's data from L2: write a buffer larger than L2, then
@@ -370,7 +415,7 @@ class Bench:
         self.flush_sink = self.flush_read.sum()
 
     def step(self, events=None, q=None, k_new=None, v_new=None, slots=None, bt=None, lens=None, out=None,
-             stream=None):
+             stream=None, rslots=None, seal=None):
         kvq = self.kvq
         q = q or self.q
         k_new, v_new = k_new or self.k_new, v_new or self.v_new
@@ -381,7 +426,13 @@ class Bench:
         for layer, c in enumerate(self.caches):
             if events is not None:
                 events[layer][2].record()
-            if not self.fused:
+            if self.kchan:  # append (keeping the bf16 K rows), then seal the pages it filled
+                kvq.append_kchan(c, slots, self.rslots_new if rslots is None else rslots, k_new[layer],
+                                 v_new[layer], stream=stream)
+                sp = self.seal_new if seal is None else seal
+                if sp is not None:
+                    kvq.seal_pages(c, sp, sp, stream=stream)
+            elif not self.fused:
                 kvq.append(c, slots, k_new[layer], v_new[layer], stream=stream)
             if events is not None:
                 events[layer][0].record()
@@ -484,6 +535,8 @@ class Bench:
         tensors the calls take are views of its device twin."""
         torch = self.torch
         srcs = list(self.q) + list(self.k_new) + list(self.v_new) + [self.slots_new, self.bt, self.seq_lens]
+        if self.kchan:
+            srcs += [self.rslots_new] + ([self.seal_new] if self.seal_new is not None else [])
         offs, total = stage_layout(srcs)
         h_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
         d_buf = torch.empty(total, dtype=torch.uint8, device=self.dev)
@@ -492,14 +545,16 @@ class Bench:
         d_views = [stage_view(d_buf, t, off) for t, off in zip(srcs, offs)]
         nl = len(self.q)
         d_q, d_k, d_v = d_views[:nl], d_views[nl:2 * nl], d_views[2 * nl:3 * nl]
-        d_slots, d_bt, d_lens = d_views[3 * nl:]
+        d_slots, d_bt, d_lens = d_views[3 * nl:3 * nl + 3]
+        d_rs = d_views[3 * nl + 3] if self.kchan else None
+        d_seal = d_views[3 * nl + 4] if self.kchan and self.seal_new is not None else None
         h_out = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
         h2d = total
         d2h = h_out.numel() * 4
 
         def one():
             d_buf.copy_(h_buf, non_blocking=True)
-            self.step(q=d_q, k_new=d_k, v_new=d_v, slots=d_slots, bt=d_bt, lens=d_lens)
+            self.step(q=d_q, k_new=d_k, v_new=d_v, slots=d_slots, bt=d_bt, lens=d_lens, rslots=d_rs, seal=d_seal)
             h_out.copy_(self.out, non_blocking=True)
 
         for _ in range(warmup):
@@ -515,6 +570,27 @@ class Bench:
             evs[i][1].record()
         torch.cuda.synchronize(self.dev)
         return [a.elapsed_time(b) for a, b in evs], h2d, d2h
+
+    def seal_loop(self, seconds: float):
+        """Per-channel K: the seal of every page the prefill filled (layer 0),
+        one launch, each bracketed by CUDA events after an L2 flush, repeated
+        for `seconds`.  Returns (ms per launch, pages per launch)."""
+        torch = self.torch
+        E = torch.cuda.Event
+        pages = self.seal_all[0]
+        c = self.caches[0]
+        ms = []
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            evs = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(32)]
+            for a, b in evs:
+                self.flush_l2()
+                a.record()
+                self.kvq.seal_pages(c, pages, pages)
+                b.record()
+            torch.cuda.synchronize(self.dev)
+            ms += [a.elapsed_time(b) for a, b in evs]
+        return ms, int(pages.numel())
 
     def close(self):
         self.graph = None
@@ -576,6 +652,18 @@ def measure_workload(w, dev, local_rank, args, world, rank, barrier, headline: b
     ms_per_step = max_over_ranks(sum(timed), world, dev) / steps
     eager_per_step = max_over_ranks(sum(eager_ms), world, dev) / steps
     e2e_ms, h2d, d2h = bench.run_e2e(max(3, steps // 2), 3)
+    seal_rec = None
+    if bench.kchan:
+        s_ms, s_pages = bench.seal_loop(min(args.kernel_seconds, 0.5))
+        peak0, _ = measured_hbm_peak()
+        H, D, P = w.kv_heads, w.head_dim, w.page_size
+        sb = s_pages * (8 + H * (P * D * 2 + P * D + D * 2 + P * 4))
+        sm = statistics.mean(s_ms)
+        seal_rec = {"kernel": "seal_kernel (per-channel K re-quantization of full pages)",
+                    "pages_per_launch": s_pages, "kv_heads": H, "mean_launch_us": round(sm * 1e3, 3),
+                    "algorithmic_bytes_per_launch": sb, "achieved_gbs": round(sb / (sm * 1e-3) / 1e9, 2),
+                    "peak": peak0, "frac": round(sb / (sm * 1e-3) / 1e9 / peak0, 4),
+                    "what": "every page the prefill filled, re-sealed from its residual slot in one launch"}
     e2e_per_step = max_over_ranks(statistics.mean(e2e_ms), world, dev)
     st2 = bench.kvq.last_device_error()
     if status == bench.kvq.OK:
@@ -601,7 +689,9 @@ def measure_workload(w, dev, local_rank, args, world, rank, barrier, headline: b
         "append_tokens_per_s_step": round(total_append / (ms_per_step * 1e-3), 1),
         "algorithmic_bytes_per_step": total_step,
         "roofline": roofline_block(w, nb, k2_ms, peak, peak_kind, fused=bench.fused),
-        "append": append_line(nb, w, statistics.mean(k2_ms if bench.fused else k1_ms), peak, fused=bench.fused),
+        "append": append_line(nb, w, statistics.mean(k2_ms if bench.fused else k1_ms), peak, fused=bench.fused,
+                              kchan=bench.kchan),
+        **({"seal": seal_rec} if seal_rec is not None else {}),
         "kernel_loop": {"steps": loop_steps, "wall_s": round(loop_wall, 3),
                         "what": "eager steps, each launch bracketed by CUDA events; the clocks below are "
                                 "sampled across the timed steps and this loop"},
@@ -666,21 +756,31 @@ def _oracle_prepare(w, lens, n_new, seqs, layer):
     P = w.page_size
     sub = lens[seqs]
     bt, npg = inp.page_table(sub, P, w.seed + 99, spare=1)
-    c = oracle.OracleCache(w.scheme, npg, P, w.kv_heads, w.head_dim)
+    kc = w.scheme == "int8kc"  # per-channel K: residual slot = page id; full pages sealed
+    c = oracle.OracleCache(w.scheme, npg, P, w.kv_heads, w.head_dim, resid_slots=npg if kc else 0)
     new = []
     for i, b in enumerate(seqs):
         L, n = int(lens[b]), int(n_new[b])
         k, v = inp.kv_rows(w, layer, b, 0, L)
-        c.append(inp.slots(bt, i, np.arange(0, L - n), P), k[: L - n], v[: L - n])
-        new.append((inp.slots(bt, i, np.arange(L - n, L), P), k[L - n:], v[L - n:]))
+        sl = inp.slots(bt, i, np.arange(0, L - n), P)
+        c.append(sl, k[: L - n], v[: L - n], resid_slot=(sl // P).astype(np.int32) if kc else None)
+        if kc:
+            full = bt[i, :(L - n) // P].astype(np.int32)
+            c.seal(full, full)
+        sl = inp.slots(bt, i, np.arange(L - n, L), P)
+        fill = np.array([bt[i, t // P] for t in range(L - n, L) if t % P == P - 1], np.int32)
+        new.append((sl, k[L - n:], v[L - n:], fill))
     q = inp.queries(w, layer)[seqs]
     return c, bt, sub, new, q
 
 
 def _oracle_step(w, prepared):
     c, bt, sub, new, q = prepared
-    for slots, k, v in new:
-        c.append(slots, k, v)
+    kc = w.scheme == "int8kc"
+    for slots, k, v, fill in new:
+        c.append(slots, k, v, resid_slot=(slots // w.page_size).astype(np.int32) if kc else None)
+        if kc and fill.size:
+            c.seal(fill, fill)
     return c.decode_attn(q, bt, sub, w.q_heads)
 
 
@@ -691,7 +791,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=HEADLINE, choices=sorted(inp.WORKLOADS))
-    ap.add_argument("--sub", default="2,3,5",
+    ap.add_argument("--sub", default="2,3,5,6",
                     help="other workloads measured as sub-records of the line at N=1 ('' for none)")
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--kernel-seconds", type=float, default=1.0,

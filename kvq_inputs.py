@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the five workloads.
+"""Seeded synthetic inputs for the six workloads.
 
 This module holds NO quantization or attention arithmetic: it only draws
 random bf16 key/value/query tensors, sequence lengths and page tables.  Both
@@ -27,6 +27,10 @@ plainest choice is taken and stated here):
   5  long-128k-int8   1 layer, B=1, 131072 tokens, Hq 64 / Hkv 8, d 128,
                       page 16, N(0,1), INT8; split-K decode plus 4096-token
                       chunked appends.
+  6  llama3-8b-int8kc workload 2's shapes, lengths and rows (same seed) with
+                      per-channel K scales: every full page sealed, the open
+                      page of each sequence in per-token form; decode step +
+                      1-token append + the seal of the pages it fills.
 
 The queries are N(0,1) everywhere.  Every array is a pure function of
 (workload seed, layer, sequence), so a sampled check can regenerate exactly
@@ -76,6 +80,8 @@ WORKLOADS = {
                 ("lognormal", 4096, 1.0, 1024, 32768), seed=3, heavy_pairs=10, heavy_nu=4.0),
     4: Workload(4, "int4-g32-8layer", "int4", 8, 16, 32, 8, 128, 32, ("fixed", 32768), seed=4),
     5: Workload(5, "long-128k-int8", "int8", 1, 1, 64, 8, 128, 16, ("fixed", 131072), seed=5),
+    6: Workload(6, "llama3-8b-layer-int8kc", "int8kc", 1, 32, 32, 8, 128, 16, ("uniform", 512, 4096),
+                seed=2, outlier_pairs=10, outlier_gain=8.0),
 }
 
 
