@@ -513,6 +513,11 @@ class Bench:
         k2, k1, n = [], [], 0
         t0 = time.perf_counter()
         while True:
+            # the stream first idles (a device-side sleep of ~15 ms) while the
+            # host enqueues the batch, so that no launch waits on the host
+            # inside a bracketed interval (a step of short launches would
+            # otherwise time the host's launch latency, not the kernel)
+            torch.cuda._sleep(30_000_000)
             for i in range(batch):
                 self.flush_l2()
                 self.step(events=evs[i])

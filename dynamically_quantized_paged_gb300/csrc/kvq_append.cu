@@ -186,8 +186,8 @@ __global__ void __launch_bounds__(APPEND_THREADS, 2) append_kernel(AppendParams 
 // Inference", section "Understanding Dynamic Quantization Techniques"):
 // s_j = max_t |x| / 127, S = max_j s_j, factor r_j = fp16 round-up of
 // s_j / S, code = round-half-even(x / (r_j S)), every token scale S; each
-// step one correctly rounded IEEE operation.  Not on the decode's path (once
-// per filled page), so the quotients are plain IEEE divisions.
+// step one correctly rounded IEEE operation (the quotients through the token
+// rule's reciprocal with its exactness check, which gives the same codes).
 template <int D>
 __global__ void __launch_bounds__(D) seal_kernel(AppendParams p, const int32_t* pages, const int32_t* rslots) {
     const int i = blockIdx.x, h = blockIdx.y, j = threadIdx.x;
@@ -198,8 +198,16 @@ __global__ void __launch_bounds__(D) seal_kernel(AppendParams p, const int32_t* 
         return;
     }
     const uint16_t* x = p.k_resid + ((int64_t)rs * H + h) * P * D + j;
+    // this channel's values, 16 tokens at a time (page_size is a multiple of
+    // 16); the last 16 stay in registers for the codes below
+    float xs[16];
     float amax = 0.0f;
-    for (int t = 0; t < P; ++t) amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)x[(int64_t)t * D] << 16)));
+    for (int t0 = 0; t0 < P; t0 += 16) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xs[i] = __uint_as_float((uint32_t)x[(int64_t)(t0 + i) * D] << 16);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(xs[i]));
+    }
     const float sj = __fdiv_rn(amax, 127.0f);
     __shared__ float red[D / 32];
     float S = sj;
@@ -223,13 +231,20 @@ __global__ void __launch_bounds__(D) seal_kernel(AppendParams p, const int32_t* 
     }
     const __half r = __float2half_ru(__fdiv_rn(sj, S));
     const float e = __fmul_rn(__half2float(r), S);
-    for (int t = 0; t < P; ++t) {
-        int q = 0;
-        if (e != 0.0f) {
-            const float y = rintf(__fdiv_rn(__uint_as_float((uint32_t)x[(int64_t)t * D] << 16), e));
-            q = (int)fminf(fmaxf(y, -127.0f), 127.0f);
+    // round-half-even of fl(x / e), 16 tokens at a time (page_size is a
+    // multiple of 16; every lane of the warp takes part): the reciprocal with
+    // the exactness check of the token rule, since |x / e| <= 127 (1 + 2^-22)
+    const float re = approx_rcp(e);
+    for (int t0 = 0; t0 < P; t0 += 16) {
+        int q[16];
+        if (P > 16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) xs[i] = __uint_as_float((uint32_t)x[(int64_t)(t0 + i) * D] << 16);
         }
-        codes[(int64_t)t * D] = (int8_t)q;
+        rne_quotients<16>(xs, e, re, q);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)  // an all-zero channel (e = 0) has codes 0
+            codes[(int64_t)(t0 + i) * D] = (int8_t)(e != 0.0f ? min(max(q[i], -127), 127) : 0);
     }
     *chan = __half_as_ushort(r);
     for (int t = j; t < P; t += D) tok[t] = S;
