@@ -56,7 +56,7 @@ struct AppendCfg {
 };
 
 template <int SCHEME, int D>
-__global__ void __launch_bounds__(APPEND_THREADS, 2) append_kernel(AppendParams p) {
+__global__ void __launch_bounds__(APPEND_THREADS, 3) append_kernel(AppendParams p) {
     using C = AppendCfg<D>;
     constexpr int LPR = C::LPR;
     constexpr int PPW = C::PPW;
@@ -291,7 +291,7 @@ cudaError_t launch_append_t(AppendParams p, cudaStream_t s) {
     magic_divisor((uint32_t)p.num_kv_heads, &p.heads_mul, &p.heads_shift);
     magic_divisor((uint32_t)p.page_size, &p.page_mul, &p.page_shift);
     // as many CTAs as there are items for their warps (small appends are
-    // latency-bound), at most one wave of 2 resident CTAs per SM (then each
+    // latency-bound), at most one wave of 3 resident CTAs per SM (then each
     // warp loops over its items)
     using C = AppendCfg<D>;
     static std::atomic<int> configured[64];
@@ -302,12 +302,16 @@ cudaError_t launch_append_t(AppendParams p, cudaStream_t s) {
     if (!configured[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(append_kernel<SCHEME, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
+        // three resident CTAs need the largest shared-memory carveout
+        e = cudaFuncSetAttribute(append_kernel<SCHEME, D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
         configured[dev].store(1, std::memory_order_release);
     }
     const int64_t pairs = (int64_t)p.num_tokens * p.num_kv_heads;
     const int64_t items = (pairs + C::PPW - 1) / C::PPW;
     int64_t blocks = (items + C::WARPS - 1) / C::WARPS;
-    const int64_t cap = (int64_t)device_sm_count() * 2;
+    const int64_t cap = (int64_t)device_sm_count() * 3;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     append_kernel<SCHEME, D><<<(unsigned)blocks, APPEND_THREADS, C::SMEM, s>>>(p);

@@ -124,6 +124,27 @@ def test_kchan_append_seal_decode(D, G):
     assert np.all(got[0] == 0)
 
 
+def test_kchan_bf16_output_and_two_launch_form():
+    """The per-channel decode through the other output paths: bf16 rows equal
+    the fp32 rows rounded to nearest even, and the two-launch form
+    (partial, then merge) gives bitwise the one-launch output."""
+    w = _work(2, 8, 128, 16, seed=956, batch=len(RAGGED))
+    c = KcCase(w, RAGGED, steps=2)
+    ref32 = c.decode()
+    B, Hq, D = len(RAGGED), w.q_heads, w.head_dim
+    args = (dev_bits(c.q), dev(c.bt), dev(c.lens))
+    ws = kvq.alloc_workspace(c.g, B, Hq, c.bt.shape[1], device=DEV)
+    o16 = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=DEV)
+    kvq.decode_attn(c.g, *args, o16, ws)
+    o2 = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    kvq.decode_partial(c.g, *args, o2, ws)
+    kvq.decode_merge(c.g, *args, o2, ws)
+    assert kvq.last_device_error() == kvq.OK
+    want16 = torch.from_numpy(ref32.astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(o16.cpu().view(torch.int16), want16.view(torch.int16))
+    assert np.array_equal(o2.cpu().numpy().astype(np.float64), ref32)
+
+
 def test_kchan_page_32_and_host_tier():
     w = _work(2, 4, 128, 32, seed=951, batch=len(RAGGED))
     c = KcCase(w, RAGGED, steps=5, host_pages=6)
