@@ -39,18 +39,24 @@ __device__ __forceinline__ float approx_rcp(float s) {
 
 // INT8: the same rounding as rne_quotients, with each code left as the low
 // byte of t = RN(y + 1.5 * 2^23) (whose low mantissa bits hold the integer
-// RNE(y) for |y| < 2^22), packed four to a word.
+// RNE(y) for |y| < 2^22), packed four to a word.  Pairs of elements go through
+// the packed fp32 operations (each half one correctly rounded IEEE operation,
+// the same bits as the scalar ones): y = x r, t = y + M, and the rounding
+// residual y - (t - M), exact for |y| < 2^22.
 template <int N>
 __device__ __forceinline__ void rne_codes_s8(const float* x, float s, float r, uint32_t* wd) {
     constexpr float M = 12582912.0f;  // 1.5 * 2^23
     uint32_t t[N];
     float dmax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const float y = __fmul_rn(x[i], r);
-        const float tf = __fadd_rn(y, M);
-        t[i] = __float_as_uint(tf);
-        dmax = fmaxf(dmax, fabsf(__fsub_rn(y, __fsub_rn(tf, M))));
+    for (int i = 0; i < N; i += 2) {
+        const float2 y = __fmul2_rn(make_float2(x[i], x[i + 1]), make_float2(r, r));
+        const float2 tf = __fadd2_rn(y, make_float2(M, M));
+        const float2 back = __fadd2_rn(tf, make_float2(-M, -M));
+        const float2 d = __fadd2_rn(y, make_float2(-back.x, -back.y));
+        t[i] = __float_as_uint(tf.x);
+        t[i + 1] = __float_as_uint(tf.y);
+        dmax = fmaxf(dmax, fmaxf(fabsf(d.x), fabsf(d.y)));
     }
     const bool r_inf = !(r <= 0x1.fffffep127f);
     if (__any_sync(0xffffffffu, !(dmax < 0.5f - 0x1p-14f) || r_inf)) {
@@ -67,15 +73,22 @@ __device__ __forceinline__ void rne_codes_s8(const float* x, float s, float r, u
                             0x5410);
 }
 
+// The same rounding as integers: q_i = the bits of t = RN(y + 1.5 * 2^23)
+// less those of 1.5 * 2^23 (the two's-complement integer RNE(y) for
+// |y| < 2^22), by the packed operations as above.
 template <int N>
 __device__ __forceinline__ void rne_quotients(const float* x, float s, float r, int* q) {
+    constexpr float M = 12582912.0f;  // 1.5 * 2^23
     float dmax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const float y = __fmul_rn(x[i], r);
-        const float c = rintf(y);
-        q[i] = (int)c;
-        dmax = fmaxf(dmax, fabsf(__fsub_rn(y, c)));
+    for (int i = 0; i < N; i += 2) {
+        const float2 y = __fmul2_rn(make_float2(x[i], x[i + 1]), make_float2(r, r));
+        const float2 tf = __fadd2_rn(y, make_float2(M, M));
+        const float2 back = __fadd2_rn(tf, make_float2(-M, -M));
+        const float2 d = __fadd2_rn(y, make_float2(-back.x, -back.y));
+        q[i] = (int)(__float_as_uint(tf.x) - __float_as_uint(M));
+        q[i + 1] = (int)(__float_as_uint(tf.y) - __float_as_uint(M));
+        dmax = fmaxf(dmax, fmaxf(fabsf(d.x), fabsf(d.y)));
     }
     const bool r_inf = !(r <= 0x1.fffffep127f);
     if (__any_sync(0xffffffffu, !(dmax < 0.5f - 0x1p-14f) || r_inf)) {
