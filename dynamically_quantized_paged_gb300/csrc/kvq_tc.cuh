@@ -805,7 +805,9 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                                 for (int k = 0; k < 4; ++k) {
                                     const __half2 x = *reinterpret_cast<const __half2*>(&r[cc * 8 + h2 * 4 + k]);
                                     const __half2 fk = *reinterpret_cast<const __half2*>(&fw[k]);
-                                    const __half2 hi = __hmul2(x, fk);
+                                    // hi rounded on its own (__hmul2_rn: never contracted
+                                    // into the fma below, which would make lo 0)
+                                    const __half2 hi = __hmul2_rn(x, fk);
                                     const __half2 lo = __hfma2(x, fk, __hneg2(hi));
                                     r[cc * 8 + h2 * 4 + k] = *reinterpret_cast<const uint32_t*>(&hi);
                                     rlo[cc * 8 + h2 * 4 + k] = *reinterpret_cast<const uint32_t*>(&lo);
@@ -875,7 +877,12 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     float v;
-                    if constexpr (C::INT8) {
+                    if constexpr (C::KCH) {
+                        // the sums carry fractions (codes times factors): recombined
+                        // in fp32, not through integers
+                        const float sh = fmaf(__uint_as_float(sr[g]), 256.0f, __uint_as_float(sr[G + g]));
+                        v = sh * (psc[g] * ks_c[0]);
+                    } else if constexpr (C::INT8) {
                         const int ai = (int)__uint_as_float(sr[g]) * 256 + (int)__uint_as_float(sr[G + g]);
                         v = (float)ai * (psc[g] * ks_c[0]);
                     } else if constexpr (C::FP8) {
