@@ -218,3 +218,51 @@ def test_kchan_bad_ids_flagged_and_skipped():
         ws = kvq.alloc_workspace(c.g, 1, 4, c.bt.shape[1], device=DEV)
         kvq.decode_attn_append(c.g, k[0:1], k[0:1], dev_bits(c.q), dev(c.bt), dev(c.lens), out, ws)
     assert e.value.status == 7  # KVQ_ERR_UNSUPPORTED
+
+
+def test_kchan_step_replayed_from_a_cuda_graph():
+    """A per-channel decode step (append of each sequence's token keeping its
+    K rows, the seal of the pages it fills, the decode) recorded in a CUDA
+    graph and replayed gives the eager step's pools and output bit for bit."""
+    lens = np.array([31, 48, 17, 64], np.int32)  # tokens 31, 47 and 63 fill pages
+    w = _work(2, 4, 128, 16, seed=957, batch=len(lens))
+    c = KcCase(w, lens, steps=1)
+    P = w.page_size
+    # the step's token of each sequence again (same bytes), its slot, its page's slot
+    k_new = np.concatenate([c.rows[b][0][L - 1:L] for b, L in enumerate(lens)])
+    v_new = np.concatenate([c.rows[b][1][L - 1:L] for b, L in enumerate(lens)])
+    sl = np.concatenate([inp.slots(c.bt, b, np.array([L - 1]), P) for b, L in enumerate(lens)])
+    rs = np.array([c.page_slot(b, (L - 1) // P) for b, L in enumerate(lens)], np.int32)
+    fill = [(b, (L - 1) // P) for b, L in enumerate(lens) if (L - 1) % P == P - 1]
+    pg = np.array([c.bt[b, i] for b, i in fill], np.int32)
+    ps = np.array([c.page_slot(b, i) for b, i in fill], np.int32)
+    dk, dv, dsl, drs, dpg, dps = (dev_bits(k_new), dev_bits(v_new), dev(sl), dev(rs), dev(pg), dev(ps))
+    dq, dbt, dlen = dev_bits(c.q), dev(c.bt), dev(c.lens)
+    B, Hq, D = len(lens), w.q_heads, w.head_dim
+    ws = kvq.alloc_workspace(c.g, B, Hq, c.bt.shape[1], device=DEV)
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+
+    def step(stream=None):
+        kvq.append_kchan(c.g, dsl, drs, dk, dv, stream=stream)
+        kvq.seal_pages(c.g, dpg, dps, stream=stream)
+        kvq.decode_attn(c.g, dq, dbt, dlen, out, ws, stream=stream)
+
+    step()
+    torch.cuda.synchronize()
+    eager = out.cpu().numpy().copy()
+    pools = {n: c.g.pool(n).copy() for n in ("k_codes", "v_codes", "k_scales", "v_scales", "k_chan")}
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step(stream=s)
+    out.fill_(float("nan"))
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert kvq.last_device_error() == kvq.OK
+    assert np.array_equal(out.cpu().numpy(), eager)
+    for n, a in pools.items():
+        assert np.array_equal(c.g.pool(n), a), n
+    c.compare_pools()
+    assert_attn_close(eager.astype(np.float64), c.o.decode_attn(c.q, c.bt, c.lens, Hq), "int8kc graph step")
