@@ -33,7 +33,7 @@ EXPORTS = ["kvq_status_string", "kvq_cache_bytes", "kvq_append", "kvq_decode_wor
            "kvq_last_device_error", "kvq_allocator_create", "kvq_allocator_destroy",
            "kvq_alloc_pages", "kvq_free_pages", "kvq_allocator_free_count", "kvq_decode_attn_noalloc",
            "kvq_share_pages", "kvq_page_refcount", "kvq_copy_page", "kvq_decode_attn_out",
-           "kvq_decode_attn_append", "kvq_kchan_bytes", "kvq_append_kchan", "kvq_seal_pages"]
+           "kvq_decode_attn_append", "kvq_kchan_bytes", "kvq_append_kchan", "kvq_seal_pages", "kvq_copy_pages"]
 
 
 class KvqError(RuntimeError):
@@ -90,6 +90,7 @@ def _load() -> ctypes.CDLL:
     L.kvq_kchan_bytes.argtypes = [i32, i32, i32, i32, i32, sz, sz]
     L.kvq_append_kchan.argtypes = [cachep, P, i32, i32, i64p, P, P, P, i32, P]
     L.kvq_seal_pages.argtypes = [cachep, P, P, i32, P]
+    L.kvq_copy_pages.argtypes = [cachep, P, P, i32, P]
     for name in EXPORTS:
         getattr(L, name)  # every declared entry point must be exported
     return L
@@ -221,6 +222,16 @@ def copy_page(cache: PagedKVCache, src: int, dst: int, stream=None) -> None:
     """kvq_copy_page: copy page src into page dst (every pool), within a tier
     (copy-on-write) or between the device and host tiers (offload, fetch)."""
     _check(lib.kvq_copy_page(ctypes.byref(cache.struct), src, dst, _stream(stream)), "kvq_copy_page")
+
+
+def copy_pages(cache: PagedKVCache, src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
+    """kvq_copy_pages: copy every pool of page src[i] into page dst[i] (int32
+    [n] device arrays; either tier), one launch for the whole batch."""
+    n = src.numel()
+    if dst.numel() != n or src.element_size() != 4 or dst.element_size() != 4:
+        raise ValueError("kvq_copy_pages: src and dst must be int32 [n]")
+    _check(lib.kvq_copy_pages(ctypes.byref(cache.struct), _ptr(src), _ptr(dst), n, _stream(stream)),
+           "kvq_copy_pages")
 
 
 def append(cache: PagedKVCache, slot_mapping: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -574,6 +574,46 @@ kvq_status kvq_copy_page(const kvq_cache* cache, int32_t src, int32_t dst, kvq_s
     return KVQ_OK;
 }
 
+kvq_status kvq_copy_pages(const kvq_cache* cache, const int32_t* src, const int32_t* dst, int32_t n,
+                          kvq_stream_t stream) {
+    kvq_status st = check_cache(cache);
+    if (st != KVQ_OK) return st;
+    if (n < 0) return KVQ_ERR_INVALID_ARG;
+    if (n == 0) return KVQ_OK;
+    if (!src || !dst || !aligned(src, 4) || !aligned(dst, 4)) return KVQ_ERR_INVALID_ARG;
+    unsigned* err = kvq::device_error_word();
+    if (!err) return KVQ_ERR_CUDA;
+    // the same per-page pool sizes as kvq_copy_page
+    const int64_t rows = (int64_t)cache->num_kv_heads * cache->page_size;
+    const bool int4 = cache->scheme == KVQ_INT4_ASYM_G32, int4s = cache->scheme == KVQ_INT4_SYM_G32;
+    const bool kc = cache->scheme == KVQ_INT8_KCHAN, ht = cache->host_pages > 0;
+    const int64_t code_b = rows * (int4 || int4s ? cache->head_dim / 2 : cache->head_dim);
+    const int64_t meta_b = rows * (int4 ? (cache->head_dim / 32) * 2 : int4s ? (cache->head_dim / 32) * 4 : 4);
+    kvq::PageCopyParams p;
+    void* const dev_tier[7] = {cache->k_codes, cache->v_codes, cache->k_scales, cache->v_scales,
+                               int4 ? cache->k_zeros : nullptr, int4 ? cache->v_zeros : nullptr,
+                               kc ? cache->k_chan : nullptr};
+    void* const host_tier[7] = {cache->host_k_codes, cache->host_v_codes, cache->host_k_scales,
+                                cache->host_v_scales, int4 ? cache->host_k_zeros : nullptr,
+                                int4 ? cache->host_v_zeros : nullptr, kc ? cache->host_k_chan : nullptr};
+    const int64_t bytes[7] = {code_b, code_b, meta_b, meta_b, meta_b, meta_b,
+                              (int64_t)cache->num_kv_heads * cache->head_dim * 2};
+    for (int k = 0; k < 7; ++k) {
+        p.base[k][0] = static_cast<uint8_t*>(dev_tier[k]);
+        // with no host tier every id is a device page: the host column is never chosen
+        p.base[k][1] = ht ? static_cast<uint8_t*>(host_tier[k]) : static_cast<uint8_t*>(dev_tier[k]);
+        p.bytes[k] = bytes[k];
+    }
+    p.num_pages = cache->num_pages;
+    p.total_pages = cache->num_pages + cache->host_pages;
+    p.src = src;
+    p.dst = dst;
+    p.n = n;
+    p.err = err;
+    if (kvq::launch_copy_pages(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
 kvq_status kvq_last_device_error(kvq_stream_t stream) {
     if (current_device() < 0) return KVQ_ERR_CUDA;
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;

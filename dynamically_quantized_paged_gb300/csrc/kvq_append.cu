@@ -250,6 +250,44 @@ __global__ void __launch_bounds__(D) seal_kernel(AppendParams p, const int32_t* 
     for (int t = j; t < P; t += D) tok[t] = S;
 }
 
+// Batched page copies: CTA-strided over the pairs; every pool of page src[i]
+// to page dst[i], 16-byte words, four loads in flight per thread before
+// their stores (a host-tier page is read over NVLink-C2C, whose latency the
+// loads in flight cover).
+__global__ void __launch_bounds__(256) copy_pages_kernel(PageCopyParams p) {
+    for (int i = blockIdx.x; i < p.n; i += gridDim.x) {
+        const int s = p.src[i], d = p.dst[i];
+        if (s < 0 || s >= p.total_pages || d < 0 || d >= p.total_pages || s == d) {
+            if (threadIdx.x == 0) flag_error(p.err, ERR_BAD_TABLE);
+            continue;
+        }
+        const int ts = s >= p.num_pages, td = d >= p.num_pages;
+        const int64_t is = s - (ts ? p.num_pages : 0), id = d - (td ? p.num_pages : 0);
+#pragma unroll 1
+        for (int k = 0; k < 7; ++k) {
+            const uint8_t* from = p.base[k][ts];
+            uint8_t* to = p.base[k][td];
+            if (!from || !to) continue;
+            const int64_t words = p.bytes[k] / 16;
+            const uint4* f = reinterpret_cast<const uint4*>(from + is * p.bytes[k]);
+            uint4* t = reinterpret_cast<uint4*>(to + id * p.bytes[k]);
+            for (int64_t j0 = threadIdx.x; j0 < words; j0 += 4 * (int64_t)blockDim.x) {
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t j = j0 + u * (int64_t)blockDim.x;
+                    if (j < words) v[u] = f[j];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t j = j0 + u * (int64_t)blockDim.x;
+                    if (j < words) t[j] = v[u];
+                }
+            }
+        }
+    }
+}
+
 // K4: every page a sequence uses must lie in the pool, and the sequence must
 // fit its table row.  Without seq_lens, every entry must be -1 or in the pool.
 __global__ void validate_kernel(int num_pages, int page_size, const int32_t* block_table,
@@ -340,6 +378,15 @@ cudaError_t launch_seal(const AppendParams& p, int head_dim, const int32_t* page
     const dim3 grid((unsigned)n, (unsigned)p.num_kv_heads);
     if (head_dim == 128) seal_kernel<128><<<grid, 128, 0, s>>>(p, pages, rslots);
     else seal_kernel<64><<<grid, 64, 0, s>>>(p, pages, rslots);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_pages(const PageCopyParams& p, cudaStream_t s) {
+    int64_t blocks = p.n;
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    copy_pages_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -167,6 +167,20 @@ inline size_t decode_workspace_bytes(int n_ctas, int G, int D, int B, int Hkv, i
            2 * slots * G * sizeof(float);
 }
 
+// Batched page copies (kvq_copy_pages): pool k of tier t (0 device, 1 host)
+// starts at base[k][t] (null: the scheme has no such pool) and holds bytes[k]
+// bytes per page (a multiple of 16); page id >= num_pages is host-tier.
+struct PageCopyParams {
+    uint8_t* base[7][2];
+    int64_t bytes[7];
+    int num_pages, total_pages;
+    const int32_t* src;
+    const int32_t* dst;
+    int n;
+    unsigned* err;
+};
+cudaError_t launch_copy_pages(const PageCopyParams& p, cudaStream_t s);
+
 cudaError_t launch_append(const AppendParams& p, int scheme, int head_dim, cudaStream_t s);
 // Per-channel K: seals pages[i] from residual slot rslots[i], i < n.
 cudaError_t launch_seal(const AppendParams& p, int head_dim, const int32_t* pages, const int32_t* rslots, int n,

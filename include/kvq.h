@@ -426,6 +426,20 @@ int32_t kvq_allocator_free_count(const kvq_allocator* alloc);
  * tiers or src == dst; KVQ_ERR_CUDA if a copy cannot be enqueued. */
 kvq_status kvq_copy_page(const kvq_cache* cache, int32_t src, int32_t dst, kvq_stream_t stream);
 
+/* kvq_copy_page for many pages in one launch: for each i < n, every pool's
+ * contents of page src[i] are copied to page dst[i] (either tier: a batch of
+ * offloads, fetches or copy-on-write copies; [P3] "KV Cache Offloading":
+ * pages moved back when needed).  One kernel, 16-byte loads and stores; a
+ * host-tier page is read or written in place over NVLink-C2C.
+ *   src, dst  device, int32 [n].  The pairs must not overlap (no page is both
+ *             a source and a destination, no destination twice); their
+ *             order is unspecified.  A pair with an id outside both tiers,
+ *             or src[i] == dst[i], is skipped and flagged KVQ_ERR_BAD_TABLE.
+ * n == 0 launches nothing; KVQ_ERR_INVALID_ARG if n < 0 or an array is NULL
+ * or not 4-byte aligned. */
+kvq_status kvq_copy_pages(const kvq_cache* cache, const int32_t* src, const int32_t* dst, int32_t n,
+                          kvq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

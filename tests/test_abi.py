@@ -208,6 +208,16 @@ def test_cache_struct_layout_matches_the_header():
     assert ctypes.sizeof(kvq.CacheStruct) == 160
 
 
+def test_batched_page_copy_argument_errors_before_any_device_access():
+    c = fake_cache(num_pages=4, host_pages=3)
+    L = kvq.lib
+    assert L.kvq_copy_pages(ctypes.byref(c), None, None, 0, None) == 0     # nothing to do
+    assert L.kvq_copy_pages(ctypes.byref(c), None, None, -1, None) == 1
+    assert L.kvq_copy_pages(ctypes.byref(c), None, 1 << 20, 2, None) == 1
+    assert L.kvq_copy_pages(ctypes.byref(c), 1 << 20, (1 << 20) + 2, 2, None) == 1  # misaligned
+    assert L.kvq_copy_pages(None, 1 << 20, 1 << 21, 2, None) == 1
+
+
 def test_kchan_sizes_and_argument_errors_before_any_device_access():
     """The per-channel K scheme's pools, its append, seal and the refusal of
     the fused decode-append: every rule of the header checked on the host."""

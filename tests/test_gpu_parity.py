@@ -540,6 +540,59 @@ def test_pages_offloaded_to_the_host_tier_and_fetched_back(scheme):
         assert hp.any() and np.array_equal(hp, dp), name
 
 
+@pytest.mark.parametrize("scheme", ["int8", "int4", "int8kc"])
+def test_batched_page_copies_across_tiers(scheme):
+    """kvq_copy_pages moves a batch of pages in one launch: device pages to
+    free host-tier pages, host pages to free device pages and a device page
+    to another (copy-on-write), every pool byte for byte as the pools' host
+    copies predict; a pair naming a page outside both tiers is flagged and
+    skipped.  The decode is bit-identical through the moved pages."""
+    if scheme == "int8kc":
+        from test_gpu_kchan import KcCase, _work
+        w = _work(8, 4, 128, 16, seed=961, batch=2)
+        c = KcCase(w, [1000, 300], host_pages=20, spare=40)
+    else:
+        w = small(scheme, 32, 8, 128, 16)
+        c = Case(w, np.array([1000, 300], np.int32), spare=40, host_pages=20, extra_host_pages=20)
+    ref = c.decode()
+    total = c.g.num_pages + c.g.host_pages
+    used = set(c.bt[c.bt >= 0].tolist())
+    free_dev = [x for x in range(c.g.num_pages) if x not in used]
+    free_host = [x for x in range(c.g.num_pages, total) if x not in used]
+    dev_used = [x for x in c.bt[0] if 0 <= x < c.g.num_pages][:8]
+    host_used = [x for x in c.bt.reshape(-1) if x >= c.g.num_pages][:4]
+    assert len(dev_used) == 8 and len(host_used) >= 2
+    pairs = [(int(a), int(b)) for a, b in zip(dev_used[:5], free_host)]                 # offload
+    pairs += [(int(a), int(b)) for a, b in zip(host_used, free_dev[:len(host_used)])]    # fetch
+    pairs += [(int(dev_used[5]), int(free_dev[len(host_used)]))]                         # copy-on-write
+    names = ["k_codes", "v_codes", "k_scales", "v_scales"] + (["k_zeros", "v_zeros"] if scheme == "int4" else []) + \
+        (["k_chan"] if scheme == "int8kc" else [])
+    before = {n: c.g.pool(n).reshape(total, -1).copy() for n in names}
+    src = np.array([a for a, _ in pairs] + [total + 5], np.int32)
+    dst = np.array([b for _, b in pairs] + [free_dev[-1]], np.int32)
+    kvq.copy_pages(c.g, dev(src), dev(dst))
+    torch.cuda.synchronize()
+    assert kvq.last_device_error() == 4  # KVQ_ERR_BAD_TABLE: the pair outside both tiers
+    for n in names:
+        want = before[n].copy()
+        for a, b in pairs:
+            want[b] = before[n][a]
+        assert np.array_equal(c.g.pool(n).reshape(total, -1), want), n
+    bt2 = c.bt.copy()
+    for a, b in pairs:
+        bt2[c.bt == a] = b
+    assert np.array_equal(c.decode(bt=bt2) if scheme == "int8kc" else _decode_with(c, bt2), ref)
+
+
+def _decode_with(c, bt):
+    saved = c.bt
+    c.bt = bt
+    try:
+        return c.decode()
+    finally:
+        c.bt = saved
+
+
 # --------------------------------------------------- decode that appends its token
 @pytest.mark.parametrize("scheme,Hq,D,P", [("int8", 32, 128, 16), ("int8", 8, 64, 32), ("fp8", 16, 128, 16),
                                            ("int4", 32, 128, 32), ("int4", 16, 64, 16), ("int8", 64, 128, 16),
