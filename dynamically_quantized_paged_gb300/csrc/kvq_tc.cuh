@@ -776,7 +776,10 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
             // widen the K row into tensor memory, 16 columns at a time
             const uint32_t ta = tl + C::TM_K + (j & 1) * C::KCOL;
             constexpr int CPS = C::INT4 ? 1 : 2;  // raw 16-byte chunks per 16 columns
-#pragma unroll
+            // kept rolled (as the V widening below): the kernel's four roles
+            // run different code, and the smaller body costs fewer
+            // instruction-cache misses than the unrolled one saves
+#pragma unroll 1
             for (int c0 = 0; c0 < C::NCH; c0 += CPS) {
                 uint32_t r[16];
                 uint32_t rlo[C::KCH ? 16 : 1];  // KCH: the low parts
@@ -1050,7 +1053,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
             const int uu = ct / UNIT;
             const bool valid = uu < nu && !((badm >> uu) & 1u) && (it.u0 + uu) * UNIT + (ct % UNIT) < it.pc.len;
             uint8_t* vs = smem + C::OFF_VS + (j & 1) * C::VS_BYTES + (ct / 8) * 128 + (ct % 8) * 16;
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < C::NCH; ++c) {
                 const uint4 raw = *reinterpret_cast<const uint4*>(st + C::RV + 16 * swz(ct * C::NCH + c));
                 const uint32_t w4[4] = {raw.x ^ C::NIBX, raw.y ^ C::NIBX, raw.z ^ C::NIBX, raw.w ^ C::NIBX};
