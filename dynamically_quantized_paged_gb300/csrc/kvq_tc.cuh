@@ -1053,6 +1053,11 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
             const int uu = ct / UNIT;
             const bool valid = uu < nu && !((badm >> uu) & 1u) && (it.u0 + uu) * UNIT + (ct % UNIT) < it.pc.len;
             uint8_t* vs = smem + C::OFF_VS + (j & 1) * C::VS_BYTES + (ct / 8) * 128 + (ct % 8) * 16;
+            // the row of a token past the piece (or of a page outside the
+            // pool) needs no zeroing where every widened code is finite (INT8,
+            // both INT4): its weight is exactly 0.  E4M3 stale bytes can be
+            // NaN codes, so FP8 rows are zeroed.
+            const bool keep = valid || !C::FP8;
 #pragma unroll 1
             for (int c = 0; c < C::NCH; ++c) {
                 const uint4 raw = *reinterpret_cast<const uint4*>(st + C::RV + 16 * swz(ct * C::NCH + c));
@@ -1071,7 +1076,7 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                         }
                         const int blk = c * 4 + k;
                         *reinterpret_cast<uint4*>(vs + blk * C::VS_SBO) =
-                            valid ? make_uint4(h[0], h[1], h[2], h[3]) : make_uint4(0u, 0u, 0u, 0u);
+                            keep ? make_uint4(h[0], h[1], h[2], h[3]) : make_uint4(0u, 0u, 0u, 0u);
                     }
                 } else {
                     uint32_t h[8];
@@ -1085,9 +1090,9 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
                         }
                     }
                     *reinterpret_cast<uint4*>(vs + (2 * c) * C::VS_SBO) =
-                        valid ? make_uint4(h[0], h[1], h[2], h[3]) : make_uint4(0u, 0u, 0u, 0u);
+                        keep ? make_uint4(h[0], h[1], h[2], h[3]) : make_uint4(0u, 0u, 0u, 0u);
                     *reinterpret_cast<uint4*>(vs + (2 * c + 1) * C::VS_SBO) =
-                        valid ? make_uint4(h[4], h[5], h[6], h[7]) : make_uint4(0u, 0u, 0u, 0u);
+                        keep ? make_uint4(h[4], h[5], h[6], h[7]) : make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             fence_proxy_async_smem();
