@@ -778,8 +778,10 @@ __global__ void __launch_bounds__(Cfg<SCHEME, D, G>::THREADS, 1) decode_tc_kerne
             constexpr int CPS = C::INT4 ? 1 : 2;  // raw 16-byte chunks per 16 columns
             // kept rolled (as the V widening below): the kernel's four roles
             // run different code, and the smaller body costs fewer
-            // instruction-cache misses than the unrolled one saves
-#pragma unroll 1
+            // instruction-cache misses than the unrolled one saves (FP8,
+            // whose conversions are longer, measured best at two per pass)
+            constexpr int KUNR = C::FP8 ? 2 : 1;
+#pragma unroll KUNR
             for (int c0 = 0; c0 < C::NCH; c0 += CPS) {
                 uint32_t r[16];
                 uint32_t rlo[C::KCH ? 16 : 1];  // KCH: the low parts
