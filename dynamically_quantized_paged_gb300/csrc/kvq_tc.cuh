@@ -288,7 +288,9 @@ struct Cfg {
                                  : TM_USED <= 256 ? 256 : 512;
     static_assert(TM_USED <= 512, "tensor memory");
     // threads: token group 0-3, channel group 4-7, NPW producer warps, the MMA warp
-    static constexpr int NPW = 3;
+    // producer warps (measured: INT8 and per-channel K gain from a fourth,
+    // FP8 loses with it; symmetric INT4 stays at three for registers)
+    static constexpr int NPW = INT8 ? 4 : 3;
     static constexpr int PR_WARP0 = 8, MM_WARP = PR_WARP0 + NPW;
     static constexpr int THREADS = 32 * (MM_WARP + 1);
     // one raw stage (bytes)
