@@ -49,6 +49,7 @@ PROBLEMS = [
     ("fp8", 64, 8, [9000, 0, 40], 12),
     ("int4", 16, 4, [1, 12000, 0, 700, 5000, 33, 2048], 13),
     ("int8", 16, 8, [25000, 0], 14),
+    ("int8kc", 32, 8, [6000, 0, 900], 15),  # per-channel K (pages open: token rule, factors 1.0)
 ]
 
 
