@@ -266,3 +266,38 @@ def test_kchan_step_replayed_from_a_cuda_graph():
         assert np.array_equal(c.g.pool(n), a), n
     c.compare_pools()
     assert_attn_close(eager.astype(np.float64), c.o.decode_attn(c.q, c.bt, c.lens, Hq), "int8kc graph step")
+
+
+def test_kchan_page_48():
+    """A page size that is a multiple of 16 but not a power of two: the seal
+    walks its page in three 16-token chunks."""
+    lens = [47, 48, 49, 100, 5]
+    w = _work(2, 2, 64, 48, seed=958, batch=len(lens))
+    c = KcCase(w, lens, steps=2)
+    assert c.sealed >= 4
+    c.compare_pools()
+    assert_attn_close(c.decode(), c.o.decode_attn(c.q, c.bt, c.lens, w.q_heads), "int8kc page 48")
+
+
+def test_kchan_sealed_page_reopened():
+    """A sealed page that is freed and reused: the token appended at its
+    offset 0 sets its channel factors back to 1.0 (every head) and takes the
+    token rule; the pools match the oracle, which does the same."""
+    lens = [32]
+    w = _work(2, 4, 128, 16, seed=959, batch=1)
+    c = KcCase(w, lens, spare=2)
+    page = int(c.bt[0, 0])
+    chan_before = c.g.pool("k_chan").view(np.uint16).reshape(-1, 2, 128)[page].copy()
+    assert np.any(chan_before != 0x3C00)     # sealed: factors other than 1.0
+    r = np.random.default_rng(5)
+    k = inp.to_bf16_bits(r.standard_normal((1, 2, 128)).astype(np.float32))
+    v = inp.to_bf16_bits(r.standard_normal((1, 2, 128)).astype(np.float32))
+    sl = np.array([page * 16], np.int64)
+    rs = np.array([c.page_slot(0, 0)], np.int32)
+    kvq.append_kchan(c.g, dev(sl), dev(rs), dev_bits(k), dev_bits(v))
+    assert c.o.append(sl, k, v, resid_slot=rs) == 0
+    torch.cuda.synchronize()
+    assert kvq.last_device_error() == kvq.OK
+    chan = c.g.pool("k_chan").view(np.uint16).reshape(-1, 2, 128)[page]
+    assert np.all(chan == 0x3C00)
+    c.compare_pools()
