@@ -56,8 +56,8 @@ def outlier_block(r, P=16, D=128, n_out=4, gain=40.0):
 # ------------------------------------------------------------- the page rule ----
 def test_kchan_page_matches_torch_restatement():
     r = np.random.default_rng(71)
-    for trial in range(200):
-        P = [16, 32][trial % 2]
+    for trial in range(240):
+        P = [16, 32, 48][trial % 3]
         D = [64, 128][(trial // 2) % 2]
         mag = r.choice([1e-3, 1.0, 50.0])
         xb = outlier_block(r, P, D, n_out=int(r.integers(0, 6)), gain=float(r.choice([1.0, 8.0, 60.0])))
