@@ -540,7 +540,7 @@ def test_pages_offloaded_to_the_host_tier_and_fetched_back(scheme):
         assert hp.any() and np.array_equal(hp, dp), name
 
 
-@pytest.mark.parametrize("scheme", ["int8", "int4", "int8kc"])
+@pytest.mark.parametrize("scheme", ["int8", "fp8", "int4", "int4sym", "int8kc"])
 def test_batched_page_copies_across_tiers(scheme):
     """kvq_copy_pages moves a batch of pages in one launch: device pages to
     free host-tier pages, host pages to free device pages and a device page
